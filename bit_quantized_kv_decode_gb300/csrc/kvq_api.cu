@@ -1,0 +1,239 @@
+// C-ABI entry points: argument validation, workspace layout and dispatch.
+// Nothing here allocates memory; every launch goes to the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kMaxBatchDecode = 1024;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int block_bytes(int bits) { return kBlockTokens * kHeadDim * bits / 8; }
+
+kvq_status check_cache(const kvq_cache_desc* c) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (c->bits != 2 && c->bits != 4) return KVQ_ERR_UNSUPPORTED;
+  if ((c->k_scheme != KVQ_TOKENWISE && c->k_scheme != KVQ_CHANNELWISE) ||
+      (c->v_scheme != KVQ_TOKENWISE && c->v_scheme != KVQ_CHANNELWISE))
+    return KVQ_ERR_INVALID_ARG;
+  if (c->head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  if (c->num_kv_heads < 1 || c->num_pages < 1) return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+// Checks the current device without launching anything.
+kvq_status check_device(int* sm_count) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return KVQ_ERR_DEVICE; }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_ERR_DEVICE;
+  }
+  if (major != 10 || minor != 3) return KVQ_ERR_DEVICE;
+  if (sm_count != nullptr &&
+      cudaDeviceGetAttribute(sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_ERR_DEVICE;
+  }
+  return KVQ_OK;
+}
+
+struct WorkspaceLayout {
+  size_t counters, part_lse, part_o, total;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+WorkspaceLayout workspace_layout(int batch, int kv_heads, int num_ctas) {
+  WorkspaceLayout w;
+  w.counters = 0;
+  w.part_lse = round_up((size_t)batch * kv_heads * sizeof(int), 256);
+  w.part_o = w.part_lse + round_up((size_t)num_ctas * 2 * kGroupQ * sizeof(float), 256);
+  w.total = w.part_o + round_up((size_t)num_ctas * 2 * kGroupQ * kHeadDim * sizeof(float), 256);
+  return w;
+}
+
+kvq_status check_attn(const kvq_attn_desc* d) {
+  if (d == nullptr) return KVQ_ERR_INVALID_ARG;
+  kvq_status s = check_cache(&d->cache);
+  if (s != KVQ_OK) return s;
+  if (d->batch < 1 || d->max_blocks < 1 || d->num_q_heads < 1) return KVQ_ERR_INVALID_ARG;
+  if (d->batch > kMaxBatchDecode) return KVQ_ERR_UNSUPPORTED;
+  if (d->num_q_heads != kGroupQ * d->cache.num_kv_heads) return KVQ_ERR_UNSUPPORTED;
+  if (d->operand_mode != KVQ_OPERANDS_FP8 && d->operand_mode != KVQ_OPERANDS_BF16) return KVQ_ERR_INVALID_ARG;
+  if (d->num_ctas < 0 || (d->flags & ~KVQ_FLAG_TEST_STALL) != 0) return KVQ_ERR_INVALID_ARG;
+  if (!(std::isfinite(d->sm_scale))) return KVQ_ERR_INVALID_ARG;
+  if ((long long)d->batch * d->cache.num_kv_heads * d->max_blocks > (1LL << 30)) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+int resolve_ctas(const kvq_attn_desc* d, int sm_count) {
+  long long want = d->num_ctas > 0 ? d->num_ctas : (long long)decode_ctas_per_sm() * sm_count;
+  long long tiles_bound = (long long)d->batch * d->cache.num_kv_heads * d->max_blocks;
+  if (want > tiles_bound) want = tiles_bound;
+  return (int)(want < 1 ? 1 : want);
+}
+
+}  // namespace
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+KVQ_API const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_WORKSPACE: return "workspace too small";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_DEVICE: return "no sm_103 device";
+  }
+  return "unknown status";
+}
+
+KVQ_API int32_t kvq_version(void) { return 100; }
+
+KVQ_API kvq_status kvq_cache_bytes(const kvq_cache_desc* cache, size_t* codes_bytes, size_t* scale_bytes) {
+  kvq_status s = check_cache(cache);
+  if (s != KVQ_OK) return s;
+  if (codes_bytes == nullptr || scale_bytes == nullptr) return KVQ_ERR_INVALID_ARG;
+  const size_t blocks = (size_t)cache->num_pages * cache->num_kv_heads;
+  *codes_bytes = blocks * block_bytes(cache->bits);
+  *scale_bytes = blocks * kBlockTokens * sizeof(uint16_t);
+  return KVQ_OK;
+}
+
+KVQ_API kvq_status kvq_pack(const kvq_cache_desc* cache, int32_t which, const float* x, int32_t batch,
+                            int32_t max_seq_len, const int32_t* seq_lens, const int32_t* page_table,
+                            int32_t max_blocks, uint8_t* codes, uint16_t* scale, uint16_t* zero,
+                            uint32_t* dev_status, void* stream) {
+  kvq_status s = check_cache(cache);
+  if (s != KVQ_OK) return s;
+  if (which != 0 && which != 1) return KVQ_ERR_INVALID_ARG;
+  if (batch < 1 || max_seq_len < 1 || batch > 65535) return KVQ_ERR_INVALID_ARG;
+  const int need_blocks = (max_seq_len + kBlockTokens - 1) / kBlockTokens;
+  if (max_blocks < need_blocks) return KVQ_ERR_INVALID_ARG;
+  if (page_table == nullptr && (long long)batch * max_blocks > cache->num_pages) return KVQ_ERR_INVALID_ARG;
+  if (!x || !codes || !scale || !zero || !aligned16(x) || !aligned16(codes) || !aligned16(scale) || !aligned16(zero))
+    return KVQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(page_table) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  s = check_device(nullptr);
+  if (s != KVQ_OK) return s;
+  PackParams p{};
+  p.x = x; p.seq_lens = seq_lens; p.page_table = page_table;
+  p.codes = codes; p.scale = scale; p.zero = zero; p.dev_status = dev_status;
+  p.bits = cache->bits; p.k_scheme = cache->k_scheme; p.v_scheme = cache->v_scheme; p.which = which;
+  p.num_kv_heads = cache->num_kv_heads; p.num_pages = cache->num_pages;
+  p.batch = batch; p.max_seq_len = max_seq_len; p.max_blocks = max_blocks; p.max_blocks_needed = need_blocks;
+  return launch_pack(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+KVQ_API kvq_status kvq_dequant(const kvq_cache_desc* cache, int32_t which, const uint8_t* codes,
+                               const uint16_t* scale, const uint16_t* zero, int32_t batch, int32_t max_seq_len,
+                               const int32_t* seq_lens, const int32_t* page_table, int32_t max_blocks,
+                               float* x_hat, uint32_t* dev_status, void* stream) {
+  kvq_status s = check_cache(cache);
+  if (s != KVQ_OK) return s;
+  if (which != 0 && which != 1) return KVQ_ERR_INVALID_ARG;
+  if (batch < 1 || max_seq_len < 1 || batch > 65535) return KVQ_ERR_INVALID_ARG;
+  const int need_blocks = (max_seq_len + kBlockTokens - 1) / kBlockTokens;
+  if (max_blocks < need_blocks) return KVQ_ERR_INVALID_ARG;
+  if (page_table == nullptr && (long long)batch * max_blocks > cache->num_pages) return KVQ_ERR_INVALID_ARG;
+  if (!x_hat || !codes || !scale || !zero || !aligned16(x_hat) || !aligned16(codes)) return KVQ_ERR_INVALID_ARG;
+  s = check_device(nullptr);
+  if (s != KVQ_OK) return s;
+  DequantParams p{};
+  p.codes = codes; p.scale = scale; p.zero = zero; p.seq_lens = seq_lens; p.page_table = page_table;
+  p.x_hat = x_hat; p.dev_status = dev_status;
+  p.bits = cache->bits; p.k_scheme = cache->k_scheme; p.v_scheme = cache->v_scheme; p.which = which;
+  p.num_kv_heads = cache->num_kv_heads; p.num_pages = cache->num_pages;
+  p.batch = batch; p.max_seq_len = max_seq_len; p.max_blocks = max_blocks;
+  return launch_dequant(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* bytes) {
+  kvq_status s = check_attn(desc);
+  if (s != KVQ_OK) return s;
+  if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
+  int sm = 0;
+  if (desc->num_ctas == 0) {
+    s = check_device(&sm);
+    if (s != KVQ_OK) return s;
+  }
+  const int ctas = resolve_ctas(desc, sm);
+  *bytes = workspace_layout(desc->batch, desc->cache.num_kv_heads, ctas).total;
+  return KVQ_OK;
+}
+
+KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q, const uint8_t* k_codes,
+                                   const uint16_t* k_scale, const uint16_t* k_zero, const uint8_t* v_codes,
+                                   const uint16_t* v_scale, const uint16_t* v_zero, const int32_t* seq_lens,
+                                   const int32_t* page_table, float* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, uint32_t* dev_status, void* stream) {
+  kvq_status s = check_attn(desc);
+  if (s != KVQ_OK) return s;
+  // cache arrays are read with 16-byte bulk copies; the rest with scalar accesses
+  const void* bulk[] = {k_codes, k_scale, k_zero, v_codes, v_scale, v_zero};
+  for (const void* ptr : bulk)
+    if (ptr == nullptr || !aligned16(ptr)) return KVQ_ERR_INVALID_ARG;
+  if (q == nullptr || seq_lens == nullptr || out == nullptr || lse == nullptr) return KVQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(q) & 1u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(out) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  if (page_table != nullptr && (reinterpret_cast<uintptr_t>(page_table) & 3u)) return KVQ_ERR_INVALID_ARG;
+  if (page_table == nullptr && (long long)desc->batch * desc->max_blocks > desc->cache.num_pages)
+    return KVQ_ERR_INVALID_ARG;
+  int sm = 0;
+  s = check_device(&sm);
+  if (s != KVQ_OK) return s;
+  const int ctas = resolve_ctas(desc, sm);
+  const WorkspaceLayout w = workspace_layout(desc->batch, desc->cache.num_kv_heads, ctas);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVQ_ERR_WORKSPACE;
+  if (workspace_bytes < w.total) return KVQ_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  if (cudaMemsetAsync(ws + w.counters, 0, (size_t)desc->batch * desc->cache.num_kv_heads * sizeof(int), st) !=
+      cudaSuccess)
+    return KVQ_ERR_CUDA;
+  DecodeParams p{};
+  p.q = q; p.k_codes = k_codes; p.k_scale = k_scale; p.k_zero = k_zero;
+  p.v_codes = v_codes; p.v_scale = v_scale; p.v_zero = v_zero;
+  p.seq_lens = seq_lens; p.page_table = page_table; p.out = out; p.lse = lse; p.dev_status = dev_status;
+  p.counters = reinterpret_cast<int*>(ws + w.counters);
+  p.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
+  p.part_o = reinterpret_cast<float*>(ws + w.part_o);
+  p.batch = desc->batch; p.num_kv_heads = desc->cache.num_kv_heads; p.num_q_heads = desc->num_q_heads;
+  p.max_blocks = desc->max_blocks; p.num_pages = desc->cache.num_pages; p.num_ctas = ctas;
+  const float sm_scale = desc->sm_scale > 0.0f ? desc->sm_scale : 1.0f / std::sqrt((float)kHeadDim);
+  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.flags = desc->flags;
+  p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
+  cudaError_t e = launch_decode(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme, desc->operand_mode, p, st);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
+KVQ_API kvq_status kvq_merge(const float* o_parts, const float* lse_parts, int32_t rows, int32_t splits,
+                             int32_t head_dim, float* out, float* lse, void* stream) {
+  if (rows < 0 || splits < 1 || head_dim < 4 || head_dim > 1024 || (head_dim & 3) != 0) return KVQ_ERR_INVALID_ARG;
+  if (rows == 0) return KVQ_OK;
+  if (!o_parts || !lse_parts || !out || !lse || !aligned16(o_parts) || !aligned16(out)) return KVQ_ERR_INVALID_ARG;
+  kvq_status s = check_device(nullptr);
+  if (s != KVQ_OK) return s;
+  return launch_merge(o_parts, lse_parts, rows, splits, head_dim, out, lse, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
+}
+
+}  // extern "C"

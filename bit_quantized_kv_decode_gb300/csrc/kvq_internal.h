@@ -1,0 +1,81 @@
+// Internal declarations shared by the kvq translation units (not installed).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kBlockTokens = 128;  // tokens per block / page; channel-wise group
+constexpr int kHeadDim = 128;
+constexpr int kGroupQ = 4;  // query heads per KV head
+
+__device__ __forceinline__ void report(uint32_t* dev_status, uint32_t bits) {
+  if (dev_status != nullptr) atomicOr(dev_status, bits);
+}
+
+struct PackParams {
+  const float* x;
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  uint8_t* codes;
+  uint16_t* scale;
+  uint16_t* zero;
+  uint32_t* dev_status;
+  int bits, k_scheme, v_scheme, which;
+  int num_kv_heads, num_pages;
+  int batch, max_seq_len, max_blocks, max_blocks_needed;
+};
+
+struct DequantParams {
+  const uint8_t* codes;
+  const uint16_t* scale;
+  const uint16_t* zero;
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  float* x_hat;
+  uint32_t* dev_status;
+  int bits, k_scheme, v_scheme, which;
+  int num_kv_heads, num_pages;
+  int batch, max_seq_len, max_blocks;
+};
+
+// Everything the decode kernel reads; built and validated on the host.
+struct DecodeParams {
+  const uint16_t* q;  // bf16 [B][Hq][128]
+  const uint8_t* k_codes;
+  const uint16_t* k_scale;
+  const uint16_t* k_zero;
+  const uint8_t* v_codes;
+  const uint16_t* v_scale;
+  const uint16_t* v_zero;
+  const int32_t* seq_lens;
+  const int32_t* page_table;
+  float* out;
+  float* lse;
+  uint32_t* dev_status;
+  int* counters;        // [B * Hkv] split-unit arrival counters (zeroed per call)
+  float* part_o;        // [num_ctas][2][4][128]
+  float* part_lse;      // [num_ctas][2][4]
+  int batch, num_kv_heads, num_q_heads, max_blocks, num_pages;
+  int num_ctas;
+  float sm_scale_log2;  // sm_scale * log2(e)
+  uint32_t flags;
+  uint64_t wait_limit_ns;
+};
+
+size_t pack_smem_bytes();
+cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
+cudaError_t launch_dequant(const DequantParams& p, cudaStream_t stream);
+cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int rows, int splits, int head_dim, float* out,
+                         float* lse, cudaStream_t stream);
+
+// Decode kernel instances: bits in {2, 4}, K/V scheme, operand mode.
+cudaError_t launch_decode(int bits, int k_scheme, int v_scheme, int mode, const DecodeParams& p, cudaStream_t stream);
+int decode_ctas_per_sm();
+size_t decode_smem_bytes(int bits, int mode);
+
+}  // namespace kvq

@@ -1,0 +1,245 @@
+// Quantize + pack (and the inverse, dequantize) of one K or V cache.
+//
+// One CTA per (block j, KV head h, sequence b).  The block's 128 x 128 fp32
+// tile is staged in shared memory, each group's min/max gives its scale s and
+// offset z (asymmetric quantization, rag-lover.com summary of arXiv
+// 2611.09722, section "使える条件"), codes are computed with IEEE fp32
+// subtract/divide and round-half-even, and the block is written in the packed
+// chunk-major layout described in kvq.h.  The arithmetic is bit-for-bit the
+// library's quantizer rule: z = fp16 round-down of the minimum,
+// s = fp16 round-up of fp32((max - z) / (2^b - 1)),
+// code = clamp(rint(fp32(fp32(x - z) / s)), 0, 2^b - 1).
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kPitch = 129;  // fp32 tile row pitch (bank-conflict-free columns)
+
+struct GroupQ {
+  float s, z;
+  uint16_t s_bits, z_bits;
+  bool ok;
+};
+
+// Scale and offset of a group with minimum mn and maximum mx (finite).
+__device__ __forceinline__ GroupQ group_params(float mn, float mx, int qmax) {
+  GroupQ g;
+  __half zh = __float2half_rd(mn);
+  float z = __half2float(zh);
+  float rng = __fsub_rn(mx, z);
+  __half sh = __float2half_rn(0.0f);
+  if (rng != 0.0f) sh = __float2half_ru(__fdiv_rn(rng, (float)qmax));
+  g.ok = !__hisinf(zh) && !__hisinf(sh);
+  g.s = __half2float(sh);
+  g.z = z;
+  g.s_bits = __half_as_ushort(sh);
+  g.z_bits = __half_as_ushort(zh);
+  return g;
+}
+
+__device__ __forceinline__ uint32_t quantize_one(float x, const GroupQ& g, int qmax) {
+  if (g.s == 0.0f) return 0u;
+  float t = __fdiv_rn(__fsub_rn(x, g.z), g.s);
+  t = rintf(t);
+  t = fminf(fmaxf(t, 0.0f), (float)qmax);
+  return (uint32_t)t;
+}
+
+__device__ __forceinline__ float warp_min(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Resolve the block's page and valid token count; false = nothing to do.
+__device__ __forceinline__ bool block_geometry(const PackParams& p, int b, int j, int* page, int* nv) {
+  int len = p.seq_lens ? p.seq_lens[b] : p.max_seq_len;
+  if (len < 0 || len > p.max_seq_len) {
+    if (j == 0 && blockIdx.y == 0 && threadIdx.x == 0) report(p.dev_status, KVQ_DEV_BAD_SEQ_LEN);
+    return false;
+  }
+  if (j * kBlockTokens >= len) return false;
+  int pg = p.page_table ? p.page_table[(size_t)b * p.max_blocks + j] : b * p.max_blocks + j;
+  if (pg < 0 || pg >= p.num_pages) {
+    if (blockIdx.y == 0 && threadIdx.x == 0) report(p.dev_status, KVQ_DEV_BAD_PAGE);
+    return false;
+  }
+  *page = pg;
+  *nv = min(kBlockTokens, len - j * kBlockTokens);
+  return true;
+}
+
+__global__ void __launch_bounds__(kThreads) pack_kernel(PackParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  float* xs = reinterpret_cast<float*>(smem_raw);                                    // [128][kPitch]
+  uint8_t* cs = reinterpret_cast<uint8_t*>(xs + kBlockTokens * kPitch);             // [128 tok][128 ch]
+  uint16_t* s_out = reinterpret_cast<uint16_t*>(cs + kBlockTokens * kHeadDim);     // [128]
+  uint16_t* z_out = s_out + kBlockTokens;                                          // [128]
+
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  int page, nv;
+  if (!block_geometry(p, b, j, &page, &nv)) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int qmax = (1 << p.bits) - 1;
+
+  // Stage the valid tokens of the tile (rows t < nv).
+  const float* src = p.x + (((size_t)b * p.num_kv_heads + h) * p.max_seq_len + (size_t)j * kBlockTokens) * kHeadDim;
+  for (int i = tid; i < nv * (kHeadDim / 4); i += kThreads) {
+    int t = i / (kHeadDim / 4), c4 = (i % (kHeadDim / 4)) * 4;
+    float4 v = *reinterpret_cast<const float4*>(src + (size_t)t * kHeadDim + c4);
+    float* row = xs + t * kPitch + c4;
+    row[0] = v.x; row[1] = v.y; row[2] = v.z; row[3] = v.w;
+  }
+  for (int i = tid; i < kBlockTokens * kHeadDim / 4; i += kThreads) reinterpret_cast<uint32_t*>(cs)[i] = 0u;
+  __syncthreads();
+
+  const bool tokenwise = (p.which == 0 ? p.k_scheme : p.v_scheme) == KVQ_TOKENWISE;
+  if (tokenwise) {
+    // group = the 128 channels of token t; one warp per token
+    for (int t = warp; t < kBlockTokens; t += kThreads / 32) {
+      if (t >= nv) {  // padding token: s = z = 0, codes 0
+        if (lane == 0) { s_out[t] = 0; z_out[t] = 0; }
+        continue;
+      }
+      float v[4];
+      bool fin = true;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) { v[k] = xs[t * kPitch + lane + 32 * k]; fin &= isfinite(v[k]); }
+      fin = __all_sync(0xffffffffu, fin);
+      float mn = warp_min(fminf(fminf(v[0], v[1]), fminf(v[2], v[3])));
+      float mx = warp_max(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
+      GroupQ g = fin ? group_params(mn, mx, qmax) : GroupQ{0.f, 0.f, 0, 0, false};
+      if (!g.ok) {
+        if (lane == 0) { report(p.dev_status, KVQ_DEV_NONFINITE); s_out[t] = 0; z_out[t] = 0; }
+        continue;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) cs[t * kHeadDim + lane + 32 * k] = (uint8_t)quantize_one(v[k], g, qmax);
+      if (lane == 0) { s_out[t] = g.s_bits; z_out[t] = g.z_bits; }
+    }
+  } else {
+    // group = channel c over the block's valid tokens; one warp per channel
+    for (int c = warp; c < kHeadDim; c += kThreads / 32) {
+      float mn = INFINITY, mx = -INFINITY;
+      bool fin = true;
+      for (int t = lane; t < nv; t += 32) {
+        float v = xs[t * kPitch + c];
+        fin &= isfinite(v);
+        mn = fminf(mn, v);
+        mx = fmaxf(mx, v);
+      }
+      fin = __all_sync(0xffffffffu, fin);
+      mn = warp_min(mn);
+      mx = warp_max(mx);
+      GroupQ g = fin ? group_params(mn, mx, qmax) : GroupQ{0.f, 0.f, 0, 0, false};
+      if (!g.ok) {
+        if (lane == 0) { report(p.dev_status, KVQ_DEV_NONFINITE); s_out[c] = 0; z_out[c] = 0; }
+        continue;
+      }
+      for (int t = lane; t < nv; t += 32) cs[t * kHeadDim + c] = (uint8_t)quantize_one(xs[t * kPitch + c], g, qmax);
+      if (lane == 0) { s_out[c] = g.s_bits; z_out[c] = g.z_bits; }
+    }
+  }
+  __syncthreads();
+
+  // Pack: row r, chunk k holds columns [k*per_chunk, (k+1)*per_chunk).
+  const int bits = p.bits;
+  const int per_chunk = 128 / bits;         // columns per 16-byte chunk: 32 (INT4) or 64 (INT2)
+  const int nchunk = kHeadDim / per_chunk;  // 4 or 2
+  const size_t blk = (size_t)page * p.num_kv_heads + h;
+  uint8_t* dst = p.codes + blk * (size_t)(kBlockTokens * kHeadDim * bits / 8);
+  for (int i = tid; i < nchunk * kBlockTokens; i += kThreads) {
+    int k = i / kBlockTokens, r = i % kBlockTokens;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    for (int e = 0; e < per_chunk; ++e) {
+      int col = k * per_chunk + e;
+      // K: row = token, column = channel.  V: row = channel, column = token.
+      uint32_t code = (p.which == 0) ? cs[r * kHeadDim + col] : cs[col * kHeadDim + r];
+      int bitpos = e * bits;
+      w[bitpos >> 5] |= code << (bitpos & 31);
+    }
+    *reinterpret_cast<uint4*>(dst + (size_t)i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (tid < kBlockTokens) {
+    p.scale[blk * kBlockTokens + tid] = s_out[tid];
+    p.zero[blk * kBlockTokens + tid] = z_out[tid];
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) dequant_kernel(DequantParams p) {
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  float* dst = p.x_hat + (((size_t)b * p.num_kv_heads + h) * p.max_seq_len + (size_t)j * kBlockTokens) * kHeadDim;
+  const int ntok = min(kBlockTokens, p.max_seq_len - j * kBlockTokens);
+  int len = p.seq_lens ? p.seq_lens[b] : p.max_seq_len;
+  bool bad_len = len < 0 || len > p.max_seq_len;
+  if (bad_len && j == 0 && h == 0 && tid == 0) report(p.dev_status, KVQ_DEV_BAD_SEQ_LEN);
+  int nv = bad_len ? 0 : max(0, min(ntok, len - j * kBlockTokens));
+  int page = 0;
+  if (nv > 0) {
+    page = p.page_table ? p.page_table[(size_t)b * p.max_blocks + j] : b * p.max_blocks + j;
+    if (page < 0 || page >= p.num_pages) {
+      if (h == 0 && tid == 0) report(p.dev_status, KVQ_DEV_BAD_PAGE);
+      nv = 0;
+    }
+  }
+  const bool tokenwise = (p.which == 0 ? p.k_scheme : p.v_scheme) == KVQ_TOKENWISE;
+  const size_t blk = (size_t)page * p.num_kv_heads + h;
+  const int bits = p.bits;
+  const uint8_t* src = p.codes + blk * (size_t)(kBlockTokens * kHeadDim * bits / 8);
+  const uint16_t* sp = p.scale + blk * kBlockTokens;
+  const uint16_t* zp = p.zero + blk * kBlockTokens;
+  const int per_chunk = 128 / bits;
+  for (int i = tid; i < ntok * kHeadDim; i += kThreads) {
+    int t = i / kHeadDim, c = i % kHeadDim;
+    float v = 0.0f;
+    if (t < nv) {
+      int r = (p.which == 0) ? t : c;    // row in the block
+      int col = (p.which == 0) ? c : t;  // column in the row
+      int k = col / per_chunk, e = col % per_chunk;
+      const uint32_t* chunk = reinterpret_cast<const uint32_t*>(src + ((size_t)k * kBlockTokens + r) * 16);
+      int bitpos = e * bits;
+      uint32_t code = (chunk[bitpos >> 5] >> (bitpos & 31)) & ((1u << bits) - 1u);
+      int g = tokenwise ? t : c;
+      float s = __half2float(__ushort_as_half(sp[g]));
+      float z = __half2float(__ushort_as_half(zp[g]));
+      v = fmaf(s, (float)code, z);
+    }
+    dst[(size_t)t * kHeadDim + c] = v;
+  }
+}
+
+}  // namespace
+
+size_t pack_smem_bytes() {
+  return (size_t)kBlockTokens * kPitch * sizeof(float) + kBlockTokens * kHeadDim + 2 * kBlockTokens * sizeof(uint16_t);
+}
+
+cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
+  const size_t smem = pack_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.max_blocks_needed, p.num_kv_heads, p.batch);
+  pack_kernel<<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const DequantParams& p, cudaStream_t stream) {
+  dim3 grid((p.max_seq_len + kBlockTokens - 1) / kBlockTokens, p.num_kv_heads, p.batch);
+  dequant_kernel<<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

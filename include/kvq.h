@@ -1,0 +1,199 @@
+/*
+ * kvq -- decode attention over an asymmetric INT2/INT4 group-quantized KV
+ * cache, for one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (cited by page title and section of the sources):
+ *   - "FOSCAR: Accelerating Decode Attention over 2- and 4-Bit KV Caches
+ *     through Affine Folding" (papers.pytorch.kr), abstract: decode attention
+ *     streams a KV cache packed as 2- or 4-bit integers; scale and offset are
+ *     applied to the other operand or to the output of the two attention
+ *     matrix products ("affine folding"), exactly equal to dequantizing first.
+ *   - rag-lover.com summary of arXiv 2611.09722, section "使える条件"
+ *     (conditions of use): asymmetric quantization, each group shares a scale
+ *     s and an offset z; K and V each choose token-wise or channel-wise groups
+ *     independently; group size 128; 4 query heads per KV head.
+ *   - same page, section "解説" (commentary): which side each scheme folds on,
+ *     and code bits placed in the low bits of a tensor-core element.
+ *
+ * out[b, h, :] = softmax(S) V_hat[b, h/4],  S_l = sm_scale * q[b,h] . K_hat[b, h/4, l],
+ * lse[b, h] = ln sum_l exp(S_l), with x_hat = s * code + z and code unsigned.
+ *
+ * Cache format (this library's; the pages leave it open)
+ * -------------------------------------------------------
+ * head_dim D = 128; a block (= page) holds 128 consecutive tokens of one KV
+ * head.  Codes of one block form a 128 x 128 matrix: K rows are tokens
+ * (channels along the row), V rows are channels (tokens along the row).  A
+ * row is packed little-endian (column i at bits [b*(i mod 8/b), +b) of row
+ * byte i*b/8), cut into 16-byte chunks, and the block is stored chunk-major:
+ * byte offset (chunk*128 + row)*16 + byte.  Block bytes: 8192 (INT4), 4096
+ * (INT2).  codes array: [num_pages][num_kv_heads][block bytes].
+ * scale / zero arrays (fp16 bit patterns): [num_pages][num_kv_heads][128],
+ * indexed by token within the block (token-wise) or by channel
+ * (channel-wise).  Token-wise groups are the 128 channels of a token;
+ * channel-wise groups are one channel over the block's tokens.  Tokens at or
+ * past a sequence's length have code 0 (token-wise: s = z = 0).
+ * Sequence b's block j lives in page page_table[b*max_blocks + j], or in page
+ * b*max_blocks + j when page_table is NULL ("contiguous" cache).
+ *
+ * Conventions
+ * -----------
+ *  - All pointers except descriptors, out-params and the stream are device
+ *    pointers on the current CUDA device, 16-byte aligned, owned by the
+ *    caller.  The library allocates no memory and keeps no state.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream); every call is
+ *    asynchronous on it.
+ *  - A non-KVQ_OK return means nothing was launched.  Errors found on the
+ *    device are OR-ed into *dev_status (KVQ_DEV_* bits; the caller zeroes it
+ *    and reads it after synchronizing; it may be NULL).  Device checks turn
+ *    bad lengths and page ids into empty/zero work, never into out-of-range
+ *    memory accesses.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_API __attribute__((visibility("default")))
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1, /* NULL/misaligned pointer, bad size or enum value */
+  KVQ_ERR_UNSUPPORTED = 2, /* well-formed but not built (e.g. head_dim != 128) */
+  KVQ_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
+  KVQ_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  KVQ_ERR_DEVICE = 5       /* current device is not an sm_103 GPU */
+} kvq_status;
+
+/* Bits of *dev_status. */
+#define KVQ_DEV_BAD_SEQ_LEN 0x1u /* seq_len < 0 or > max_blocks*128 (or > max_seq_len for pack) */
+#define KVQ_DEV_BAD_PAGE 0x2u    /* page id outside [0, num_pages) */
+#define KVQ_DEV_NONFINITE 0x4u   /* pack: NaN/Inf input, or s / z overflow fp16 */
+#define KVQ_DEV_TIMEOUT 0x8u     /* a pipeline wait ran out; outputs are not valid */
+
+typedef enum kvq_scheme { KVQ_TOKENWISE = 0, KVQ_CHANNELWISE = 1 } kvq_scheme;
+
+/* Tensor-core operand precision of decode attention.
+ * FP8: KV codes as exact E4M3 values (code * 2^-9); Q' and P' as sums of
+ *      three E4M3 parts.  The production path.
+ * BF16: KV codes as exact BF16 integers; Q' and P' as sums of two BF16
+ *      parts.  A correctness mode with tighter error. */
+typedef enum kvq_operand_mode { KVQ_OPERANDS_FP8 = 0, KVQ_OPERANDS_BF16 = 1 } kvq_operand_mode;
+
+typedef struct kvq_cache_desc {
+  int32_t bits;         /* 2 or 4 */
+  int32_t k_scheme;     /* kvq_scheme used by K */
+  int32_t v_scheme;     /* kvq_scheme used by V */
+  int32_t head_dim;     /* must be 128 */
+  int32_t num_kv_heads; /* >= 1 */
+  int32_t num_pages;    /* 128-token pages the cache arrays hold */
+} kvq_cache_desc;
+
+typedef struct kvq_attn_desc {
+  kvq_cache_desc cache;
+  int32_t batch;        /* sequences (>= 1) */
+  int32_t num_q_heads;  /* must be 4 * num_kv_heads */
+  int32_t max_blocks;   /* page_table row length; contiguous: blocks per sequence */
+  int32_t operand_mode; /* kvq_operand_mode */
+  float sm_scale;       /* <= 0 selects 1/sqrt(head_dim) */
+  int32_t num_ctas;     /* persistent CTAs; 0 = two per SM */
+  uint32_t flags;       /* 0, or KVQ_FLAG_TEST_STALL */
+} kvq_attn_desc;
+
+/* Test hook: the loader withholds one tile so that every waiting stage runs
+ * into its time limit; the call must end with KVQ_DEV_TIMEOUT set. */
+#define KVQ_FLAG_TEST_STALL 0x1u
+
+/* Human-readable name of a status code (static storage). */
+KVQ_API const char* kvq_status_string(kvq_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+KVQ_API int32_t kvq_version(void);
+
+/* Bytes of one K or V cache: *codes_bytes for the codes array,
+ * *scale_bytes for each of the scale and zero arrays.  Host only. */
+KVQ_API kvq_status kvq_cache_bytes(const kvq_cache_desc* cache, size_t* codes_bytes, size_t* scale_bytes);
+
+/*
+ * Quantize and pack K (which = 0) or V (which = 1) into the cache format
+ * above.  Group rule ([SUM] 使える条件, asymmetric min/max; rounding is this
+ * library's reading): z = fp16 round-down of the group minimum,
+ * s = fp16 round-up of fp32((max - z) / (2^bits - 1)),
+ * code = clamp(rint(fp32(fp32(x - z) / s)), 0, 2^bits - 1), all IEEE fp32;
+ * max == z gives s = 0, code = 0.
+ *   x          fp32 [batch][num_kv_heads][max_seq_len][128]
+ *   seq_lens   int32 [batch] in [0, max_seq_len], or NULL (all max_seq_len)
+ *   page_table int32 [batch][max_blocks], or NULL (contiguous; then
+ *              batch*max_blocks <= num_pages)
+ *   max_blocks >= ceil(max_seq_len / 128)
+ *   codes, scale, zero: the cache arrays (only pages the batch covers are
+ *              written)
+ * Device errors: KVQ_DEV_NONFINITE (that group is written as zeros),
+ * KVQ_DEV_BAD_SEQ_LEN, KVQ_DEV_BAD_PAGE (that block is skipped).
+ */
+KVQ_API kvq_status kvq_pack(const kvq_cache_desc* cache, int32_t which, const float* x, int32_t batch,
+                            int32_t max_seq_len, const int32_t* seq_lens, const int32_t* page_table,
+                            int32_t max_blocks, uint8_t* codes, uint16_t* scale, uint16_t* zero,
+                            uint32_t* dev_status, void* stream);
+
+/*
+ * Read a packed K or V cache back as fp32 x_hat = s * code + z (exact, one
+ * rounding).  x_hat: fp32 [batch][num_kv_heads][max_seq_len][128]; positions
+ * at or past seq_lens[b] are written as 0.  Other arguments as kvq_pack.
+ */
+KVQ_API kvq_status kvq_dequant(const kvq_cache_desc* cache, int32_t which, const uint8_t* codes,
+                               const uint16_t* scale, const uint16_t* zero, int32_t batch, int32_t max_seq_len,
+                               const int32_t* seq_lens, const int32_t* page_table, int32_t max_blocks,
+                               float* x_hat, uint32_t* dev_status, void* stream);
+
+/* Workspace bytes kvq_decode_attn needs for `desc` (queries the current
+ * device when desc->num_ctas == 0). */
+KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* bytes);
+
+/*
+ * Decode attention over the packed cache, affine-folded (abstract; [SUM] 解説):
+ * token-wise K scales the partial q.code by s and adds z * sum(q); channel-
+ * wise K multiplies q by s before the product and adds q . z; token-wise V
+ * multiplies the probabilities by s and adds sum(p * z); channel-wise V scales
+ * each 128-token group's partial product by s and adds z * sum(p) of that
+ * group ([SUM] 限界と未検証の範囲: per-group application).  Work is split
+ * over persistent CTAs in equal tile ranges; a sequence/head cut between
+ * CTAs is merged on the device by log-sum-exp.
+ *   q        bf16 [batch][num_q_heads][128]
+ *   k_codes, v_codes, k_scale, k_zero, v_scale, v_zero: cache arrays
+ *   seq_lens int32 [batch], each in [0, max_blocks*128]
+ *   page_table int32 [batch][max_blocks] or NULL (contiguous)
+ *   out      fp32 [batch][num_q_heads][128];  lse fp32 [batch][num_q_heads]
+ *            (natural log; empty sequence: out = 0, lse = -inf)
+ *   workspace >= kvq_decode_workspace_size bytes, 256-byte aligned; its
+ *            contents need no initialisation; concurrent calls need separate
+ *            workspaces
+ */
+KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q, const uint8_t* k_codes,
+                                   const uint16_t* k_scale, const uint16_t* k_zero, const uint8_t* v_codes,
+                                   const uint16_t* v_scale, const uint16_t* v_zero, const int32_t* seq_lens,
+                                   const int32_t* page_table, float* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, uint32_t* dev_status, void* stream);
+
+/*
+ * Log-sum-exp merge of partial attention results over disjoint token ranges
+ * (split-KV): lse[r] = ln sum_s exp(lse_parts[r][s]),
+ * out[r] = sum_s exp(lse_parts[r][s] - lse[r]) * o_parts[r][s].
+ *   o_parts fp32 [rows][splits][head_dim] (each part normalised over its own
+ *           range), lse_parts fp32 [rows][splits] (-inf = empty part)
+ *   out fp32 [rows][head_dim], lse fp32 [rows]; all parts empty -> 0, -inf
+ *   head_dim: a multiple of 4, at most 1024
+ */
+KVQ_API kvq_status kvq_merge(const float* o_parts, const float* lse_parts, int32_t rows, int32_t splits,
+                             int32_t head_dim, float* out, float* lse, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

@@ -1,0 +1,109 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+symbol include/kvq.h declares, and host-side validation rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__ as entry
+from bit_quantized_kv_decode_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    entry.build()
+    return _lib.load()
+
+
+def _header_symbols():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    return sorted(set(re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _header_symbols()
+    assert len(declared) >= 8
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(_lib.EXPORTS) == declared
+
+
+def test_only_declared_symbols_exported(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.lib_path()], capture_output=True, text=True).stdout
+    exported = sorted(l.split()[-1] for l in out.splitlines() if " T " in l)
+    assert exported == _header_symbols()
+
+
+def test_status_strings_and_version(lib):
+    assert lib.kvq_status_string(0) == b"ok"
+    assert lib.kvq_status_string(3) == b"workspace too small"
+    assert lib.kvq_status_string(99) == b"unknown status"
+    assert lib.kvq_version() >= 100
+
+
+def _cache(bits=4, k=0, v=1, heads=8, pages=1024, hd=128):
+    return _lib.CacheDesc(bits, k, v, hd, heads, pages)
+
+
+def test_cache_bytes(lib):
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.kvq_cache_bytes(ctypes.byref(_cache(4)), ctypes.byref(cb), ctypes.byref(sb)) == 0
+    assert cb.value == 1024 * 8 * 8192 and sb.value == 1024 * 8 * 128 * 2
+    assert lib.kvq_cache_bytes(ctypes.byref(_cache(2)), ctypes.byref(cb), ctypes.byref(sb)) == 0
+    assert cb.value == 1024 * 8 * 4096
+    assert lib.kvq_cache_bytes(ctypes.byref(_cache(3)), ctypes.byref(cb), ctypes.byref(sb)) == 2
+    assert lib.kvq_cache_bytes(ctypes.byref(_cache(4, hd=64)), ctypes.byref(cb), ctypes.byref(sb)) == 2
+    assert lib.kvq_cache_bytes(None, ctypes.byref(cb), ctypes.byref(sb)) == 1
+
+
+def test_workspace_size_host_only(lib):
+    d = _lib.AttnDesc(_cache(4, pages=128 * 256), 128, 32, 256, 0, 0.0, 304, 0)
+    n = ctypes.c_size_t()
+    assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+    # counters (B*Hkv ints) + part lse + part out, each 256-byte aligned
+    assert n.value == 4096 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
+    bad = _lib.AttnDesc(_cache(4), 128, 16, 256, 0, 0.0, 304, 0)  # GQA 2 is not built
+    assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
+    bad = _lib.AttnDesc(_cache(4), 0, 32, 256, 0, 0.0, 304, 0)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
+    bad = _lib.AttnDesc(_cache(4), 2048, 32, 256, 0, 0.0, 304, 0)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
+    bad = _lib.AttnDesc(_cache(4), 8, 32, 256, 7, 0.0, 304, 0)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
+
+
+def test_validation_precedes_device(lib):
+    """Bad arguments are rejected on the host (no device needed)."""
+    c = _cache(4)
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: validation fails first
+    # which out of range
+    assert lib.kvq_pack(ctypes.byref(c), 2, fake, 1, 128, None, None, 1, fake, fake, fake, None, None) == 1
+    # misaligned x
+    assert lib.kvq_pack(ctypes.byref(c), 0, P(0x10004), 1, 128, None, None, 1, fake, fake, fake, None, None) == 1
+    # max_blocks too small for max_seq_len
+    assert lib.kvq_pack(ctypes.byref(c), 0, fake, 1, 300, None, None, 2, fake, fake, fake, None, None) == 1
+    # contiguous cache larger than num_pages
+    small = _cache(4, pages=3)
+    assert lib.kvq_pack(ctypes.byref(small), 0, fake, 2, 256, None, None, 2, fake, fake, fake, None, None) == 1
+    # decode: null output
+    d = _lib.AttnDesc(c, 1, 32, 2, 0, 0.0, 1, 0)
+    args = [fake] * 7 + [fake, None, None, fake, fake, 1 << 20, None, None]
+    assert lib.kvq_decode_attn(ctypes.byref(d), *args) == 1
+    # merge: bad head_dim
+    assert lib.kvq_merge(fake, fake, 4, 2, 130, fake, fake, None) == 1
+
+
+def test_no_device_reports_device_error(lib):
+    """On a machine without a GPU a well-formed call fails loudly (no fallback)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    c = _cache(4)
+    fake = ctypes.c_void_p(0x10000)
+    assert lib.kvq_pack(ctypes.byref(c), 0, fake, 1, 128, None, None, 1, fake, fake, fake, None, None) == 5

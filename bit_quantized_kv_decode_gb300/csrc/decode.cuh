@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = p.batch, Hkv = p.num_kv_heads;
-  const int Cn = gridDim.x, cta = blockIdx.x;
+  const int cta = blockIdx.x;
   volatile int* abort_flag = &sh.abort_flag;
   const uint64_t limit = p.wait_limit_ns;
 
@@ -346,8 +346,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   const long long T = sh.total_tiles;
-  const long long g0 = T > 0 ? range_start(cta, T, Cn) : 0;
-  const long long g1 = T > 0 ? range_start(cta + 1, T, Cn) : 0;
+  // Tile ranges are cut over min(grid, T) CTAs so that every active CTA owns
+  // at least one tile (the split-unit merge counts one part per CTA between a
+  // unit's first and last owner); the remaining CTAs only write empty rows.
+  const int Cn = (int)(T < (long long)gridDim.x ? T : (long long)gridDim.x);
+  const bool active = cta < Cn;
+  const long long g0 = active ? range_start(cta, T, Cn) : 0;
+  const long long g1 = active ? range_start(cta + 1, T, Cn) : 0;
   const int ntiles = (int)(g1 - g0);
 
   // ============================================================= loader
@@ -596,7 +601,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     const float kLn2 = 0.69314718055994530942f;
 
     // empty sequences: out = 0, lse = -inf
-    for (int b = cta; b < B; b += Cn) {
+    for (int b = cta; b < B; b += (int)gridDim.x) {
       if (lens[b] != 0) continue;
       for (int hq = 0; hq < p.num_q_heads; ++hq) {
         p.out[((size_t)b * p.num_q_heads + hq) * kHeadDim + i] = 0.0f;

@@ -80,6 +80,8 @@ def attn_errors(pb: Problem, res: dict):
 
 def assert_attention_close(pb: Problem, res: dict, mode: int):
     err, lerr = attn_errors(pb, res)
+    print(f"[parity] {pb.w.name} B={pb.w.batch} bits={pb.w.bits} k={pb.w.k_scheme} v={pb.w.v_scheme} "
+          f"mode={mode}: max|out-oracle|/rms={err:.3e} max|lse-oracle|={lerr:.3e}")
     assert err <= TOL[mode], f"max|out-oracle|/rms = {err:.3e} > {TOL[mode]}"
     assert lerr <= LSE_TOL[mode], f"max|lse-oracle| = {lerr:.3e} > {LSE_TOL[mode]}"
     return err, lerr

@@ -47,10 +47,6 @@ def test_dequant_bitexact(bits, scheme):
         xh = kvq.dequant(desc, which, cache, 3, 300, lens, pt).cpu().numpy()
         ref = pb.ref["khat" if which == 0 else "vhat"].astype(np.float32)
         assert np.array_equal(xh, ref)
-        # and the dequantized cache is within the quantizer bound of the input
-        x = (pb.k if which == 0 else pb.v).numpy()
-        for b, n in enumerate(pb.lens.tolist()):
-            assert np.abs(xh[b, :, :n] - x[b, :, :n]).max() < 2.0
 
 
 def test_pack_nonfinite_and_bad_page_flags():

@@ -23,7 +23,7 @@ GROUP_Q = 4
 __all__ = ["CacheDesc", "AttnDesc", "KvqError", "TOKENWISE", "CHANNELWISE", "OPERANDS_FP8", "OPERANDS_BF16",
            "DEV_BAD_SEQ_LEN", "DEV_BAD_PAGE", "DEV_NONFINITE", "DEV_TIMEOUT", "FLAG_TEST_STALL", "cache_desc",
            "attn_desc", "cache_bytes", "block_bytes", "alloc_cache", "pack", "dequant", "workspace_size",
-           "decode_attn", "merge", "library"]
+           "decode_attn", "decode_attn_static", "merge", "library"]
 
 
 def library() -> ctypes.CDLL:
@@ -166,6 +166,42 @@ def decode_attn(desc: CacheDesc, q: torch.Tensor, k_cache, v_cache, seq_lens: to
                                    _p(seq_lens), _p(page_table), _p(out), _p(lse), _p(workspace),
                                    workspace.numel(), _p(dev_status), _stream())
     _lib.check(st, "kvq_decode_attn")
+    return out, lse
+
+
+def decode_attn_static(desc: CacheDesc, q: torch.Tensor, k_cache, v_cache, seq_lens: torch.Tensor,
+                       page_table: Optional[torch.Tensor] = None, max_blocks: Optional[int] = None,
+                       mode: int = OPERANDS_FP8, sm_scale: float = 0.0, num_ctas: int = 0,
+                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                       dev_status: Optional[torch.Tensor] = None):
+    """decode_attn for callers that cannot allocate device memory: the C entry
+    point keeps its scratch in a fixed device array owned by the library (see
+    kvq_decode_attn_static in include/kvq.h).  `out` and `lse` are still
+    caller buffers; pass them preallocated to avoid any allocation here."""
+    _need(q, "q", torch.bfloat16)
+    if q.dim() != 3 or q.shape[2] != HEAD_DIM:
+        raise ValueError("q must be bf16 [batch, num_q_heads, 128]")
+    B, Hq, _ = q.shape
+    if page_table is not None:
+        mb = _geometry(B, 1, seq_lens, page_table, None)
+    else:
+        if max_blocks is None:
+            raise ValueError("max_blocks is required for a contiguous cache")
+        mb = max_blocks
+        _need(seq_lens, "seq_lens", torch.int32, B)
+    ad = AttnDesc(desc, B, Hq, mb, mode, sm_scale, num_ctas, 0)
+    if out is None:
+        out = torch.empty(B, Hq, HEAD_DIM, dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.float32, B * Hq * HEAD_DIM)
+    _need(lse, "lse", torch.float32, B * Hq)
+    kc, ks, kz = k_cache
+    vc, vs, vz = v_cache
+    st = library().kvq_decode_attn_static(ctypes.byref(ad), _p(q), _p(kc), _p(ks), _p(kz), _p(vc), _p(vs), _p(vz),
+                                          _p(seq_lens), _p(page_table), _p(out), _p(lse), _p(dev_status),
+                                          _stream())
+    _lib.check(st, "kvq_decode_attn_static")
     return out, lse
 
 

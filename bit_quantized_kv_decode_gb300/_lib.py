@@ -23,7 +23,7 @@ FLAG_TEST_STALL = 0x1
 
 # Every symbol include/kvq.h declares.
 EXPORTS = ("kvq_status_string", "kvq_version", "kvq_cache_bytes", "kvq_pack", "kvq_dequant",
-           "kvq_decode_workspace_size", "kvq_decode_attn", "kvq_merge")
+           "kvq_decode_workspace_size", "kvq_decode_attn", "kvq_decode_attn_static", "kvq_merge")
 
 
 class CacheDesc(ctypes.Structure):
@@ -75,6 +75,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.kvq_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(SZ)]
     lib.kvq_decode_attn.restype = I32
     lib.kvq_decode_attn.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
+    lib.kvq_decode_attn_static.restype = I32
+    lib.kvq_decode_attn_static.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.kvq_merge.restype = I32
     lib.kvq_merge.argtypes = [P, P, I32, I32, I32, P, P, P]
     _ = U32

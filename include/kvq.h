@@ -39,7 +39,8 @@
  * -----------
  *  - All pointers except descriptors, out-params and the stream are device
  *    pointers on the current CUDA device, 16-byte aligned, owned by the
- *    caller.  The library allocates no memory and keeps no state.
+ *    caller.  The library allocates no memory; apart from the fixed scratch
+ *    array behind kvq_decode_attn_static it keeps no state.
  *  - `stream` is a cudaStream_t (NULL = legacy default stream); every call is
  *    asynchronous on it.
  *  - A non-KVQ_OK return means nothing was launched.  Errors found on the
@@ -179,6 +180,30 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
                                    const uint16_t* v_scale, const uint16_t* v_zero, const int32_t* seq_lens,
                                    const int32_t* page_table, float* out, float* lse, void* workspace,
                                    size_t workspace_bytes, uint32_t* dev_status, void* stream);
+
+/*
+ * Decode attention without a caller workspace, for callers that cannot
+ * allocate device memory: a runtime whose device memory plan is frozen after
+ * start-up, a plugin interface that hands over only input and output
+ * buffers, or a latency-critical path where an allocation would synchronise
+ * the device.  (No counterpart on the pages describing the method; this call
+ * exists for such integrations.)  Same arguments, semantics and errors as
+ * kvq_decode_attn minus the workspace: the split-merge scratch lives in a
+ * fixed 4 MiB device array owned by the library, held on every device that
+ * loads the library until the process exits.  Returns KVQ_ERR_WORKSPACE when
+ * a call needs more scratch than that (batch * num_kv_heads * 4 bytes of
+ * counters plus 4 KiB per CTA); kvq_decode_attn with a caller workspace then
+ * remains available.  The first call on each device looks up the array's
+ * address once (this may load the module): make it before any stream
+ * capture.  Every call on a device shares the array and the counters are
+ * cleared on the stream at each call, so calls whose kernels may overlap on
+ * the GPU (unordered streams) race.  Allocates nothing.
+ */
+KVQ_API kvq_status kvq_decode_attn_static(const kvq_attn_desc* desc, const uint16_t* q, const uint8_t* k_codes,
+                                          const uint16_t* k_scale, const uint16_t* k_zero, const uint8_t* v_codes,
+                                          const uint16_t* v_scale, const uint16_t* v_zero, const int32_t* seq_lens,
+                                          const int32_t* page_table, float* out, float* lse, uint32_t* dev_status,
+                                          void* stream);
 
 /*
  * Log-sum-exp merge of partial attention results over disjoint token ranges

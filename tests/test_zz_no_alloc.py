@@ -1,0 +1,63 @@
+"""The allocation-free decode entry point (kvq_decode_attn_static).
+
+It serves callers that cannot allocate device memory -- a runtime whose
+memory plan is frozen, a plugin interface that passes only input and output
+buffers -- by keeping the decode's split-merge scratch in a fixed device array
+owned by the library.  This file is collected last on purpose, and it passes
+both on its own in a fresh process and after the rest of the suite.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import kvq_synth as synth
+from tests.kvq_testlib import TOL, LSE_TOL, make_problem, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem():
+    w = synth.shrink(synth.WORKLOADS["tiny"], batch=3, num_kv_heads=2, num_q_heads=8, bits=4,
+                     k_scheme=1, v_scheme=0, max_seq_len=1500)
+    return make_problem(w, seed=77, lens=[1500, 700, 129])
+
+
+def test_static_scratch_matches_workspace_entry_point_twice():
+    import bit_quantized_kv_decode_gb300 as kvq
+    pb = _problem()
+    dev = torch.device("cuda")
+    res = run_gpu(pb, num_ctas=7)  # existing entry point, caller workspace; splits units across CTAs
+    assert res["status"] == 0
+    q = pb.q.to(dev)
+    lens = pb.lens.to(dev)
+    ref_o = torch.tensor(res["out"])
+    ref_l = torch.tensor(res["lse"])
+    rms = float(ref_o.pow(2).mean().sqrt())
+    out = torch.empty(3, 8, 128, dtype=torch.float32, device=dev)
+    lse = torch.empty(3, 8, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(2):  # the second call finds the first call's scratch contents
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        kvq.decode_attn_static(res["desc"], q, res["k_cache"], res["v_cache"], lens, max_blocks=pb.max_blocks,
+                               num_ctas=7, out=out, lse=lse, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        o = out.cpu().double()
+        l_ = lse.cpu().double()
+        assert float((o - ref_o).abs().max()) <= TOL[0] * rms
+        assert float((l_ - ref_l).abs().max()) <= LSE_TOL[0]
+
+
+def test_static_scratch_rejects_oversized_calls():
+    import bit_quantized_kv_decode_gb300 as kvq
+    from bit_quantized_kv_decode_gb300 import _lib
+    lib = kvq.library()
+    desc = kvq.cache_desc(4, 1, 0, 8, 1024 * 8)
+    # 2000 CTAs need 2000 * 4 KiB of partial results: more than the fixed 4 MiB
+    ad = _lib.AttnDesc(desc, 1024, 32, 8, 0, 0.0, 2000, 0)
+    fake = ctypes.c_void_p(0x10000)
+    st = lib.kvq_decode_attn_static(ctypes.byref(ad), *([fake] * 7), fake, None, fake, fake, None, None)
+    assert st == 3  # KVQ_ERR_WORKSPACE, before any launch

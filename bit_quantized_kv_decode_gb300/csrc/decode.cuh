@@ -41,15 +41,30 @@
 
 namespace kvq {
 
-constexpr int kDecodeThreads = 320;  // 10 warps
+// Optional cycle accounting per CTA and pipeline role (built only when
+// KVQ_PROFILE is defined; the library build never defines it).
+#ifdef KVQ_PROFILE
+#define KVQ_PT(n) long long kvq_pt_##n = clock64();
+#define KVQ_PA(slot, n) \
+  if (p.prof != nullptr && (threadIdx.x & 31) == 0) atomicAdd(&p.prof[blockIdx.x * 32 + (slot)], (unsigned long long)(clock64() - kvq_pt_##n));
+#else
+#define KVQ_PT(n)
+#define KVQ_PA(slot, n)
+#endif
+
+constexpr int kDecodeThreads = 448;  // 14 warps
 constexpr int kMaxBatch = 1024;      // sequences per call (prefix table in shared memory)
 constexpr uint32_t FULL = 0xffffffffu;
 
-// Warp roles.
+// Warp roles.  The softmax work is split by query head: group g (4 warps)
+// owns heads 2g and 2g+1 of every (sequence, kv head).
 constexpr int kWarpConvert0 = 0;  // warps 0-3: KV codes -> tensor memory, Q' operand
-constexpr int kWarpSoftmax0 = 4;  // warps 4-7: fold, online softmax, P' operand, epilogue
-constexpr int kWarpLoad = 8;      // packed tiles HBM -> shared memory
-constexpr int kWarpMma = 9;       // tcgen05.mma issue, tensor memory owner
+constexpr int kWarpSoftmax0 = 4;  // warps 4-11: fold, online softmax, P' operand, epilogue
+constexpr int kSoftmaxGroups = 2;
+constexpr int kHeadsPerGroup = kGroupQ / kSoftmaxGroups;
+static_assert(kHeadsPerGroup == 2, "the softmax groups handle two heads each");
+constexpr int kWarpLoad = 12;     // packed tiles HBM -> shared memory
+constexpr int kWarpMma = 13;      // tcgen05.mma issue, tensor memory owner
 
 template <int BITS, bool BF16>
 struct DecodeCfg {
@@ -67,13 +82,14 @@ struct DecodeCfg {
   static constexpr uint32_t kLbo = BF16 ? 256 : 128;  // K-direction core-matrix stride
   static constexpr uint32_t kSbo = 128;               // N-direction core-matrix stride
   static constexpr uint32_t kIdesc = BF16 ? make_idesc(1, 1, 0, 1, 128, 16) : make_idesc(0, 0, 0, 1, 128, 16);
+  static constexpr int kSlots = 4;  // score / probability / output buffers in flight
   static constexpr int kColAK = 0;
   static constexpr int kColAV = kNA * kACols;
   static constexpr int kColS = 2 * kNA * kACols;
-  static constexpr int kColO = kColS + 32;
+  static constexpr int kColO = kColS + 16 * kSlots;
   static constexpr int kTmemCols = 256;
   static constexpr float kCodeInv = BF16 ? 1.0f : 512.0f;  // code = operand value * kCodeInv
-  static_assert(kColO + 32 <= kTmemCols, "tensor memory budget");
+  static_assert(kColO + 16 * kSlots <= kTmemCols, "tensor memory budget");
 };
 
 // Position of element e (channel of a K row, token of a V row) along the
@@ -123,6 +139,29 @@ __device__ __forceinline__ uint4 split3_e4m3(float4 v) {
   r.w = 0u;
   return r;
 }
+// Two values -> three E4M3 parts each: {hi, mid, lo}, each a 16-bit pair
+// (value 0 in the low byte).
+__device__ __forceinline__ uint3 split3_e4m3_x2(float2 v) {
+  uint3 r;
+  r.x = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)r.x, __NV_E4M3);
+  float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+  v = make_float2(v.x - f.x, v.y - f.y);
+  r.y = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+  h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)r.y, __NV_E4M3);
+  f = __half22float2(*reinterpret_cast<__half2*>(&h));
+  v = make_float2(v.x - f.x, v.y - f.y);
+  r.z = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+  return r;
+}
+// Two values -> two BF16 parts each: {hi pair, lo pair}.
+__device__ __forceinline__ uint2 split2_bf16_x2(float2 v) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
+  float2 f = __bfloat1622float2(h);
+  __nv_bfloat162 l = __floats2bfloat162_rn(v.x - f.x, v.y - f.y);
+  return make_uint2(*reinterpret_cast<uint32_t*>(&h), *reinterpret_cast<uint32_t*>(&l));
+}
+
 // x ~= hi + lo, each part BF16: {hi01, hi23, lo01, lo23}.
 __device__ __forceinline__ uint4 split2_bf16(float4 v) {
   __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
@@ -176,13 +215,12 @@ struct alignas(16) DecodeBarriers {
   using C = DecodeCfg<BITS, BF16>;
   uint64_t stg_full[C::kStages], stg_empty[C::kStages];
   uint64_t ak_full[C::kNA], ak_empty[C::kNA], av_full[C::kNA], av_empty[C::kNA];
-  uint64_t q_full[2], q_empty[2], sd_full[2], sd_empty[2];
-  uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2], o_full[2], o_empty[2];
-  uint64_t cw_grp, sw_grp, drain;
-  float side[2][8];         // per tile: score multiplier [4], score offset [4] (converter -> softmax)
-  float cw_red[2][4][8];    // converter group reduction scratch [parity][warp][value]
-  float sw_red[2][4][8];    // softmax group reduction scratch
-  int flag[2];              // split-unit "last arriver" broadcast
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[C::kSlots], s_empty[C::kSlots], p_full[C::kSlots], p_empty[C::kSlots];
+  uint64_t o_full[C::kSlots], o_empty[C::kSlots];
+  uint64_t sw_grp[kSoftmaxGroups], drain;
+  float sw_red[kSoftmaxGroups][2][4][8];  // reduction scratch [group][parity][warp][value]
+  int flag[kSoftmaxGroups];               // split-unit "last arriver" broadcast
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;
@@ -191,7 +229,8 @@ struct alignas(16) DecodeBarriers {
 template <int BITS, bool BF16>
 constexpr size_t decode_smem_layout_bytes() {
   using C = DecodeCfg<BITS, BF16>;
-  size_t b = (size_t)C::kStages * C::kStageBytes + 4 * (size_t)C::kBBytes + sizeof(DecodeBarriers<BITS, BF16>) +
+  size_t b = (size_t)C::kStages * C::kStageBytes + (2 + C::kSlots) * (size_t)C::kBBytes +
+             sizeof(DecodeBarriers<BITS, BF16>) +
              (2 * kMaxBatch + 1) * sizeof(int) + 1024;
   return b < 80 * 1024 ? 80 * 1024 : b;  // >= 80 KB keeps at most two CTAs per SM
 }
@@ -247,7 +286,40 @@ __device__ __forceinline__ float warp_maxf(float v) {
 
 __device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
 
+// Order-preserving integer key of a float, so that maxima can use redux.sync.
+__device__ __forceinline__ int fkey(float f) {
+  int b = __float_as_int(f);
+  return b ^ ((b >> 31) & 0x7fffffff);
+}
+__device__ __forceinline__ float unkey(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7fffffff)); }
+__device__ __forceinline__ float warp_max_redux(float f) { return unkey(__reduce_max_sync(FULL, fkey(f))); }
+
+// Largest of 128 non-negative fp16 values in shared memory; every warp that
+// calls it gets the same value without talking to the other warps.
+__device__ __forceinline__ float max_f16_128(const uint16_t* v) {
+  uint2 w = *reinterpret_cast<const uint2*>(v + 4 * lane_id());
+  uint32_t m = max(max(w.x & 0xffffu, w.x >> 16), max(w.y & 0xffffu, w.y >> 16));
+  return h2f((uint16_t)__reduce_max_sync(FULL, m));
+}
+
 __device__ __forceinline__ float bf2f(uint16_t bits) { return __uint_as_float((uint32_t)bits << 16); }
+
+// Per-(sequence, kv head) query statistics, computed by each warp on its own
+// (identical in every warp): qmax[h] = max_d |q[h, d]|, qsum[h] = sum_d q[h, d]
+// for NH consecutive query heads starting at qb (16-byte aligned rows of 128
+// bf16).
+template <int NH>
+__device__ __forceinline__ void unit_q_stats(const uint16_t* qb, bool need_sum, float (&qmax)[NH], float (&qsum)[NH]) {
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    uint2 w = *reinterpret_cast<const uint2*>(qb + h * kHeadDim + 4 * lane_id());
+    float x0 = bf2f((uint16_t)(w.x & 0xffffu)), x1 = bf2f((uint16_t)(w.x >> 16));
+    float x2 = bf2f((uint16_t)(w.y & 0xffffu)), x3 = bf2f((uint16_t)(w.y >> 16));
+    float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
+    qmax[h] = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(m)));
+    qsum[h] = need_sum ? warp_sum((x0 + x1) + (x2 + x3)) : 0.0f;
+  }
+}
 
 // Walks the global tile order (sequence-major, then KV head, then block).
 struct TileIter {
@@ -279,6 +351,16 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long T, int C) {
 }
 __device__ __forceinline__ long long range_start(int c, long long T, int C) { return (long long)c * T / C; }
 
+// Sum of the operand-split accumulator columns of head (2 * grp + k):
+// columns n = 4 * part + head.  Only compile-time indices touch acc[].
+template <bool BF16>
+__device__ __forceinline__ float split_sum(const uint32_t (&acc)[16], int grp, int k) {
+  const float h0 = __uint_as_float(acc[k]) + __uint_as_float(acc[4 + k]) + (BF16 ? 0.f : __uint_as_float(acc[8 + k]));
+  const float h1 = __uint_as_float(acc[2 + k]) + __uint_as_float(acc[6 + k]) +
+                   (BF16 ? 0.f : __uint_as_float(acc[10 + k]));
+  return grp ? h1 : h0;
+}
+
 // ================================================================= kernel
 template <int BITS, bool KCW, bool VCW, bool BF16>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeParams p) {
@@ -287,8 +369,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* stages = smem_raw;
   unsigned char* qop = stages + (size_t)C::kStages * C::kStageBytes;  // [2][kBBytes]
-  unsigned char* pop = qop + 2 * C::kBBytes;                          // [2][kBBytes]
-  Bars& sh = *reinterpret_cast<Bars*>(pop + 2 * C::kBBytes);
+  unsigned char* pop = qop + 2 * C::kBBytes;                          // [kSlots][kBBytes]
+  Bars& sh = *reinterpret_cast<Bars*>(pop + C::kSlots * C::kBBytes);
   int* prefix = reinterpret_cast<int*>(&sh + 1);  // [B + 1] tile offsets
   int* lens = prefix + (kMaxBatch + 1);           // [B] validated sequence lengths
 
@@ -300,19 +382,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
   // ------------------------------------------------------------ set-up
   if (tid == 0) {
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(&sh.stg_full[s], 1); mbar_init(&sh.stg_empty[s], 8); }
+    for (int s = 0; s < C::kStages; ++s) { mbar_init(&sh.stg_full[s], 1); mbar_init(&sh.stg_empty[s], 12); }
     for (int a = 0; a < C::kNA; ++a) {
       mbar_init(&sh.ak_full[a], 4); mbar_init(&sh.ak_empty[a], 1);
       mbar_init(&sh.av_full[a], 4); mbar_init(&sh.av_empty[a], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&sh.q_full[s], 4); mbar_init(&sh.q_empty[s], 1);
-      mbar_init(&sh.sd_full[s], 4); mbar_init(&sh.sd_empty[s], 4);
-      mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 4);
-      mbar_init(&sh.p_full[s], 4); mbar_init(&sh.p_empty[s], 1);
-      mbar_init(&sh.o_full[s], 1); mbar_init(&sh.o_empty[s], 4);
+    for (int s = 0; s < 2; ++s) { mbar_init(&sh.q_full[s], 4); mbar_init(&sh.q_empty[s], 1); }
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 8);
+      mbar_init(&sh.p_full[s], 8); mbar_init(&sh.p_empty[s], 1);
+      mbar_init(&sh.o_full[s], 1); mbar_init(&sh.o_empty[s], 8);
     }
-    mbar_init(&sh.cw_grp, 4); mbar_init(&sh.sw_grp, 4); mbar_init(&sh.drain, 1);
+    for (int g = 0; g < kSoftmaxGroups; ++g) mbar_init(&sh.sw_grp[g], 4);
+    mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_barrier_init();
   }
@@ -325,10 +407,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     }
     lens[b] = len;
   }
-  if (BF16) {  // N columns 8..15 of the BF16 operands stay zero
-    for (int i = tid; i < 4 * C::kBBytes / 16; i += kDecodeThreads)
-      reinterpret_cast<uint4*>(qop)[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
+  // operand columns nobody writes (N = 12..15, or 8..15 for BF16) stay zero
+  for (int i = tid; i < (2 + C::kSlots) * C::kBBytes / 16; i += kDecodeThreads)
+    reinterpret_cast<uint4*>(qop)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (warp == kWarpMma) { tmem_alloc(&sh.tmem_base, C::kTmemCols); tmem_relinquish(); }
   __syncthreads();
   if (tid == 0) {
@@ -359,17 +440,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   if (warp == kWarpLoad) {
     if (lane == 0 && ntiles > 0) {
       const uint64_t policy = l2_policy_evict_first();
-      int issued_parity[C::kStages];
-      for (int s = 0; s < C::kStages; ++s) issued_parity[s] = -1;
+      uint32_t issued = 0u, issued_par = 0u;  // per stage: a copy was issued / its phase parity
       TileIter it;
       it.init(prefix, B, Hkv, (int)g0);
       for (int t = 0; t < ntiles; ++t, it.next(prefix, B, Hkv)) {
         const int s = t % C::kStages;
         const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
+        KVQ_PT(le)
         if (!mbar_wait_bounded(&sh.stg_empty[s], ph ^ 1u, abort_flag, limit)) {
           set_abort(abort_flag, p.dev_status);
           break;
         }
+        KVQ_PA(0, le)
         if ((p.flags & KVQ_FLAG_TEST_STALL) && cta == 0 && t == 1) continue;  // withhold one tile
         int page = p.page_table ? p.page_table[(size_t)it.b * p.max_blocks + it.j] : it.b * p.max_blocks + it.j;
         if (page < 0 || page >= p.num_pages) {
@@ -389,57 +471,76 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                              policy);
         bulk_g2s_evict_first(sz + 3 * C::kSzBytes, p.v_zero + blk * kBlockTokens, C::kSzBytes, &sh.stg_full[s],
                              policy);
-        issued_parity[s] = (int)ph;
+        issued |= 1u << s;
+        issued_par = (issued_par & ~(1u << s)) | (ph << s);
       }
       // never leave a copy in flight: wait for every issued stage to land
       for (int s = 0; s < C::kStages; ++s)
-        if (issued_parity[s] >= 0) mbar_wait_bounded(&sh.stg_full[s], (uint32_t)issued_parity[s], nullptr, limit);
+        if (issued & (1u << s)) mbar_wait_bounded(&sh.stg_full[s], (issued_par >> s) & 1u, nullptr, limit);
     }
   }
   // ================================================================ MMA
+  // Issues QK^T of tile nq and PV of tile np in whatever order their inputs
+  // become ready (non-blocking tests), so neither product waits behind the
+  // other.  QK^T(t): A = K codes, B = Q', D = S slot.  PV(t): A = V codes,
+  // B = P', D = O slot.
   else if (warp == kWarpMma) {
     if (lane == 0 && ntiles > 0) {
       bool ok = true;
-      auto issue_pv = [&](int t) -> bool {
-        const int a = t % C::kNA, sl = t & 1;
-        const uint32_t pa = (uint32_t)(t / C::kNA) & 1u, p2 = (uint32_t)(t >> 1) & 1u;
-        if (!mbar_wait_bounded(&sh.av_full[a], pa, abort_flag, limit)) return false;
-        if (!mbar_wait_bounded(&sh.p_full[sl], p2, abort_flag, limit)) return false;
-        if (!mbar_wait_bounded(&sh.o_empty[sl], p2 ^ 1u, abort_flag, limit)) return false;
-        tc_fence_after();
-        const uint32_t b0 = smem_u32(pop + sl * C::kBBytes);
+      int nq = 0, np = 0;
+      uint64_t idle_since = 0;
+      while (np < ntiles) {
+        bool progressed = false;
+        if (np < nq) {
+          const int a = np % C::kNA, sl = np % C::kSlots;
+          const uint32_t pa = (uint32_t)(np / C::kNA) & 1u, ps4 = (uint32_t)(np / C::kSlots) & 1u;
+          if (mbar_test(&sh.av_full[a], pa) && mbar_test(&sh.p_full[sl], ps4) &&
+              mbar_test(&sh.o_empty[sl], ps4 ^ 1u)) {
+            tc_fence_after();
+            const uint32_t b0 = smem_u32(pop + sl * C::kBBytes);
 #pragma unroll
-        for (int k = 0; k < C::kKSteps; ++k) {
-          uint64_t bd = make_smem_desc(b0 + k * C::kKStepBBytes, C::kLbo, C::kSbo);
-          uint32_t d = tmem + C::kColO + 16 * sl, av = tmem + C::kColAV + a * C::kACols + 8 * k;
-          if (BF16) mma_f16_ts(d, av, bd, C::kIdesc, k > 0); else mma_f8f6f4_ts(d, av, bd, C::kIdesc, k > 0);
+            for (int k = 0; k < C::kKSteps; ++k) {
+              uint64_t bd = make_smem_desc(b0 + k * C::kKStepBBytes, C::kLbo, C::kSbo);
+              uint32_t d = tmem + C::kColO + 16 * sl, av = tmem + C::kColAV + a * C::kACols + 8 * k;
+              if (BF16) mma_f16_ts(d, av, bd, C::kIdesc, k > 0); else mma_f8f6f4_ts(d, av, bd, C::kIdesc, k > 0);
+            }
+            tc_commit(&sh.av_empty[a]);
+            tc_commit(&sh.p_empty[sl]);
+            tc_commit(&sh.o_full[sl]);
+            ++np;
+            progressed = true;
+          }
         }
-        tc_commit(&sh.av_empty[a]);
-        tc_commit(&sh.p_empty[sl]);
-        tc_commit(&sh.o_full[sl]);
-        return true;
-      };
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const int a = t % C::kNA, sl = t & 1;
-        const uint32_t pa = (uint32_t)(t / C::kNA) & 1u, p2 = (uint32_t)(t >> 1) & 1u;
-        ok = mbar_wait_bounded(&sh.ak_full[a], pa, abort_flag, limit) &&
-             mbar_wait_bounded(&sh.q_full[sl], p2, abort_flag, limit) &&
-             mbar_wait_bounded(&sh.s_empty[sl], p2 ^ 1u, abort_flag, limit);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t b0 = smem_u32(qop + sl * C::kBBytes);
+        if (nq < ntiles) {
+          const int a = nq % C::kNA, sl = nq % C::kSlots, q2 = nq & 1;
+          const uint32_t pa = (uint32_t)(nq / C::kNA) & 1u, ps4 = (uint32_t)(nq / C::kSlots) & 1u,
+                         p2 = (uint32_t)(nq >> 1) & 1u;
+          if (mbar_test(&sh.ak_full[a], pa) && mbar_test(&sh.q_full[q2], p2) &&
+              mbar_test(&sh.s_empty[sl], ps4 ^ 1u)) {
+            tc_fence_after();
+            const uint32_t b0 = smem_u32(qop + q2 * C::kBBytes);
 #pragma unroll
-        for (int k = 0; k < C::kKSteps; ++k) {
-          uint64_t bd = make_smem_desc(b0 + k * C::kKStepBBytes, C::kLbo, C::kSbo);
-          uint32_t d = tmem + C::kColS + 16 * sl, ak = tmem + C::kColAK + a * C::kACols + 8 * k;
-          if (BF16) mma_f16_ts(d, ak, bd, C::kIdesc, k > 0); else mma_f8f6f4_ts(d, ak, bd, C::kIdesc, k > 0);
+            for (int k = 0; k < C::kKSteps; ++k) {
+              uint64_t bd = make_smem_desc(b0 + k * C::kKStepBBytes, C::kLbo, C::kSbo);
+              uint32_t d = tmem + C::kColS + 16 * sl, ak = tmem + C::kColAK + a * C::kACols + 8 * k;
+              if (BF16) mma_f16_ts(d, ak, bd, C::kIdesc, k > 0); else mma_f8f6f4_ts(d, ak, bd, C::kIdesc, k > 0);
+            }
+            tc_commit(&sh.ak_empty[a]);
+            tc_commit(&sh.q_empty[q2]);
+            tc_commit(&sh.s_full[sl]);
+            ++nq;
+            progressed = true;
+          }
         }
-        tc_commit(&sh.ak_empty[a]);
-        tc_commit(&sh.q_empty[sl]);
-        tc_commit(&sh.s_full[sl]);
-        if (t > 0) ok = issue_pv(t - 1);
+        if (progressed) {
+          idle_since = 0;
+        } else {
+          __nanosleep(20);  // back off: leave issue slots to the warps sharing this sub-partition
+          const uint64_t now = globaltimer_ns();
+          if (idle_since == 0) idle_since = now;
+          if (*abort_flag || now - idle_since > limit) { ok = false; break; }
+        }
       }
-      if (ok) ok = issue_pv(ntiles - 1);
       if (!ok) set_abort(abort_flag, p.dev_status);
       // drain: all issued MMAs complete before tensor memory is released
       tc_commit(&sh.drain);
@@ -448,193 +549,173 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   }
   // ========================================================== converters
   else if (warp < kWarpSoftmax0) {
-    const int r = tid;  // tensor-memory lane = A row = Q' channel
+    const int r = tid;  // tensor-memory lane = A row; also this thread's channel of Q'
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    uint32_t grp_phase = 0;
-    float qv[4] = {0.f, 0.f, 0.f, 0.f};  // q[b, 4h + i, r]
-    uint4 qtok = make_uint4(0u, 0u, 0u, 0u);  // token-wise K: this channel's Q' row
-    float tok_mult[4], tok_add[4];
     const int qrow = a_pos<BITS, BF16>(r);
+    float qv[4] = {0.f, 0.f, 0.f, 0.f};    // q[b, 4h + i, r]
+    float qmax[4] = {0.f, 0.f, 0.f, 0.f};  // per-unit max |q|
+    int seg = -1, slot_seg0 = -2, slot_seg1 = -2;  // Q' slot contents (token-wise K: constant per segment)
     TileIter it;
     if (ntiles > 0) it.init(prefix, B, Hkv, (int)g0);
     for (int t = 0; t < ntiles; ++t, it.next(prefix, B, Hkv)) {
       const int s = t % C::kStages, a = t % C::kNA, sl = t & 1;
       const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNA) & 1u,
                      p2 = (uint32_t)(t >> 1) & 1u;
-      const bool seg_first = (t == 0) || it.j == 0;
+      KVQ_PT(c0)
       if (!warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) { set_abort(abort_flag, p.dev_status); break; }
+      KVQ_PA(1, c0)
       const unsigned char* st = stages + (size_t)s * C::kStageBytes;
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
-      const uint16_t* kz = ks + kBlockTokens;
-
-      // ---- K codes -> A_K[a] (row r = token r)
-      if (!warp_wait(&sh.ak_empty[a], pa ^ 1u, abort_flag, limit)) { set_abort(abort_flag, p.dev_status); break; }
-      {
-        uint32_t o[C::kACols];
+      if (t == 0 || it.j == 0) {  // new (sequence, kv head): its four query rows
+        ++seg;
+        const uint16_t* qb = p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim;
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-          uint4 v = *reinterpret_cast<const uint4*>(st + ((size_t)c * kBlockTokens + r) * 16);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) Convert<BITS, BF16>::run(w[i], &o[(4 * c + i) * Convert<BITS, BF16>::kOut]);
-        }
-        const uint32_t col = tmem + lane_off + C::kColAK + a * C::kACols;
-#pragma unroll
-        for (int c0 = 0; c0 < C::kACols; c0 += 32)
-          tmem_st_32x32b_x32(col + c0, *reinterpret_cast<const uint32_t(*)[32]>(&o[c0]));
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.ak_full[a]);
+        for (int i = 0; i < 4; ++i) qv[i] = bf2f(qb[i * kHeadDim + r]);
+        float qsum[4];
+        unit_q_stats(qb, false, qmax, qsum);
       }
 
-      // ---- Q' operand and score constants for this tile
-      if (seg_first) {
-        const uint16_t* qsrc = p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim + r;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) qv[i] = bf2f(qsrc[i * kHeadDim]);
-        if (!KCW) {  // token-wise K: Q' = q (prescaled), constant over the segment
-          float m[4], sm[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) { m[i] = warp_maxf(fabsf(qv[i])); sm[i] = warp_sum(qv[i]); }
-          float* red = sh.cw_red[grp_phase][warp];
-          if (lane == 0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) { red[i] = m[i]; red[4 + i] = sm[i]; }
-          }
-          const uint32_t use = grp_phase;
-          if (!group_sync(&sh.cw_grp, grp_phase, abort_flag, limit)) { set_abort(abort_flag, p.dev_status); break; }
-          float qs[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float mx = 0.f, su = 0.f;
-#pragma unroll
-            for (int w = 0; w < 4; ++w) { mx = fmaxf(mx, sh.cw_red[use][w][i]); su += sh.cw_red[use][w][4 + i]; }
-            qs[i] = BF16 ? 1.0f : pow2_prescale(mx);
-            tok_mult[i] = C::kCodeInv / qs[i] * p.sm_scale_log2;
-            tok_add[i] = su * p.sm_scale_log2;
-          }
-          float4 v = make_float4(qv[0] * qs[0], qv[1] * qs[1], qv[2] * qs[2], qv[3] * qs[3]);
-          qtok = BF16 ? split2_bf16(v) : split3_e4m3(v);
-        }
-      }
-      if (!warp_wait(&sh.q_empty[sl], p2 ^ 1u, abort_flag, limit) ||
-          !warp_wait(&sh.sd_empty[sl], p2 ^ 1u, abort_flag, limit)) {
-        set_abort(abort_flag, p.dev_status);
-        break;
-      }
-      uint4 qrow_bytes;
-      float mult[4], add[4];
-      if (!KCW) {
-        qrow_bytes = qtok;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) { mult[i] = tok_mult[i]; add[i] = tok_add[i]; }
-      } else {  // channel-wise K: Q' = q * s_g (operand fold), offset q . z_g
-        const float sd = h2f(ks[r]), zd = h2f(kz[r]);
-        float qf[4], m[4], sm[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          qf[i] = qv[i] * sd;
-          m[i] = warp_maxf(fabsf(qf[i]));
-          sm[i] = warp_sum(qv[i] * zd);
-        }
-        float* red = sh.cw_red[grp_phase][warp];
-        if (lane == 0) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) { red[i] = m[i]; red[4 + i] = sm[i]; }
-        }
-        const uint32_t use = grp_phase;
-        if (!group_sync(&sh.cw_grp, grp_phase, abort_flag, limit)) { set_abort(abort_flag, p.dev_status); break; }
+      // ---- Q' operand: token-wise K uses q (written once per segment per
+      // slot); channel-wise K folds this group's scales into q.
+      KVQ_PT(c4)
+      if (!warp_wait(&sh.q_empty[sl], p2 ^ 1u, abort_flag, limit)) { set_abort(abort_flag, p.dev_status); break; }
+      KVQ_PA(5, c4)
+      KVQ_PT(c3)
+      if (KCW || (sl ? slot_seg1 : slot_seg0) != seg) {
+        float sd = 1.0f, smax = 1.0f;
+        if (KCW) { sd = h2f(ks[r]); smax = max_f16_128(ks); }
         float qs[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float mx = 0.f, su = 0.f;
-#pragma unroll
-          for (int w = 0; w < 4; ++w) { mx = fmaxf(mx, sh.cw_red[use][w][i]); su += sh.cw_red[use][w][4 + i]; }
-          qs[i] = BF16 ? 1.0f : pow2_prescale(mx);
-          mult[i] = C::kCodeInv / qs[i] * p.sm_scale_log2;
-          add[i] = su * p.sm_scale_log2;
-        }
-        float4 v = make_float4(qf[0] * qs[0], qf[1] * qs[1], qf[2] * qs[2], qf[3] * qs[3]);
-        qrow_bytes = BF16 ? split2_bf16(v) : split3_e4m3(v);
+        for (int i = 0; i < 4; ++i) qs[i] = BF16 ? 1.0f : pow2_prescale(qmax[i] * smax);
+        float4 v = make_float4(qv[0] * sd * qs[0], qv[1] * sd * qs[1], qv[2] * sd * qs[2], qv[3] * sd * qs[3]);
+        *reinterpret_cast<uint4*>(qop + sl * C::kBBytes + b_row_off<BF16>(qrow)) =
+            BF16 ? split2_bf16(v) : split3_e4m3(v);
+        fence_proxy_async_smem();
+        if (sl) slot_seg1 = seg; else slot_seg0 = seg;
       }
-      *reinterpret_cast<uint4*>(qop + sl * C::kBBytes + b_row_off<BF16>(qrow)) = qrow_bytes;
-      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.q_full[sl]);
-      if (tid == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) { sh.side[sl][i] = mult[i]; sh.side[sl][4 + i] = add[i]; }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.sd_full[sl]);
+      KVQ_PA(4, c3)
 
-      // ---- V codes -> A_V[a] (row r = channel r)
-      if (!warp_wait(&sh.av_empty[a], pa ^ 1u, abort_flag, limit)) { set_abort(abort_flag, p.dev_status); break; }
-      {
-        uint32_t o[C::kACols];
+      // ---- K codes -> A_K[a] (row r = token r), V codes -> A_V[a] (row r = channel r).
+      // K is handed to the MMA before V's buffer is awaited, so QK^T never
+      // waits for an earlier tile's PV.
+      KVQ_PT(c2)
+      bool stalled = false;
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-          uint4 v = *reinterpret_cast<const uint4*>(st + C::kBlockBytes + ((size_t)c * kBlockTokens + r) * 16);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int kv = 0; kv < 2; ++kv) {
+        KVQ_PT(cw)
+        if (!warp_wait(kv ? &sh.av_empty[a] : &sh.ak_empty[a], pa ^ 1u, abort_flag, limit)) { stalled = true; break; }
+        KVQ_PA(kv ? 6 : 2, cw)
+        KVQ_PT(cc)
+        constexpr int kPasses = C::kACols / 32, kPerPass = C::kChunks / kPasses;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) Convert<BITS, BF16>::run(w[i], &o[(4 * c + i) * Convert<BITS, BF16>::kOut]);
+        for (int ps2 = 0; ps2 < kPasses; ++ps2) {
+          uint32_t o[32];
+#pragma unroll
+          for (int c = 0; c < kPerPass; ++c) {
+            uint4 v = *reinterpret_cast<const uint4*>(
+                st + kv * C::kBlockBytes + ((size_t)(ps2 * kPerPass + c) * kBlockTokens + r) * 16);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) Convert<BITS, BF16>::run(w[i], &o[(4 * c + i) * Convert<BITS, BF16>::kOut]);
+          }
+          tmem_st_32x32b_x32(tmem + lane_off + (kv ? C::kColAV : C::kColAK) + a * C::kACols + 32 * ps2, o);
         }
-        const uint32_t col = tmem + lane_off + C::kColAV + a * C::kACols;
-#pragma unroll
-        for (int c0 = 0; c0 < C::kACols; c0 += 32)
-          tmem_st_32x32b_x32(col + c0, *reinterpret_cast<const uint32_t(*)[32]>(&o[c0]));
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) { mbar_arrive(&sh.av_full[a]); mbar_arrive(&sh.stg_empty[s]); }
+        if (kv == 0) {  // K first: QK^T need not wait for V's buffer
+          tc_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.ak_full[a]);
+        }
+        KVQ_PA(kv ? 8 : 7, cc)
       }
+      KVQ_PT(cf)
+      if (stalled) { set_abort(abort_flag, p.dev_status); break; }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sh.av_full[a]);
+        mbar_arrive(&sh.stg_empty[s]);
+      }
+      KVQ_PA(9, cf)
+      KVQ_PA(3, c2)
     }
   }
   // ============================================================= softmax
   else {
-    const int i = tid - kWarpSoftmax0 * 32;  // tensor-memory lane: token (scores) / channel (output)
-    const int sw = warp - kWarpSoftmax0;
+    constexpr int NH = kHeadsPerGroup;
+    const int swt = tid - kWarpSoftmax0 * 32;
+    const int grp = swt >> 7;                // head group: heads hbase, hbase + 1
+    const int i = swt & 127;                 // tensor-memory lane: token (scores) / channel (output)
+    const int sw = i >> 5;                   // warp within the group = lane quarter
+    const int hbase = grp * NH;
     const uint32_t lane_off = (uint32_t)(sw * 32) << 16;
     const int prow = a_pos<BITS, BF16>(i);
+    uint64_t* gbar = &sh.sw_grp[grp];
     uint32_t grp_phase = 0;
     const float kLn2 = 0.69314718055994530942f;
+    const float kFix = 67108864.0f;  // 2^26: fixed-point scale of p for integer warp sums
 
     // empty sequences: out = 0, lse = -inf
     for (int b = cta; b < B; b += (int)gridDim.x) {
       if (lens[b] != 0) continue;
-      for (int hq = 0; hq < p.num_q_heads; ++hq) {
+      for (int hq = grp; hq < p.num_q_heads; hq += kSoftmaxGroups) {
         p.out[((size_t)b * p.num_q_heads + hq) * kHeadDim + i] = 0.0f;
         if (i == 0) p.lse[(size_t)b * p.num_q_heads + hq] = -INFINITY;
       }
     }
 
-    float m[4], lp[4], zp[4], O[4];          // running max (log2), partial sum, partial sum(p z), output
-    float a_prev[4], ts_prev[4], pinv_prev = 0.f, sv_prev = 0.f, zv_prev = 0.f;  // deferred epilogue inputs
+    float m[NH], lp[NH], zp[NH], O[NH];  // running max (log2 units), partial sum p, partial sum p*z, output
+    float a_prev[NH], ws_prev[NH];       // deferred epilogue inputs
+    float pinv_prev = 0.f, sv_prev = 0.f, zv_prev = 0.f;
+    float qi[NH], qmax[NH], mult[NH], add[NH];
+#pragma unroll
+    for (int k = 0; k < NH; ++k) { qi[k] = 0.f; qmax[k] = 0.f; mult[k] = 0.f; add[k] = 0.f; ws_prev[k] = 0.f; }
     auto reset = [&]() {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) { m[k] = -INFINITY; lp[k] = 0.f; zp[k] = 0.f; O[k] = 0.f; }
+      for (int k = 0; k < NH; ++k) { m[k] = -INFINITY; lp[k] = 0.f; zp[k] = 0.f; O[k] = 0.f; }
     };
     reset();
 
+    // Cross-warp sum of the previous tile's per-warp p sums (channel-wise V).
+    auto combine_prev_sums = [&](float (&ts)[NH]) -> bool {
+      float* red = sh.sw_red[grp][grp_phase][sw];
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < NH; ++k) red[k] = ws_prev[k];
+      }
+      const uint32_t use = grp_phase;
+      if (!group_sync(gbar, grp_phase, abort_flag, limit)) return false;
+#pragma unroll
+      for (int k = 0; k < NH; ++k)
+        ts[k] = (sh.sw_red[grp][use][0][k] + sh.sw_red[grp][use][1][k]) +
+                (sh.sw_red[grp][use][2][k] + sh.sw_red[grp][use][3][k]);
+      return true;
+    };
+
     // PV epilogue of tile t: O = O * alpha + folded partial product
-    auto epilogue = [&](int t) -> bool {
-      const int sl = t & 1;
-      const uint32_t p2 = (uint32_t)(t >> 1) & 1u;
+    auto epilogue = [&](int t, const float (&ts)[NH]) -> bool {
+      const int sl = t % C::kSlots;
+      const uint32_t p2 = (uint32_t)(t / C::kSlots) & 1u;
+      KVQ_PT(e0)
       if (!warp_wait(&sh.o_full[sl], p2, abort_flag, limit)) return false;
+      KVQ_PA(23, e0)
       tc_fence_after();
       uint32_t acc[16];
+      KVQ_PT(el)
       tmem_ld_32x32b_x16(tmem + lane_off + C::kColO + 16 * sl, acc);
       tc_wait_ld();
+      KVQ_PA(27, el)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.o_empty[sl]);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float o = __uint_as_float(acc[k]) + __uint_as_float(acc[4 + k]);
-        if (!BF16) o += __uint_as_float(acc[8 + k]);
+      for (int k = 0; k < NH; ++k) {
+        float o = split_sum<BF16>(acc, grp, k);
         o *= pinv_prev;
-        if (VCW) O[k] = fmaf(O[k], a_prev[k], fmaf(sv_prev, o, zv_prev * ts_prev[k]));
+        if (VCW) O[k] = fmaf(O[k], a_prev[k], fmaf(sv_prev, o, zv_prev * ts[k]));
         else O[k] = fmaf(O[k], a_prev[k], o);
       }
       return true;
@@ -642,60 +723,58 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
     // finish a (sequence, kv head) segment: normalise, store or merge
     auto finalize = [&](int b, int h, bool first_global, bool last_global, long long ustart, long long uend) -> bool {
-      float lsum[4], zsum[4];
+      float lsum[NH], zsum[NH];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) { lsum[k] = warp_sum(lp[k]); zsum[k] = VCW ? 0.f : warp_sum(zp[k]); }
-      float* red = sh.sw_red[grp_phase][sw];
+      for (int k = 0; k < NH; ++k) { lsum[k] = warp_sum(lp[k]); zsum[k] = VCW ? 0.f : warp_sum(zp[k]); }
+      float* red = sh.sw_red[grp][grp_phase][sw];
       if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) { red[k] = lsum[k]; red[4 + k] = zsum[k]; }
+        for (int k = 0; k < NH; ++k) { red[k] = lsum[k]; red[NH + k] = zsum[k]; }
       }
       const uint32_t use = grp_phase;
-      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
-      float res[4], lse2[4];
+      if (!group_sync(gbar, grp_phase, abort_flag, limit)) return false;
+      float res[NH], lse2[NH];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < NH; ++k) {
         float l = 0.f, z = 0.f;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) { l += sh.sw_red[use][w][k]; z += sh.sw_red[use][w][4 + k]; }
+        for (int w = 0; w < 4; ++w) { l += sh.sw_red[grp][use][w][k]; z += sh.sw_red[grp][use][w][NH + k]; }
         res[k] = (O[k] + z) / l;
         lse2[k] = m[k] + __log2f(l);
       }
-      const size_t row0 = (size_t)b * p.num_q_heads + (size_t)h * kGroupQ;
+      const size_t row0 = (size_t)b * p.num_q_heads + (size_t)h * kGroupQ + hbase;
       if (first_global && last_global) {  // whole (sequence, head) in this CTA
 #pragma unroll
-        for (int k = 0; k < 4; ++k) p.out[(row0 + k) * kHeadDim + i] = res[k];
-        if (i < 4) p.lse[row0 + i] = lse2[i] * kLn2;
+        for (int k = 0; k < NH; ++k) p.out[(row0 + k) * kHeadDim + i] = res[k];
+        if (i < NH) p.lse[row0 + i] = (i == 0 ? lse2[0] : lse2[NH - 1]) * kLn2;
         return true;
       }
-      // split: publish this part, the last part to arrive merges all parts
+      // split: publish this part; the last part to arrive merges all parts
       const int c_first = cta_of_tile(ustart, T, Cn), c_last = cta_of_tile(uend - 1, T, Cn);
       const int slot = (ustart <= g0) ? 0 : 1;
-      float* po = p.part_o + ((size_t)cta * 2 + slot) * kGroupQ * kHeadDim;
+      float* po = p.part_o + (((size_t)cta * 2 + slot) * kGroupQ + hbase) * kHeadDim;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) po[k * kHeadDim + i] = res[k];
-      if (i < 4) p.part_lse[((size_t)cta * 2 + slot) * kGroupQ + i] = lse2[i] * kLn2;
+      for (int k = 0; k < NH; ++k) po[k * kHeadDim + i] = res[k];
+      if (i < NH) p.part_lse[((size_t)cta * 2 + slot) * kGroupQ + hbase + i] = (i == 0 ? lse2[0] : lse2[NH - 1]) * kLn2;
       __threadfence();
-      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
-      const int u = b * Hkv + h;
+      if (!group_sync(gbar, grp_phase, abort_flag, limit)) return false;
+      const int u = (b * Hkv + h) * kSoftmaxGroups + grp;
       if (i == 0) {
         int old = atomicAdd(&p.counters[u], 1);
-        sh.flag[use] = (old == c_last - c_first) ? 1 : 0;
+        sh.flag[grp] = (old == c_last - c_first) ? 1 : 0;
       }
-      const uint32_t use2 = grp_phase;
-      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
-      if (!sh.flag[use]) return true;
-      (void)use2;
+      if (!group_sync(gbar, grp_phase, abort_flag, limit)) return false;
+      if (!sh.flag[grp]) return true;
       __threadfence();
-      float mx[4], den[4], acc[4];
+      float mx[NH], den[NH], acc[NH];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) { mx[k] = -INFINITY; den[k] = 0.f; acc[k] = 0.f; }
+      for (int k = 0; k < NH; ++k) { mx[k] = -INFINITY; den[k] = 0.f; acc[k] = 0.f; }
       for (int c = c_first; c <= c_last; ++c) {
         const int sl2 = (ustart <= range_start(c, T, Cn)) ? 0 : 1;
-        const float* pl = p.part_lse + ((size_t)c * 2 + sl2) * kGroupQ;
-        const float* pv = p.part_o + ((size_t)c * 2 + sl2) * kGroupQ * kHeadDim;
+        const float* pl = p.part_lse + ((size_t)c * 2 + sl2) * kGroupQ + hbase;
+        const float* pv = p.part_o + (((size_t)c * 2 + sl2) * kGroupQ + hbase) * kHeadDim;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < NH; ++k) {
           float l = __ldcg(pl + k), v = __ldcg(pv + k * kHeadDim + i);
           float nm = fmaxf(mx[k], l);
           float sc = __expf(mx[k] - nm), w = __expf(l - nm);
@@ -705,8 +784,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         }
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) p.out[(row0 + k) * kHeadDim + i] = acc[k] / den[k];
-      if (i < 4) p.lse[row0 + i] = mx[i] + __logf(den[i]);
+      for (int k = 0; k < NH; ++k) {
+        p.out[(row0 + k) * kHeadDim + i] = acc[k] / den[k];
+        if (i == k) p.lse[row0 + k] = mx[k] + __logf(den[k]);
+      }
       if (i == 0) p.counters[u] = 0;
       return true;
     };
@@ -719,124 +800,176 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     long long pus = 0, pue = 0;
     bool ok = true;
     for (int t = 0; t < ntiles && ok; ++t, it.next(prefix, B, Hkv)) {
-      const int s = t % C::kStages, sl = t & 1;
-      const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, p2 = (uint32_t)(t >> 1) & 1u;
+      const int s = t % C::kStages, sl = t % C::kSlots;
+      const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, p2 = (uint32_t)(t / C::kSlots) & 1u;
       const long long g = g0 + t;
       const long long ustart = g - it.j, uend = ustart + it.nblk;
       const bool seg_first = (t == 0) || it.j == 0;
       if (seg_first && pend >= 0) {  // close the previous segment
-        ok = epilogue(pend) && finalize(pb, ph, pfirst, pue <= g1, pus, pue);
+        KVQ_PT(f0)
+        float ts[NH];
+#pragma unroll
+        for (int k = 0; k < NH; ++k) ts[k] = 0.f;
+        ok = (!VCW || combine_prev_sums(ts)) && epilogue(pend, ts) && finalize(pb, ph, pfirst, pue <= g1, pus, pue);
+        KVQ_PA(24, f0)
         if (!ok) break;
         reset();
         pend = -1;
       }
-      if (seg_first) { pb = it.b; ph = it.h; pfirst = ustart >= g0; pus = ustart; pue = uend; }
+      if (seg_first) {
+        pb = it.b; ph = it.h; pfirst = ustart >= g0; pus = ustart; pue = uend;
+        const uint16_t* qb = p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ + hbase) * kHeadDim;
+        float qsum[NH];
+        unit_q_stats<NH>(qb, !KCW, qmax, qsum);
+#pragma unroll
+        for (int k = 0; k < NH; ++k) {
+          if (KCW) {
+            qi[k] = bf2f(qb[k * kHeadDim + i]);
+          } else {  // token-wise K: S = s_l * (q . code) + z_l * sum(q), constant factors per segment
+            const float qs = BF16 ? 1.0f : pow2_prescale(qmax[k]);
+            mult[k] = C::kCodeInv / qs * p.sm_scale_log2;
+            add[k] = qsum[k] * p.sm_scale_log2;
+          }
+        }
+      }
       const int nvalid = min(kBlockTokens, lens[it.b] - it.j * kBlockTokens);
 
       // ---- scores of this tile (lane i = token i)
-      if (!warp_wait(&sh.s_full[sl], p2, abort_flag, limit) || !warp_wait(&sh.stg_full[s], ps, abort_flag, limit) ||
-          !warp_wait(&sh.sd_full[sl], p2, abort_flag, limit)) { ok = false; break; }
+      KVQ_PT(s0)
+      if (!warp_wait(&sh.s_full[sl], p2, abort_flag, limit) || !warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) {
+        ok = false;
+        break;
+      }
+      KVQ_PA(16, s0)
+      KVQ_PT(s1)
       tc_fence_after();
       uint32_t acc[16];
+      KVQ_PT(sl0)
       tmem_ld_32x32b_x16(tmem + lane_off + C::kColS + 16 * sl, acc);
-      tc_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.s_empty[sl]);
-      float mult[4], add[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) { mult[k] = sh.side[sl][k]; add[k] = sh.side[sl][4 + k]; }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.sd_empty[sl]);
       const unsigned char* st = stages + (size_t)s * C::kStageBytes;
       const uint16_t* szp = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
       const float ks_i = h2f(szp[i]), kz_i = h2f(szp[kBlockTokens + i]);
       const float vs_i = h2f(szp[2 * kBlockTokens + i]), vz_i = h2f(szp[3 * kBlockTokens + i]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.stg_empty[s]);
-
-      const bool valid = i < nvalid;
-      float sc[4];
+      const uint32_t vs_bits = szp[2 * kBlockTokens + i];
+      if (KCW) {  // this group's Q' prescale (the value the converters used)
+        const float smax = max_f16_128(szp);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float a = __uint_as_float(acc[k]) + __uint_as_float(acc[4 + k]);
-        if (!BF16) a += __uint_as_float(acc[8 + k]);
-        float v = KCW ? fmaf(a, mult[k], add[k]) : fmaf(a * mult[k], ks_i, kz_i * add[k]);
-        sc[k] = valid ? v : -INFINITY;
-      }
-      // tile maxima (4 heads) and, for token-wise V, the largest scale
-      float* red = sh.sw_red[grp_phase][sw];
-      {
-        float tm[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tm[k] = warp_maxf(sc[k]);
-        float smax = VCW ? 0.f : warp_maxf(valid ? vs_i : 0.f);
-        if (lane == 0) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) red[k] = tm[k];
-          red[4] = smax;
+        for (int k = 0; k < NH; ++k) {
+          const float qs = BF16 ? 1.0f : pow2_prescale(qmax[k] * smax);
+          mult[k] = C::kCodeInv / qs * p.sm_scale_log2;
         }
       }
-      uint32_t use = grp_phase;
-      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) { ok = false; break; }
-      float alpha[4], pr[4], smax = 0.f;
+      tc_wait_ld();
+      KVQ_PA(25, sl0)
+      KVQ_PT(sl1)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) { mbar_arrive(&sh.s_empty[sl]); mbar_arrive(&sh.stg_empty[s]); }
+
+      const bool valid = i < nvalid;
+      float sc[NH];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float tmx = -INFINITY;
+      for (int k = 0; k < NH; ++k) {
+        float a = split_sum<BF16>(acc, grp, k);
+        // channel-wise K adds q . z_g (below, once reduced over channels)
+        float v = KCW ? a * mult[k] : fmaf(a * mult[k], ks_i, kz_i * add[k]);
+        sc[k] = valid ? v : -INFINITY;
+      }
+      // one reduction round: tile maxima, channel-wise K offsets q . z_g,
+      // token-wise V largest scale, channel-wise V previous tile's sum(p)
+      {
+        float* red = sh.sw_red[grp][grp_phase][sw];
+        float tm[NH], cg[NH];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) tmx = fmaxf(tmx, sh.sw_red[use][w][k]);
-        const float mn = fmaxf(m[k], tmx);
+        for (int k = 0; k < NH; ++k) tm[k] = warp_max_redux(sc[k]);
+        if (KCW) {
+#pragma unroll
+          for (int k = 0; k < NH; ++k) cg[k] = warp_sum(qi[k] * kz_i);
+        }
+        const uint32_t vmax = VCW ? 0u : __reduce_max_sync(FULL, vs_bits);
+        if (lane == 0) {
+#pragma unroll
+          for (int k = 0; k < NH; ++k) {
+            red[k] = tm[k];
+            if (KCW) red[NH + k] = cg[k];
+            if (VCW) red[2 * NH + k] = ws_prev[k];
+          }
+          red[3 * NH] = __uint_as_float(vmax);
+        }
+      }
+      const uint32_t use = grp_phase;
+      KVQ_PA(26, sl1)
+      KVQ_PA(17, s1)
+      KVQ_PT(s2)
+      if (!group_sync(gbar, grp_phase, abort_flag, limit)) { ok = false; break; }
+      KVQ_PA(18, s2)
+      KVQ_PT(s3)
+      const float (*rd)[8] = sh.sw_red[grp][use];
+      float alpha[NH], pr[NH], ts_prev[NH];
+#pragma unroll
+      for (int k = 0; k < NH; ++k) {
+        const float tmx = fmaxf(fmaxf(rd[0][k], rd[1][k]), fmaxf(rd[2][k], rd[3][k]));
+        const float cgs = KCW ? ((rd[0][NH + k] + rd[1][NH + k]) + (rd[2][NH + k] + rd[3][NH + k])) * p.sm_scale_log2
+                              : 0.0f;
+        ts_prev[k] = VCW ? (rd[0][2 * NH + k] + rd[1][2 * NH + k]) + (rd[2][2 * NH + k] + rd[3][2 * NH + k]) : 0.f;
+        const float mn = fmaxf(m[k], tmx + cgs);
         alpha[k] = exp2f(m[k] - mn);
         m[k] = mn;
-        pr[k] = exp2f(sc[k] - mn);
+        pr[k] = exp2f(sc[k] + cgs - mn);
         lp[k] = fmaf(lp[k], alpha[k], pr[k]);
         if (!VCW) zp[k] = fmaf(zp[k], alpha[k], pr[k] * vz_i);
       }
+      float smax_v = 0.f;
       if (!VCW) {
+        uint32_t mv = 0u;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) smax = fmaxf(smax, sh.sw_red[use][w][4]);
+        for (int w = 0; w < 4; ++w) mv = max(mv, __float_as_uint(rd[w][3 * NH]));
+        smax_v = h2f((uint16_t)mv);
       }
       // P' operand (lane i = token i): token-wise V folds s into P
-      const float pscale = VCW ? 256.0f : (BF16 ? 1.0f : pow2_prescale(smax));
+      const float pscale = VCW ? 256.0f : (BF16 ? 1.0f : pow2_prescale(smax_v));
       const float pmul = VCW ? pscale : vs_i * pscale;
-      float4 pv = make_float4(pr[0] * pmul, pr[1] * pmul, pr[2] * pmul, pr[3] * pmul);
-      uint4 prow_bytes = BF16 ? split2_bf16(pv) : split3_e4m3(pv);
+      const float2 pv = make_float2(pr[0] * pmul, pr[NH - 1] * pmul);
+      KVQ_PA(19, s3)
+      KVQ_PT(s4)
       if (!warp_wait(&sh.p_empty[sl], p2 ^ 1u, abort_flag, limit)) { ok = false; break; }
-      *reinterpret_cast<uint4*>(pop + sl * C::kBBytes + b_row_off<BF16>(prow)) = prow_bytes;
+      KVQ_PA(20, s4)
+      unsigned char* prow_ptr = pop + sl * C::kBBytes + b_row_off<BF16>(prow);
+      if (BF16) {  // column n = 4 * part + head: parts at byte 8 * part + 2 * head
+        const uint2 w = split2_bf16_x2(pv);
+        *reinterpret_cast<uint32_t*>(prow_ptr + 2 * hbase) = w.x;
+        *reinterpret_cast<uint32_t*>(prow_ptr + 8 + 2 * hbase) = w.y;
+      } else {     // column n = 4 * part + head: one byte each
+        const uint3 w = split3_e4m3_x2(pv);
+        *reinterpret_cast<uint16_t*>(prow_ptr + hbase) = (uint16_t)w.x;
+        *reinterpret_cast<uint16_t*>(prow_ptr + 4 + hbase) = (uint16_t)w.y;
+        *reinterpret_cast<uint16_t*>(prow_ptr + 8 + hbase) = (uint16_t)w.z;
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.p_full[sl]);
 
-      // channel-wise V needs this group's sum(p) for its offset term
-      float tsum[4] = {0.f, 0.f, 0.f, 0.f};
-      if (VCW) {
-        float ws[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) ws[k] = warp_sum(pr[k]);
-        red = sh.sw_red[grp_phase][sw];
-        if (lane == 0) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k) red[k] = ws[k];
-        }
-        use = grp_phase;
-        if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) { ok = false; break; }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-#pragma unroll
-          for (int w = 0; w < 4; ++w) tsum[k] += sh.sw_red[use][w][k];
-        }
-      }
-
       // epilogue of the previous tile of this segment
-      if (pend >= 0) { ok = epilogue(pend); if (!ok) break; }
+      KVQ_PT(s6)
+      if (pend >= 0) { ok = epilogue(pend, ts_prev); if (!ok) break; }
+      KVQ_PA(22, s6)
       pend = t;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) { a_prev[k] = alpha[k]; ts_prev[k] = tsum[k]; }
+      for (int k = 0; k < NH; ++k) {
+        a_prev[k] = alpha[k];
+        // channel-wise V: this group's per-warp sum(p), in exact fixed point
+        if (VCW) ws_prev[k] = (float)__reduce_add_sync(FULL, __float2uint_rn(pr[k] * kFix)) * (1.0f / kFix);
+      }
       pinv_prev = C::kCodeInv / pscale;
       sv_prev = vs_i;  // channel-wise V: lane i = channel i
       zv_prev = vz_i;
     }
-    if (ok && pend >= 0) ok = epilogue(pend) && finalize(pb, ph, pfirst, pue <= g1, pus, pue);
+    if (ok && pend >= 0) {
+      float ts[NH];
+#pragma unroll
+      for (int k = 0; k < NH; ++k) ts[k] = 0.f;
+      ok = (!VCW || combine_prev_sums(ts)) && epilogue(pend, ts) && finalize(pb, ph, pfirst, pue <= g1, pus, pue);
+    }
     if (!ok && ntiles > 0) set_abort(abort_flag, p.dev_status);
   }
 

@@ -55,7 +55,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 WorkspaceLayout workspace_layout(int batch, int kv_heads, int num_ctas) {
   WorkspaceLayout w;
   w.counters = 0;
-  w.part_lse = round_up((size_t)batch * kv_heads * sizeof(int), 256);
+  w.part_lse = round_up((size_t)batch * kv_heads * kCounterGroups * sizeof(int), 256);
   w.part_o = w.part_lse + round_up((size_t)num_ctas * 2 * kGroupQ * sizeof(float), 256);
   w.total = w.part_o + round_up((size_t)num_ctas * 2 * kGroupQ * kHeadDim * sizeof(float), 256);
   return w;
@@ -86,6 +86,11 @@ int resolve_ctas(const kvq_attn_desc* d, int sm_count) {
 }  // namespace kvq
 
 using namespace kvq;
+
+#ifdef KVQ_PROFILE
+static unsigned long long* g_prof_counters = nullptr;
+extern "C" KVQ_API void kvq_prof_set(unsigned long long* counters) { g_prof_counters = counters; }
+#endif
 
 extern "C" {
 
@@ -188,7 +193,7 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
   for (const void* ptr : bulk)
     if (ptr == nullptr || !aligned16(ptr)) return KVQ_ERR_INVALID_ARG;
   if (q == nullptr || seq_lens == nullptr || out == nullptr || lse == nullptr) return KVQ_ERR_INVALID_ARG;
-  if ((reinterpret_cast<uintptr_t>(q) & 1u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
       (reinterpret_cast<uintptr_t>(out) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
     return KVQ_ERR_INVALID_ARG;
   if (page_table != nullptr && (reinterpret_cast<uintptr_t>(page_table) & 3u)) return KVQ_ERR_INVALID_ARG;
@@ -203,7 +208,8 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
   if (workspace_bytes < w.total) return KVQ_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  if (cudaMemsetAsync(ws + w.counters, 0, (size_t)desc->batch * desc->cache.num_kv_heads * sizeof(int), st) !=
+  if (cudaMemsetAsync(ws + w.counters, 0, (size_t)desc->batch * desc->cache.num_kv_heads * kCounterGroups * sizeof(int),
+                      st) !=
       cudaSuccess)
     return KVQ_ERR_CUDA;
   DecodeParams p{};
@@ -219,6 +225,9 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.flags = desc->flags;
   p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
+#ifdef KVQ_PROFILE
+  p.prof = g_prof_counters;
+#endif
   cudaError_t e = launch_decode(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme, desc->operand_mode, p, st);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }

@@ -379,9 +379,14 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the INT2 scheme sweep")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-units", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller cases for profiler captures)")
+    ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     w = synth.WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = synth.shrink(w, batch=args.batch, name=f"{w.name}_b{args.batch}")
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -394,12 +399,12 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world)
-    res = measure_kvq(w, args.seed + rank, args.steps, args.warmup, dev)
+    res = measure_kvq(w, args.seed + rank, args.steps, args.warmup, dev, e2e=not args.no_e2e)
     barrier(world)
     ms = max_over_ranks(res["ms"], world, dev)
-    e2e_ms = max_over_ranks(res["e2e_ms"], world, dev)
+    e2e_ms = max_over_ranks(res["e2e_ms"], world, dev) if "e2e_ms" in res else float("nan")
     extra = []
-    if not args.no_extra and w.name == DEFAULT_WORKLOAD:
+    if not args.no_extra and w.name == DEFAULT_WORKLOAD and args.batch is None:
         w2 = synth.WORKLOADS["b128_l32k_int2"]
         for ks, vs in ((1, 0), (0, 0), (0, 1), (1, 1)):
             r2 = measure_kvq(w2, args.seed + rank, max(20, args.steps // 4), args.warmup, dev, ks, vs, e2e=False)
@@ -428,8 +433,8 @@ def main():
                      "traffic": profile_traffic(w.name),
                      "algorithmic_bytes_per_launch": res["bytes"],
                      "duration_source": "CUDA events around each kvq_decode_attn call (counter memset + kernel)"},
-        "e2e": {"value": total_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+        "e2e": ({"value": total_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]} if "e2e_ms" in res else None),
         "gpu_launches": res["launches"],
         "clocks": clk,
         "int2_sweep": extra,

@@ -52,19 +52,15 @@ namespace kvq {
 #define KVQ_PA(slot, n)
 #endif
 
-constexpr int kDecodeThreads = 448;  // 14 warps
+constexpr int kDecodeThreads = 320;  // 10 warps
 constexpr int kMaxBatch = 1024;      // sequences per call (prefix table in shared memory)
 constexpr uint32_t FULL = 0xffffffffu;
 
-// Warp roles.  The softmax work is split by query head: group g (4 warps)
-// owns heads 2g and 2g+1 of every (sequence, kv head).
+// Warp roles.
 constexpr int kWarpConvert0 = 0;  // warps 0-3: KV codes -> tensor memory, Q' operand
-constexpr int kWarpSoftmax0 = 4;  // warps 4-11: fold, online softmax, P' operand, epilogue
-constexpr int kSoftmaxGroups = 2;
-constexpr int kHeadsPerGroup = kGroupQ / kSoftmaxGroups;
-static_assert(kHeadsPerGroup == 2, "the softmax groups handle two heads each");
-constexpr int kWarpLoad = 12;     // packed tiles HBM -> shared memory
-constexpr int kWarpMma = 13;      // tcgen05.mma issue, tensor memory owner
+constexpr int kWarpSoftmax0 = 4;  // warps 4-7: fold, online softmax, P' operand, epilogue (two tiles per step)
+constexpr int kWarpLoad = 8;      // packed tiles HBM -> shared memory
+constexpr int kWarpMma = 9;       // tcgen05.mma issue, tensor memory owner
 
 template <int BITS, bool BF16>
 struct DecodeCfg {
@@ -139,29 +135,6 @@ __device__ __forceinline__ uint4 split3_e4m3(float4 v) {
   r.w = 0u;
   return r;
 }
-// Two values -> three E4M3 parts each: {hi, mid, lo}, each a 16-bit pair
-// (value 0 in the low byte).
-__device__ __forceinline__ uint3 split3_e4m3_x2(float2 v) {
-  uint3 r;
-  r.x = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)r.x, __NV_E4M3);
-  float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
-  v = make_float2(v.x - f.x, v.y - f.y);
-  r.y = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
-  h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)r.y, __NV_E4M3);
-  f = __half22float2(*reinterpret_cast<__half2*>(&h));
-  v = make_float2(v.x - f.x, v.y - f.y);
-  r.z = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
-  return r;
-}
-// Two values -> two BF16 parts each: {hi pair, lo pair}.
-__device__ __forceinline__ uint2 split2_bf16_x2(float2 v) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(v.x, v.y);
-  float2 f = __bfloat1622float2(h);
-  __nv_bfloat162 l = __floats2bfloat162_rn(v.x - f.x, v.y - f.y);
-  return make_uint2(*reinterpret_cast<uint32_t*>(&h), *reinterpret_cast<uint32_t*>(&l));
-}
-
 // x ~= hi + lo, each part BF16: {hi01, hi23, lo01, lo23}.
 __device__ __forceinline__ uint4 split2_bf16(float4 v) {
   __nv_bfloat162 h01 = __floats2bfloat162_rn(v.x, v.y), h23 = __floats2bfloat162_rn(v.z, v.w);
@@ -181,6 +154,39 @@ __device__ __forceinline__ float pow2_prescale(float m) {
   int e = (int)((__float_as_uint(m) >> 23) & 0xffu);
   if (e == 0 || e == 0xff) return 1.0f;
   return __uint_as_float((uint32_t)(261 - e) << 23);  // 2^(7 - (e - 127))
+}
+// 1 / pow2_prescale(m), exactly (no division).
+__device__ __forceinline__ float pow2_prescale_inv(float m) {
+  int e = (int)((__float_as_uint(m) >> 23) & 0xffu);
+  if (e == 0 || e == 0xff) return 1.0f;
+  return __uint_as_float((uint32_t)(e - 7) << 23);  // 2^((e - 127) - 7)
+}
+
+// 2^x (hardware approximation, flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// x ~= hi + mid + lo (each E4M3), with the residuals taken in f16x2
+// arithmetic: {hi, mid, lo, 0} words, element i in byte i.  Used for P'
+// (the fp16 rounding of x stays below the operand's own error).
+__device__ __forceinline__ uint4 split3_e4m3_via_f16(float4 v) {
+  __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  uint32_t w[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const __nv_fp8x2_storage_t ea = __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<__half2_raw*>(&a), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t eb = __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<__half2_raw*>(&b), __NV_SATFINITE, __NV_E4M3);
+    w[k] = (uint32_t)ea | ((uint32_t)eb << 16);
+    if (k < 2) {
+      __half2_raw ra = __nv_cvt_fp8x2_to_halfraw2(ea, __NV_E4M3), rb = __nv_cvt_fp8x2_to_halfraw2(eb, __NV_E4M3);
+      a = __hsub2(a, *reinterpret_cast<__half2*>(&ra));
+      b = __hsub2(b, *reinterpret_cast<__half2*>(&rb));
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], 0u);
 }
 
 // Converted code words of one packed 32-bit word.
@@ -218,9 +224,9 @@ struct alignas(16) DecodeBarriers {
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[C::kSlots], s_empty[C::kSlots], p_full[C::kSlots], p_empty[C::kSlots];
   uint64_t o_full[C::kSlots], o_empty[C::kSlots];
-  uint64_t sw_grp[kSoftmaxGroups], drain;
-  float sw_red[kSoftmaxGroups][2][4][8];  // reduction scratch [group][parity][warp][value]
-  int flag[kSoftmaxGroups];               // split-unit "last arriver" broadcast
+  uint64_t sw_grp, drain;
+  float sw_red[2][4][32];  // softmax-group reduction scratch [parity][warp][value]
+  int flag;                // split-unit "last arriver" broadcast
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;
@@ -238,23 +244,23 @@ constexpr size_t decode_smem_layout_bytes() {
 // --------------------------------------------------------------- helpers
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
-// All lanes poll; the warp gives up together (after the time limit or when
-// the CTA has been told to abort).
+// All lanes wait (sleeping inside try_wait until the phase completes); the
+// warp gives up together, after the time limit or when the CTA has been told
+// to abort.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t limit_ns) {
+  if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
   uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    bool ok = mbar_try_wait(bar, parity);
+  for (;;) {
+    bool ok = mbar_try_wait_sleep(bar, parity, 20000u);
     if (__all_sync(FULL, ok)) return true;
-    if ((it & 31u) == 31u) {
-      int stop = 0;
-      if (lane_id() == 0) {
-        uint64_t now = globaltimer_ns();
-        if (t0 == 0) t0 = now;
-        stop = (*abort_flag != 0) || (now - t0 > limit_ns);
-      }
-      if (__shfl_sync(FULL, stop, 0)) return false;
+    int stop = 0;
+    if (lane_id() == 0) {
+      uint64_t now = globaltimer_ns();
+      if (t0 == 0) t0 = now;
+      stop = (*abort_flag != 0) || (now - t0 > limit_ns);
     }
+    if (__shfl_sync(FULL, stop, 0)) return false;
   }
 }
 
@@ -351,16 +357,6 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long T, int C) {
 }
 __device__ __forceinline__ long long range_start(int c, long long T, int C) { return (long long)c * T / C; }
 
-// Sum of the operand-split accumulator columns of head (2 * grp + k):
-// columns n = 4 * part + head.  Only compile-time indices touch acc[].
-template <bool BF16>
-__device__ __forceinline__ float split_sum(const uint32_t (&acc)[16], int grp, int k) {
-  const float h0 = __uint_as_float(acc[k]) + __uint_as_float(acc[4 + k]) + (BF16 ? 0.f : __uint_as_float(acc[8 + k]));
-  const float h1 = __uint_as_float(acc[2 + k]) + __uint_as_float(acc[6 + k]) +
-                   (BF16 ? 0.f : __uint_as_float(acc[10 + k]));
-  return grp ? h1 : h0;
-}
-
 // ================================================================= kernel
 template <int BITS, bool KCW, bool VCW, bool BF16>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeParams p) {
@@ -382,18 +378,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
   // ------------------------------------------------------------ set-up
   if (tid == 0) {
-    for (int s = 0; s < C::kStages; ++s) { mbar_init(&sh.stg_full[s], 1); mbar_init(&sh.stg_empty[s], 12); }
+    for (int s = 0; s < C::kStages; ++s) { mbar_init(&sh.stg_full[s], 1); mbar_init(&sh.stg_empty[s], 8); }
     for (int a = 0; a < C::kNA; ++a) {
       mbar_init(&sh.ak_full[a], 4); mbar_init(&sh.ak_empty[a], 1);
       mbar_init(&sh.av_full[a], 4); mbar_init(&sh.av_empty[a], 1);
     }
     for (int s = 0; s < 2; ++s) { mbar_init(&sh.q_full[s], 4); mbar_init(&sh.q_empty[s], 1); }
     for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 8);
-      mbar_init(&sh.p_full[s], 8); mbar_init(&sh.p_empty[s], 1);
-      mbar_init(&sh.o_full[s], 1); mbar_init(&sh.o_empty[s], 8);
+      mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 4);
+      mbar_init(&sh.p_full[s], 4); mbar_init(&sh.p_empty[s], 1);
+      mbar_init(&sh.o_full[s], 1); mbar_init(&sh.o_empty[s], 4);
     }
-    for (int g = 0; g < kSoftmaxGroups; ++g) mbar_init(&sh.sw_grp[g], 4);
+    mbar_init(&sh.sw_grp, 4);
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_barrier_init();
@@ -489,6 +485,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       bool ok = true;
       int nq = 0, np = 0;
       uint64_t idle_since = 0;
+      uint32_t backoff = 32;
       while (np < ntiles) {
         bool progressed = false;
         if (np < nq) {
@@ -534,8 +531,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         }
         if (progressed) {
           idle_since = 0;
+          backoff = 32;
         } else {
-          __nanosleep(20);  // back off: leave issue slots to the warps sharing this sub-partition
+          __nanosleep(backoff);  // back off: leave issue slots to the warps sharing this sub-partition
+          backoff = backoff < 512 ? 2 * backoff : 512;
           const uint64_t now = globaltimer_ns();
           if (idle_since == 0) idle_since = now;
           if (*abort_flag || now - idle_since > limit) { ok = false; break; }
@@ -572,7 +571,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 #pragma unroll
         for (int i = 0; i < 4; ++i) qv[i] = bf2f(qb[i * kHeadDim + r]);
         float qsum[4];
-        unit_q_stats(qb, false, qmax, qsum);
+        unit_q_stats<4>(qb, false, qmax, qsum);
       }
 
       // ---- Q' operand: token-wise K uses q (written once per segment per
@@ -644,137 +643,165 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     }
   }
   // ============================================================= softmax
+  // Two tiles of one (sequence, kv head) per step: the fixed per-step costs
+  // (waits, the cross-warp reduction round, bookkeeping) are paid once per
+  // pair, and both tiles share one running-max update.
   else {
-    constexpr int NH = kHeadsPerGroup;
-    const int swt = tid - kWarpSoftmax0 * 32;
-    const int grp = swt >> 7;                // head group: heads hbase, hbase + 1
-    const int i = swt & 127;                 // tensor-memory lane: token (scores) / channel (output)
-    const int sw = i >> 5;                   // warp within the group = lane quarter
-    const int hbase = grp * NH;
+    const int i = tid - kWarpSoftmax0 * 32;  // tensor-memory lane: token (scores) / channel (output)
+    const int sw = warp - kWarpSoftmax0;     // warp = lane quarter
     const uint32_t lane_off = (uint32_t)(sw * 32) << 16;
     const int prow = a_pos<BITS, BF16>(i);
-    uint64_t* gbar = &sh.sw_grp[grp];
     uint32_t grp_phase = 0;
     const float kLn2 = 0.69314718055994530942f;
     const float kFix = 67108864.0f;  // 2^26: fixed-point scale of p for integer warp sums
+    // reduction-round payload slots: [0,8) tile maxima, [8,16) channel-wise K
+    // offsets q.z_g, [16,24) channel-wise V previous tiles' sum(p), [24,26)
+    // token-wise V largest scale; value v = tile * 4 + head within a block
+    constexpr int kTM = 0, kCG = 8, kWS = 16, kVM = 24, kNV = 26;
+    const bool lane_max = (lane < kCG) || (lane >= kVM);  // lane's value combines by max, else by sum
 
     // empty sequences: out = 0, lse = -inf
     for (int b = cta; b < B; b += (int)gridDim.x) {
       if (lens[b] != 0) continue;
-      for (int hq = grp; hq < p.num_q_heads; hq += kSoftmaxGroups) {
+      for (int hq = 0; hq < p.num_q_heads; ++hq) {
         p.out[((size_t)b * p.num_q_heads + hq) * kHeadDim + i] = 0.0f;
         if (i == 0) p.lse[(size_t)b * p.num_q_heads + hq] = -INFINITY;
       }
     }
 
-    float m[NH], lp[NH], zp[NH], O[NH];  // running max (log2 units), partial sum p, partial sum p*z, output
-    float a_prev[NH], ws_prev[NH];       // deferred epilogue inputs
-    float pinv_prev = 0.f, sv_prev = 0.f, zv_prev = 0.f;
-    float qi[NH], qmax[NH], mult[NH], add[NH];
+    float m[4], lp[4], zp[4], O[4];  // running max (log2 units), partial sum p, partial sum p*z, output
+    // deferred epilogue inputs of the previous step (up to two tiles)
+    int pend = -1, pend_n = 0;
+    float a_prev[4], ws_prev[8], pinv_prev[2], sv_prev[2], zv_prev[2];
+    float qi[4], qmax[4], mult[4], add[4];
 #pragma unroll
-    for (int k = 0; k < NH; ++k) { qi[k] = 0.f; qmax[k] = 0.f; mult[k] = 0.f; add[k] = 0.f; ws_prev[k] = 0.f; }
+    for (int k = 0; k < 4; ++k) { qi[k] = 0.f; qmax[k] = 0.f; mult[k] = 0.f; add[k] = 0.f; a_prev[k] = 0.f; }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ws_prev[k] = 0.f;
+    pinv_prev[0] = pinv_prev[1] = sv_prev[0] = sv_prev[1] = zv_prev[0] = zv_prev[1] = 0.f;
     auto reset = [&]() {
 #pragma unroll
-      for (int k = 0; k < NH; ++k) { m[k] = -INFINITY; lp[k] = 0.f; zp[k] = 0.f; O[k] = 0.f; }
+      for (int k = 0; k < 4; ++k) { m[k] = -INFINITY; lp[k] = 0.f; zp[k] = 0.f; O[k] = 0.f; }
     };
     reset();
 
-    // Cross-warp sum of the previous tile's per-warp p sums (channel-wise V).
-    auto combine_prev_sums = [&](float (&ts)[NH]) -> bool {
-      float* red = sh.sw_red[grp][grp_phase][sw];
+    // One cross-warp round: lane 0 of every warp publishes `vals`, then lane
+    // v merges value v over the four warps and the results are broadcast.
+    auto round = [&](const float (&vals)[kNV], float (&res)[kNV]) -> bool {
+      float* red = sh.sw_red[grp_phase][sw];
       if (lane == 0) {
 #pragma unroll
-        for (int k = 0; k < NH; ++k) red[k] = ws_prev[k];
+        for (int v = 0; v < kNV; v += 2) *reinterpret_cast<float2*>(red + v) = make_float2(vals[v], vals[v + 1]);
       }
       const uint32_t use = grp_phase;
-      if (!group_sync(gbar, grp_phase, abort_flag, limit)) return false;
+      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
+      const int v = lane < kNV ? lane : 0;
+      const float r0 = sh.sw_red[use][0][v], r1 = sh.sw_red[use][1][v];
+      const float r2 = sh.sw_red[use][2][v], r3 = sh.sw_red[use][3][v];
+      const float mine = lane_max ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : (r0 + r1) + (r2 + r3);
 #pragma unroll
-      for (int k = 0; k < NH; ++k)
-        ts[k] = (sh.sw_red[grp][use][0][k] + sh.sw_red[grp][use][1][k]) +
-                (sh.sw_red[grp][use][2][k] + sh.sw_red[grp][use][3][k]);
+      for (int k = 0; k < kNV; ++k) res[k] = __shfl_sync(FULL, mine, k);
       return true;
     };
 
-    // PV epilogue of tile t: O = O * alpha + folded partial product
-    auto epilogue = [&](int t, const float (&ts)[NH]) -> bool {
-      const int sl = t % C::kSlots;
-      const uint32_t p2 = (uint32_t)(t / C::kSlots) & 1u;
-      KVQ_PT(e0)
-      if (!warp_wait(&sh.o_full[sl], p2, abort_flag, limit)) return false;
-      KVQ_PA(23, e0)
-      tc_fence_after();
-      uint32_t acc[16];
-      KVQ_PT(el)
-      tmem_ld_32x32b_x16(tmem + lane_off + C::kColO + 16 * sl, acc);
-      tc_wait_ld();
-      KVQ_PA(27, el)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.o_empty[sl]);
+    // PV epilogue of the previous step's tiles: O = O * alpha + folded partial products
+    auto epilogue = [&](const float (&ts)[8]) -> bool {
+      float o_add[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < NH; ++k) {
-        float o = split_sum<BF16>(acc, grp, k);
-        o *= pinv_prev;
-        if (VCW) O[k] = fmaf(O[k], a_prev[k], fmaf(sv_prev, o, zv_prev * ts[k]));
-        else O[k] = fmaf(O[k], a_prev[k], o);
+      for (int u = 0; u < 2; ++u) {
+        if (u >= pend_n) break;
+        const int t = pend + u;
+        const int sl = t % C::kSlots;
+        const uint32_t p2 = (uint32_t)(t / C::kSlots) & 1u;
+        KVQ_PT(e0)
+        if (!warp_wait(&sh.o_full[sl], p2, abort_flag, limit)) return false;
+        KVQ_PA(23, e0)
+        tc_fence_after();
+        uint32_t acc[16];
+        tmem_ld_32x32b_x16(tmem + lane_off + C::kColO + 16 * sl, acc);
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.o_empty[sl]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float o = __uint_as_float(acc[k]) + __uint_as_float(acc[4 + k]);
+          if (!BF16) o += __uint_as_float(acc[8 + k]);
+          o *= pinv_prev[u];
+          o_add[k] += VCW ? fmaf(sv_prev[u], o, zv_prev[u] * ts[4 * u + k]) : o;
+        }
       }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) O[k] = fmaf(O[k], a_prev[k], o_add[k]);
+      return true;
+    };
+
+    // Cross-warp sums of the previous step's per-warp p sums (channel-wise V),
+    // for a drain that has no following step to carry them.
+    auto combine_prev_sums = [&](float (&ts)[8]) -> bool {
+      float vals[kNV], res[kNV];
+#pragma unroll
+      for (int k = 0; k < kNV; ++k) vals[k] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) vals[kWS + k] = ws_prev[k];
+      if (!round(vals, res)) return false;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ts[k] = res[kWS + k];
       return true;
     };
 
     // finish a (sequence, kv head) segment: normalise, store or merge
     auto finalize = [&](int b, int h, bool first_global, bool last_global, long long ustart, long long uend) -> bool {
-      float lsum[NH], zsum[NH];
+      float vals[kNV], res[kNV];
 #pragma unroll
-      for (int k = 0; k < NH; ++k) { lsum[k] = warp_sum(lp[k]); zsum[k] = VCW ? 0.f : warp_sum(zp[k]); }
-      float* red = sh.sw_red[grp][grp_phase][sw];
-      if (lane == 0) {
+      for (int k = 0; k < kNV; ++k) vals[k] = 0.f;
 #pragma unroll
-        for (int k = 0; k < NH; ++k) { red[k] = lsum[k]; red[NH + k] = zsum[k]; }
+      for (int k = 0; k < 4; ++k) { vals[kCG + k] = warp_sum(lp[k]); vals[kCG + 4 + k] = VCW ? 0.f : warp_sum(zp[k]); }
+      if (!round(vals, res)) return false;
+      float out4[4], lse4[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float l = res[kCG + k], z = res[kCG + 4 + k];
+        out4[k] = (O[k] + z) / l;
+        lse4[k] = (m[k] + __log2f(l)) * kLn2;
       }
-      const uint32_t use = grp_phase;
-      if (!group_sync(gbar, grp_phase, abort_flag, limit)) return false;
-      float res[NH], lse2[NH];
-#pragma unroll
-      for (int k = 0; k < NH; ++k) {
-        float l = 0.f, z = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) { l += sh.sw_red[grp][use][w][k]; z += sh.sw_red[grp][use][w][NH + k]; }
-        res[k] = (O[k] + z) / l;
-        lse2[k] = m[k] + __log2f(l);
-      }
-      const size_t row0 = (size_t)b * p.num_q_heads + (size_t)h * kGroupQ + hbase;
+      const size_t row0 = (size_t)b * p.num_q_heads + (size_t)h * kGroupQ;
       if (first_global && last_global) {  // whole (sequence, head) in this CTA
 #pragma unroll
-        for (int k = 0; k < NH; ++k) p.out[(row0 + k) * kHeadDim + i] = res[k];
-        if (i < NH) p.lse[row0 + i] = (i == 0 ? lse2[0] : lse2[NH - 1]) * kLn2;
+        for (int k = 0; k < 4; ++k) {
+          p.out[(row0 + k) * kHeadDim + i] = out4[k];
+          if (i == k) p.lse[row0 + k] = lse4[k];
+        }
         return true;
       }
       // split: publish this part; the last part to arrive merges all parts
       const int c_first = cta_of_tile(ustart, T, Cn), c_last = cta_of_tile(uend - 1, T, Cn);
       const int slot = (ustart <= g0) ? 0 : 1;
-      float* po = p.part_o + (((size_t)cta * 2 + slot) * kGroupQ + hbase) * kHeadDim;
+      float* po = p.part_o + ((size_t)cta * 2 + slot) * kGroupQ * kHeadDim;
 #pragma unroll
-      for (int k = 0; k < NH; ++k) po[k * kHeadDim + i] = res[k];
-      if (i < NH) p.part_lse[((size_t)cta * 2 + slot) * kGroupQ + hbase + i] = (i == 0 ? lse2[0] : lse2[NH - 1]) * kLn2;
+      for (int k = 0; k < 4; ++k) {
+        po[k * kHeadDim + i] = out4[k];
+        if (i == k) p.part_lse[((size_t)cta * 2 + slot) * kGroupQ + k] = lse4[k];
+      }
       __threadfence();
-      if (!group_sync(gbar, grp_phase, abort_flag, limit)) return false;
-      const int u = (b * Hkv + h) * kSoftmaxGroups + grp;
+      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
+      const int u = b * Hkv + h;
       if (i == 0) {
         int old = atomicAdd(&p.counters[u], 1);
-        sh.flag[grp] = (old == c_last - c_first) ? 1 : 0;
+        sh.flag = (old == c_last - c_first) ? 1 : 0;
       }
-      if (!group_sync(gbar, grp_phase, abort_flag, limit)) return false;
-      if (!sh.flag[grp]) return true;
+      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
+      if (!sh.flag) return true;
       __threadfence();
-      float mx[NH], den[NH], acc[NH];
+      float mx[4], den[4], acc[4];
 #pragma unroll
-      for (int k = 0; k < NH; ++k) { mx[k] = -INFINITY; den[k] = 0.f; acc[k] = 0.f; }
+      for (int k = 0; k < 4; ++k) { mx[k] = -INFINITY; den[k] = 0.f; acc[k] = 0.f; }
       for (int c = c_first; c <= c_last; ++c) {
         const int sl2 = (ustart <= range_start(c, T, Cn)) ? 0 : 1;
-        const float* pl = p.part_lse + ((size_t)c * 2 + sl2) * kGroupQ + hbase;
-        const float* pv = p.part_o + (((size_t)c * 2 + sl2) * kGroupQ + hbase) * kHeadDim;
+        const float* pl = p.part_lse + ((size_t)c * 2 + sl2) * kGroupQ;
+        const float* pv = p.part_o + ((size_t)c * 2 + sl2) * kGroupQ * kHeadDim;
 #pragma unroll
-        for (int k = 0; k < NH; ++k) {
+        for (int k = 0; k < 4; ++k) {
           float l = __ldcg(pl + k), v = __ldcg(pv + k * kHeadDim + i);
           float nm = fmaxf(mx[k], l);
           float sc = __expf(mx[k] - nm), w = __expf(l - nm);
@@ -784,7 +811,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         }
       }
 #pragma unroll
-      for (int k = 0; k < NH; ++k) {
+      for (int k = 0; k < 4; ++k) {
         p.out[(row0 + k) * kHeadDim + i] = acc[k] / den[k];
         if (i == k) p.lse[row0 + k] = mx[k] + __logf(den[k]);
       }
@@ -792,184 +819,174 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       return true;
     };
 
+    auto drain = [&](void) -> bool {
+      float ts[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ts[k] = 0.f;
+      return (!VCW || combine_prev_sums(ts)) && epilogue(ts);
+    };
+
     TileIter it;
     if (ntiles > 0) it.init(prefix, B, Hkv, (int)g0);
-    int pend = -1;
     int pb = 0, ph = 0;
     bool pfirst = false;
     long long pus = 0, pue = 0;
     bool ok = true;
-    for (int t = 0; t < ntiles && ok; ++t, it.next(prefix, B, Hkv)) {
-      const int s = t % C::kStages, sl = t % C::kSlots;
-      const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, p2 = (uint32_t)(t / C::kSlots) & 1u;
+    for (int t = 0; t < ntiles && ok;) {
       const long long g = g0 + t;
       const long long ustart = g - it.j, uend = ustart + it.nblk;
       const bool seg_first = (t == 0) || it.j == 0;
-      if (seg_first && pend >= 0) {  // close the previous segment
+      if (seg_first && pend_n > 0) {  // close the previous segment
         KVQ_PT(f0)
-        float ts[NH];
-#pragma unroll
-        for (int k = 0; k < NH; ++k) ts[k] = 0.f;
-        ok = (!VCW || combine_prev_sums(ts)) && epilogue(pend, ts) && finalize(pb, ph, pfirst, pue <= g1, pus, pue);
+        ok = drain() && finalize(pb, ph, pfirst, pue <= g1, pus, pue);
         KVQ_PA(24, f0)
         if (!ok) break;
         reset();
-        pend = -1;
+        pend_n = 0;
       }
       if (seg_first) {
         pb = it.b; ph = it.h; pfirst = ustart >= g0; pus = ustart; pue = uend;
-        const uint16_t* qb = p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ + hbase) * kHeadDim;
-        float qsum[NH];
-        unit_q_stats<NH>(qb, !KCW, qmax, qsum);
+        const uint16_t* qb = p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim;
+        float qsum[4];
+        unit_q_stats<4>(qb, !KCW, qmax, qsum);
 #pragma unroll
-        for (int k = 0; k < NH; ++k) {
+        for (int k = 0; k < 4; ++k) {
           if (KCW) {
             qi[k] = bf2f(qb[k * kHeadDim + i]);
           } else {  // token-wise K: S = s_l * (q . code) + z_l * sum(q), constant factors per segment
-            const float qs = BF16 ? 1.0f : pow2_prescale(qmax[k]);
-            mult[k] = C::kCodeInv / qs * p.sm_scale_log2;
+            mult[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_prescale_inv(qmax[k])) * p.sm_scale_log2;
             add[k] = qsum[k] * p.sm_scale_log2;
           }
         }
       }
-      const int nvalid = min(kBlockTokens, lens[it.b] - it.j * kBlockTokens);
+      // this step: tile t and, if it belongs to the same segment, tile t + 1
+      const int n = (t + 1 < ntiles && it.j + 1 < it.nblk) ? 2 : 1;
+      const int len = lens[it.b];
 
-      // ---- scores of this tile (lane i = token i)
       KVQ_PT(s0)
-      if (!warp_wait(&sh.s_full[sl], p2, abort_flag, limit) || !warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) {
-        ok = false;
-        break;
+      float sc[8], vs_t[2], vz_t[2], pv_scale_t[2];
+      float vals[kNV];
+#pragma unroll
+      for (int k = 0; k < kNV; ++k) vals[k] = 0.f;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (u >= n) {  // no second tile: neutral values
+#pragma unroll
+          for (int k = 0; k < 4; ++k) { sc[4 * u + k] = -INFINITY; vals[kTM + 4 * u + k] = -INFINITY; }
+          vs_t[u] = 0.f; vz_t[u] = 0.f;
+          continue;
+        }
+        const int tt = t + u;
+        const int s = tt % C::kStages, sl = tt % C::kSlots;
+        const uint32_t ps = (uint32_t)(tt / C::kStages) & 1u, p2 = (uint32_t)(tt / C::kSlots) & 1u;
+        if (!warp_wait(&sh.s_full[sl], p2, abort_flag, limit) || !warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t acc[16];
+        tmem_ld_32x32b_x16(tmem + lane_off + C::kColS + 16 * sl, acc);
+        const unsigned char* st = stages + (size_t)s * C::kStageBytes;
+        const uint16_t* szp = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
+        const float ks_i = h2f(szp[i]), kz_i = h2f(szp[kBlockTokens + i]);
+        vs_t[u] = h2f(szp[2 * kBlockTokens + i]);
+        vz_t[u] = h2f(szp[3 * kBlockTokens + i]);
+        if (KCW) {  // this group's Q' prescale (the value the converters used)
+          const float smax = max_f16_128(szp);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mult[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_prescale_inv(qmax[k] * smax)) * p.sm_scale_log2;
+        }
+        if (!VCW) vals[kVM + u] = h2f((uint16_t)__reduce_max_sync(FULL, (uint32_t)szp[2 * kBlockTokens + i]));
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) { mbar_arrive(&sh.s_empty[sl]); mbar_arrive(&sh.stg_empty[s]); }
+        const bool valid = i < len - (it.j + u) * kBlockTokens;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float a = __uint_as_float(acc[k]) + __uint_as_float(acc[4 + k]);
+          if (!BF16) a += __uint_as_float(acc[8 + k]);
+          // channel-wise K adds q . z_g once reduced over channels
+          const float v = KCW ? a * mult[k] : fmaf(a * mult[k], ks_i, kz_i * add[k]);
+          sc[4 * u + k] = valid ? v : -INFINITY;
+          vals[kTM + 4 * u + k] = warp_max_redux(sc[4 * u + k]);
+          if (KCW) vals[kCG + 4 * u + k] = warp_sum(qi[k] * kz_i);
+        }
+      }
+      if (!ok) break;
+      if (VCW) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) vals[kWS + k] = ws_prev[k];
       }
       KVQ_PA(16, s0)
-      KVQ_PT(s1)
-      tc_fence_after();
-      uint32_t acc[16];
-      KVQ_PT(sl0)
-      tmem_ld_32x32b_x16(tmem + lane_off + C::kColS + 16 * sl, acc);
-      const unsigned char* st = stages + (size_t)s * C::kStageBytes;
-      const uint16_t* szp = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
-      const float ks_i = h2f(szp[i]), kz_i = h2f(szp[kBlockTokens + i]);
-      const float vs_i = h2f(szp[2 * kBlockTokens + i]), vz_i = h2f(szp[3 * kBlockTokens + i]);
-      const uint32_t vs_bits = szp[2 * kBlockTokens + i];
-      if (KCW) {  // this group's Q' prescale (the value the converters used)
-        const float smax = max_f16_128(szp);
-#pragma unroll
-        for (int k = 0; k < NH; ++k) {
-          const float qs = BF16 ? 1.0f : pow2_prescale(qmax[k] * smax);
-          mult[k] = C::kCodeInv / qs * p.sm_scale_log2;
-        }
-      }
-      tc_wait_ld();
-      KVQ_PA(25, sl0)
-      KVQ_PT(sl1)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) { mbar_arrive(&sh.s_empty[sl]); mbar_arrive(&sh.stg_empty[s]); }
-
-      const bool valid = i < nvalid;
-      float sc[NH];
-#pragma unroll
-      for (int k = 0; k < NH; ++k) {
-        float a = split_sum<BF16>(acc, grp, k);
-        // channel-wise K adds q . z_g (below, once reduced over channels)
-        float v = KCW ? a * mult[k] : fmaf(a * mult[k], ks_i, kz_i * add[k]);
-        sc[k] = valid ? v : -INFINITY;
-      }
-      // one reduction round: tile maxima, channel-wise K offsets q . z_g,
-      // token-wise V largest scale, channel-wise V previous tile's sum(p)
-      {
-        float* red = sh.sw_red[grp][grp_phase][sw];
-        float tm[NH], cg[NH];
-#pragma unroll
-        for (int k = 0; k < NH; ++k) tm[k] = warp_max_redux(sc[k]);
-        if (KCW) {
-#pragma unroll
-          for (int k = 0; k < NH; ++k) cg[k] = warp_sum(qi[k] * kz_i);
-        }
-        const uint32_t vmax = VCW ? 0u : __reduce_max_sync(FULL, vs_bits);
-        if (lane == 0) {
-#pragma unroll
-          for (int k = 0; k < NH; ++k) {
-            red[k] = tm[k];
-            if (KCW) red[NH + k] = cg[k];
-            if (VCW) red[2 * NH + k] = ws_prev[k];
-          }
-          red[3 * NH] = __uint_as_float(vmax);
-        }
-      }
-      const uint32_t use = grp_phase;
-      KVQ_PA(26, sl1)
-      KVQ_PA(17, s1)
       KVQ_PT(s2)
-      if (!group_sync(gbar, grp_phase, abort_flag, limit)) { ok = false; break; }
+      float res[kNV];
+      if (!round(vals, res)) { ok = false; break; }
       KVQ_PA(18, s2)
       KVQ_PT(s3)
-      const float (*rd)[8] = sh.sw_red[grp][use];
-      float alpha[NH], pr[NH], ts_prev[NH];
+      // one running-max update for the pair
+      float pr[8], alpha[4];
 #pragma unroll
-      for (int k = 0; k < NH; ++k) {
-        const float tmx = fmaxf(fmaxf(rd[0][k], rd[1][k]), fmaxf(rd[2][k], rd[3][k]));
-        const float cgs = KCW ? ((rd[0][NH + k] + rd[1][NH + k]) + (rd[2][NH + k] + rd[3][NH + k])) * p.sm_scale_log2
-                              : 0.0f;
-        ts_prev[k] = VCW ? (rd[0][2 * NH + k] + rd[1][2 * NH + k]) + (rd[2][2 * NH + k] + rd[3][2 * NH + k]) : 0.f;
-        const float mn = fmaxf(m[k], tmx + cgs);
-        alpha[k] = exp2f(m[k] - mn);
+      for (int k = 0; k < 4; ++k) {
+        const float cg0 = KCW ? res[kCG + k] * p.sm_scale_log2 : 0.f;
+        const float cg1 = KCW ? res[kCG + 4 + k] * p.sm_scale_log2 : 0.f;
+        const float mn = fmaxf(m[k], fmaxf(res[kTM + k] + cg0, res[kTM + 4 + k] + cg1));
+        alpha[k] = ex2(m[k] - mn);
         m[k] = mn;
-        pr[k] = exp2f(sc[k] + cgs - mn);
-        lp[k] = fmaf(lp[k], alpha[k], pr[k]);
-        if (!VCW) zp[k] = fmaf(zp[k], alpha[k], pr[k] * vz_i);
+        pr[k] = ex2(sc[k] + cg0 - mn);
+        pr[4 + k] = ex2(sc[4 + k] + cg1 - mn);
+        lp[k] = fmaf(lp[k], alpha[k], pr[k] + pr[4 + k]);
+        if (!VCW) zp[k] = fmaf(zp[k], alpha[k], fmaf(pr[k], vz_t[0], pr[4 + k] * vz_t[1]));
       }
-      float smax_v = 0.f;
-      if (!VCW) {
-        uint32_t mv = 0u;
+      // P' operands (lane i = token i): token-wise V folds s into P
 #pragma unroll
-        for (int w = 0; w < 4; ++w) mv = max(mv, __float_as_uint(rd[w][3 * NH]));
-        smax_v = h2f((uint16_t)mv);
+      for (int u = 0; u < 2; ++u) {
+        if (u >= n) break;
+        const int tt = t + u, sl = tt % C::kSlots;
+        const uint32_t p2 = (uint32_t)(tt / C::kSlots) & 1u;
+        const float pscale = VCW ? 256.0f : (BF16 ? 1.0f : pow2_prescale(res[kVM + u]));
+        pv_scale_t[u] = VCW ? (1.0f / 256.0f) : (BF16 ? 1.0f : pow2_prescale_inv(res[kVM + u]));
+        const float pmul = VCW ? pscale : vs_t[u] * pscale;
+        const float4 pv = make_float4(pr[4 * u] * pmul, pr[4 * u + 1] * pmul, pr[4 * u + 2] * pmul, pr[4 * u + 3] * pmul);
+        const uint4 bytes = BF16 ? split2_bf16(pv) : split3_e4m3_via_f16(pv);
+        if (!warp_wait(&sh.p_empty[sl], p2 ^ 1u, abort_flag, limit)) { ok = false; break; }
+        *reinterpret_cast<uint4*>(pop + sl * C::kBBytes + b_row_off<BF16>(prow)) = bytes;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.p_full[sl]);
       }
-      // P' operand (lane i = token i): token-wise V folds s into P
-      const float pscale = VCW ? 256.0f : (BF16 ? 1.0f : pow2_prescale(smax_v));
-      const float pmul = VCW ? pscale : vs_i * pscale;
-      const float2 pv = make_float2(pr[0] * pmul, pr[NH - 1] * pmul);
+      if (!ok) break;
       KVQ_PA(19, s3)
-      KVQ_PT(s4)
-      if (!warp_wait(&sh.p_empty[sl], p2 ^ 1u, abort_flag, limit)) { ok = false; break; }
-      KVQ_PA(20, s4)
-      unsigned char* prow_ptr = pop + sl * C::kBBytes + b_row_off<BF16>(prow);
-      if (BF16) {  // column n = 4 * part + head: parts at byte 8 * part + 2 * head
-        const uint2 w = split2_bf16_x2(pv);
-        *reinterpret_cast<uint32_t*>(prow_ptr + 2 * hbase) = w.x;
-        *reinterpret_cast<uint32_t*>(prow_ptr + 8 + 2 * hbase) = w.y;
-      } else {     // column n = 4 * part + head: one byte each
-        const uint3 w = split3_e4m3_x2(pv);
-        *reinterpret_cast<uint16_t*>(prow_ptr + hbase) = (uint16_t)w.x;
-        *reinterpret_cast<uint16_t*>(prow_ptr + 4 + hbase) = (uint16_t)w.y;
-        *reinterpret_cast<uint16_t*>(prow_ptr + 8 + hbase) = (uint16_t)w.z;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.p_full[sl]);
 
-      // epilogue of the previous tile of this segment
+      // epilogue of the previous step (its sums of p arrived in this round)
       KVQ_PT(s6)
-      if (pend >= 0) { ok = epilogue(pend, ts_prev); if (!ok) break; }
+      if (pend_n > 0) {
+        float ts[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ts[k] = VCW ? res[kWS + k] : 0.f;
+        if (!epilogue(ts)) { ok = false; break; }
+      }
       KVQ_PA(22, s6)
       pend = t;
+      pend_n = n;
 #pragma unroll
-      for (int k = 0; k < NH; ++k) {
-        a_prev[k] = alpha[k];
+      for (int k = 0; k < 4; ++k) a_prev[k] = alpha[k];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        pinv_prev[u] = C::kCodeInv * pv_scale_t[u];
+        sv_prev[u] = vs_t[u];  // channel-wise V: lane i = channel i
+        zv_prev[u] = vz_t[u];
         // channel-wise V: this group's per-warp sum(p), in exact fixed point
-        if (VCW) ws_prev[k] = (float)__reduce_add_sync(FULL, __float2uint_rn(pr[k] * kFix)) * (1.0f / kFix);
-      }
-      pinv_prev = C::kCodeInv / pscale;
-      sv_prev = vs_i;  // channel-wise V: lane i = channel i
-      zv_prev = vz_i;
-    }
-    if (ok && pend >= 0) {
-      float ts[NH];
 #pragma unroll
-      for (int k = 0; k < NH; ++k) ts[k] = 0.f;
-      ok = (!VCW || combine_prev_sums(ts)) && epilogue(pend, ts) && finalize(pb, ph, pfirst, pue <= g1, pus, pue);
+        for (int k = 0; k < 4; ++k)
+          ws_prev[4 * u + k] = VCW ? (float)__reduce_add_sync(FULL, __float2uint_rn(pr[4 * u + k] * kFix)) * (1.0f / kFix)
+                                   : 0.f;
+      }
+      for (int u = 0; u < n; ++u) it.next(prefix, B, Hkv);
+      t += n;
     }
+    if (ok && pend_n > 0) ok = drain() && finalize(pb, ph, pfirst, pue <= g1, pus, pue);
     if (!ok && ntiles > 0) set_abort(abort_flag, p.dev_status);
   }
 

@@ -12,7 +12,7 @@ namespace kvq {
 constexpr int kBlockTokens = 128;  // tokens per block / page; channel-wise group
 constexpr int kHeadDim = 128;
 constexpr int kGroupQ = 4;  // query heads per KV head
-constexpr int kCounterGroups = 2;  // split-merge arrival counters per (sequence, kv head)
+constexpr int kCounterGroups = 1;  // split-merge arrival counters per (sequence, kv head)
 
 __device__ __forceinline__ void report(uint32_t* dev_status, uint32_t bits) {
   if (dev_status != nullptr) atomicOr(dev_status, bits);
@@ -58,7 +58,7 @@ struct DecodeParams {
   float* out;
   float* lse;
   uint32_t* dev_status;
-  int* counters;        // [B * Hkv * 2] split-unit arrival counters (zeroed per call)
+  int* counters;        // [B * Hkv] split-unit arrival counters (zeroed per call)
   float* part_o;        // [num_ctas][2][4][128]
   float* part_lse;      // [num_ctas][2][4]
   int batch, num_kv_heads, num_q_heads, max_blocks, num_pages;

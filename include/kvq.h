@@ -191,7 +191,7 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
  * kvq_decode_attn minus the workspace: the split-merge scratch lives in a
  * fixed 4 MiB device array owned by the library, held on every device that
  * loads the library until the process exits.  Returns KVQ_ERR_WORKSPACE when
- * a call needs more scratch than that (batch * num_kv_heads * 8 bytes of
+ * a call needs more scratch than that (batch * num_kv_heads * 4 bytes of
  * counters plus 4 KiB per CTA); kvq_decode_attn with a caller workspace then
  * remains available.  The first call on each device looks up the array's
  * address once (this may load the module): make it before any stream

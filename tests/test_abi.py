@@ -65,8 +65,8 @@ def test_workspace_size_host_only(lib):
     d = _lib.AttnDesc(_cache(4, pages=128 * 256), 128, 32, 256, 0, 0.0, 304, 0)
     n = ctypes.c_size_t()
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
-    # counters (2 per sequence x kv head) + part lse + part out, each 256-byte aligned
-    assert n.value == 128 * 8 * 2 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
+    # counters (one per sequence x kv head) + part lse + part out, each 256-byte aligned
+    assert n.value == 128 * 8 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
     bad = _lib.AttnDesc(_cache(4), 128, 16, 256, 0, 0.0, 304, 0)  # GQA 2 is not built
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
     bad = _lib.AttnDesc(_cache(4), 0, 32, 256, 0, 0.0, 304, 0)

@@ -547,6 +547,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     }
   }
   // ========================================================== converters
+  // Software-pipelined: Q' and K of tile t + 1 are produced before V of tile
+  // t, so QK^T runs a tile ahead and never waits behind an earlier PV.
   else if (warp < kWarpSoftmax0) {
     const int r = tid;  // tensor-memory lane = A row; also this thread's channel of Q'
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -556,12 +558,31 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     int seg = -1, slot_seg0 = -2, slot_seg1 = -2;  // Q' slot contents (token-wise K: constant per segment)
     TileIter it;
     if (ntiles > 0) it.init(prefix, B, Hkv, (int)g0);
-    for (int t = 0; t < ntiles; ++t, it.next(prefix, B, Hkv)) {
+
+    // codes of one packed row -> tensor-memory row (32 columns per store)
+    auto convert_rows = [&](const unsigned char* blk, uint32_t col) {
+      constexpr int kPasses = C::kACols / 32, kPerPass = C::kChunks / kPasses;
+#pragma unroll
+      for (int ps2 = 0; ps2 < kPasses; ++ps2) {
+        uint32_t o[32];
+#pragma unroll
+        for (int c = 0; c < kPerPass; ++c) {
+          uint4 v = *reinterpret_cast<const uint4*>(blk + ((size_t)(ps2 * kPerPass + c) * kBlockTokens + r) * 16);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) Convert<BITS, BF16>::run(w[i], &o[(4 * c + i) * Convert<BITS, BF16>::kOut]);
+        }
+        tmem_st_32x32b_x32(col + 32 * ps2, o);
+      }
+    };
+
+    // stage wait, Q' operand and K codes of tile t (it = tile t)
+    auto k_part = [&](int t) -> bool {
       const int s = t % C::kStages, a = t % C::kNA, sl = t & 1;
       const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNA) & 1u,
                      p2 = (uint32_t)(t >> 1) & 1u;
       KVQ_PT(c0)
-      if (!warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) { set_abort(abort_flag, p.dev_status); break; }
+      if (!warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) return false;
       KVQ_PA(1, c0)
       const unsigned char* st = stages + (size_t)s * C::kStageBytes;
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
@@ -573,11 +594,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         float qsum[4];
         unit_q_stats<4>(qb, false, qmax, qsum);
       }
-
-      // ---- Q' operand: token-wise K uses q (written once per segment per
-      // slot); channel-wise K folds this group's scales into q.
+      // Q' operand: token-wise K uses q (written once per segment per slot);
+      // channel-wise K folds this group's scales into q.
       KVQ_PT(c4)
-      if (!warp_wait(&sh.q_empty[sl], p2 ^ 1u, abort_flag, limit)) { set_abort(abort_flag, p.dev_status); break; }
+      if (!warp_wait(&sh.q_empty[sl], p2 ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(5, c4)
       KVQ_PT(c3)
       if (KCW || (sl ? slot_seg1 : slot_seg0) != seg) {
@@ -595,42 +615,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.q_full[sl]);
       KVQ_PA(4, c3)
-
-      // ---- K codes -> A_K[a] (row r = token r), V codes -> A_V[a] (row r = channel r).
-      // K is handed to the MMA before V's buffer is awaited, so QK^T never
-      // waits for an earlier tile's PV.
+      // K codes -> A_K[a] (row r = token r)
+      KVQ_PT(c1)
+      if (!warp_wait(&sh.ak_empty[a], pa ^ 1u, abort_flag, limit)) return false;
+      KVQ_PA(2, c1)
       KVQ_PT(c2)
-      bool stalled = false;
-#pragma unroll
-      for (int kv = 0; kv < 2; ++kv) {
-        KVQ_PT(cw)
-        if (!warp_wait(kv ? &sh.av_empty[a] : &sh.ak_empty[a], pa ^ 1u, abort_flag, limit)) { stalled = true; break; }
-        KVQ_PA(kv ? 6 : 2, cw)
-        KVQ_PT(cc)
-        constexpr int kPasses = C::kACols / 32, kPerPass = C::kChunks / kPasses;
-#pragma unroll
-        for (int ps2 = 0; ps2 < kPasses; ++ps2) {
-          uint32_t o[32];
-#pragma unroll
-          for (int c = 0; c < kPerPass; ++c) {
-            uint4 v = *reinterpret_cast<const uint4*>(
-                st + kv * C::kBlockBytes + ((size_t)(ps2 * kPerPass + c) * kBlockTokens + r) * 16);
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) Convert<BITS, BF16>::run(w[i], &o[(4 * c + i) * Convert<BITS, BF16>::kOut]);
-          }
-          tmem_st_32x32b_x32(tmem + lane_off + (kv ? C::kColAV : C::kColAK) + a * C::kACols + 32 * ps2, o);
-        }
-        if (kv == 0) {  // K first: QK^T need not wait for V's buffer
-          tc_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.ak_full[a]);
-        }
-        KVQ_PA(kv ? 8 : 7, cc)
-      }
-      KVQ_PT(cf)
-      if (stalled) { set_abort(abort_flag, p.dev_status); break; }
+      convert_rows(st, tmem + lane_off + C::kColAK + a * C::kACols);
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.ak_full[a]);
+      KVQ_PA(7, c2)
+      return true;
+    };
+
+    // V codes of tile t -> A_V[a] (row r = channel r); releases the stage
+    auto v_part = [&](int t) -> bool {
+      const int s = t % C::kStages, a = t % C::kNA;
+      const uint32_t pa = (uint32_t)(t / C::kNA) & 1u;
+      KVQ_PT(c5)
+      if (!warp_wait(&sh.av_empty[a], pa ^ 1u, abort_flag, limit)) return false;
+      KVQ_PA(6, c5)
+      KVQ_PT(c6)
+      convert_rows(stages + (size_t)s * C::kStageBytes + C::kBlockBytes, tmem + lane_off + C::kColAV + a * C::kACols);
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -638,9 +645,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         mbar_arrive(&sh.av_full[a]);
         mbar_arrive(&sh.stg_empty[s]);
       }
-      KVQ_PA(9, cf)
-      KVQ_PA(3, c2)
+      KVQ_PA(8, c6)
+      return true;
+    };
+
+    bool ok = ntiles == 0 || k_part(0);
+    if (ntiles > 0) it.next(prefix, B, Hkv);
+    for (int t = 0; t < ntiles && ok; ++t) {
+      if (t + 1 < ntiles) {
+        ok = k_part(t + 1);
+        it.next(prefix, B, Hkv);
+        if (!ok) break;
+      }
+      ok = v_part(t);
     }
+    if (!ok) set_abort(abort_flag, p.dev_status);
   }
   // ============================================================= softmax
   // Two tiles of one (sequence, kv head) per step: the fixed per-step costs
@@ -952,11 +971,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         const uint4 bytes = BF16 ? split2_bf16(pv) : split3_e4m3_via_f16(pv);
         if (!warp_wait(&sh.p_empty[sl], p2 ^ 1u, abort_flag, limit)) { ok = false; break; }
         *reinterpret_cast<uint4*>(pop + sl * C::kBBytes + b_row_off<BF16>(prow)) = bytes;
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.p_full[sl]);
       }
       if (!ok) break;
+      fence_proxy_async_smem();  // both P' rows visible to the tensor core
+      __syncwarp();
+      if (lane == 0) {
+        for (int u = 0; u < n; ++u) mbar_arrive(&sh.p_full[(t + u) % C::kSlots]);
+      }
       KVQ_PA(19, s3)
 
       // epilogue of the previous step (its sums of p arrived in this round)

@@ -42,11 +42,13 @@
 namespace kvq {
 
 // Optional cycle accounting per CTA and pipeline role (built only when
-// KVQ_PROFILE is defined; the library build never defines it).
+// KVQ_PROFILE is defined; the library build never defines it).  Probes add
+// into shared memory: a global atomic per probe would stall the next
+// mbarrier arrive, whose release semantics wait for it to complete.
 #ifdef KVQ_PROFILE
 #define KVQ_PT(n) long long kvq_pt_##n = clock64();
 #define KVQ_PA(slot, n) \
-  if (p.prof != nullptr && (threadIdx.x & 31) == 0) atomicAdd(&p.prof[blockIdx.x * 32 + (slot)], (unsigned long long)(clock64() - kvq_pt_##n));
+  if (p.prof != nullptr && (threadIdx.x & 31) == 0) atomicAdd(&sh.prof[slot], (unsigned long long)(clock64() - kvq_pt_##n));
 #else
 #define KVQ_PT(n)
 #define KVQ_PA(slot, n)
@@ -230,6 +232,9 @@ struct alignas(16) DecodeBarriers {
   uint32_t tmem_base;
   int abort_flag;
   int total_tiles;
+#ifdef KVQ_PROFILE
+  unsigned long long prof[32];  // cycle accounting, flushed to global memory at exit
+#endif
 };
 
 template <int BITS, bool BF16>
@@ -390,6 +395,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       mbar_init(&sh.o_full[s], 1); mbar_init(&sh.o_empty[s], 4);
     }
     mbar_init(&sh.sw_grp, 4);
+#ifdef KVQ_PROFILE
+    for (int s = 0; s < 32; ++s) sh.prof[s] = 0ull;
+#endif
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_barrier_init();
@@ -1018,6 +1026,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+#ifdef KVQ_PROFILE
+  if (p.prof != nullptr && tid < 32) atomicAdd(&p.prof[blockIdx.x * 32 + tid], sh.prof[tid]);
+#endif
 }
 
 template <int BITS, bool KCW, bool VCW, bool BF16>

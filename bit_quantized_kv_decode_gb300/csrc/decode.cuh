@@ -72,7 +72,8 @@ struct DecodeCfg {
   static constexpr int kSzBytes = kBlockTokens * 2;                       // one fp16 [128] array
   static constexpr int kStageBytes = 2 * kBlockBytes + 4 * kSzBytes;
   static constexpr int kACols = BF16 ? 64 : 32;  // tensor-memory columns of one 128 x 128 A tile
-  static constexpr int kNA = BF16 ? 1 : 2;       // A tile buffers per operand
+  static constexpr int kNAK = BF16 ? 1 : 2;      // A tile buffers: K codes
+  static constexpr int kNAV = BF16 ? 1 : 2;      // A tile buffers: V codes
   static constexpr int kSplits = BF16 ? 2 : 3;   // parts of Q' and P'
   static constexpr int kBBytes = BF16 ? 4096 : 2048;  // one B operand (128 K-rows x N=16)
   static constexpr int kKSteps = BF16 ? 8 : 4;
@@ -82,8 +83,8 @@ struct DecodeCfg {
   static constexpr uint32_t kIdesc = BF16 ? make_idesc(1, 1, 0, 1, 128, 16) : make_idesc(0, 0, 0, 1, 128, 16);
   static constexpr int kSlots = 4;  // score / probability / output buffers in flight
   static constexpr int kColAK = 0;
-  static constexpr int kColAV = kNA * kACols;
-  static constexpr int kColS = 2 * kNA * kACols;
+  static constexpr int kColAV = kNAK * kACols;
+  static constexpr int kColS = kColAV + kNAV * kACols;
   static constexpr int kColO = kColS + 16 * kSlots;
   static constexpr int kTmemCols = 256;
   static constexpr float kCodeInv = BF16 ? 1.0f : 512.0f;  // code = operand value * kCodeInv
@@ -164,6 +165,28 @@ __device__ __forceinline__ float pow2_prescale_inv(float m) {
   return __uint_as_float((uint32_t)(e - 7) << 23);  // 2^((e - 127) - 7)
 }
 
+// Channel-wise K prescale of Q', split into a per-segment head factor and a
+// per-tile group factor.  With E_q = floor(log2 qmax) and E_s the exponent
+// of the group's largest fp16 scale, Q' = q * s * 2^(6 - E_q) * 2^(-E_s)
+// stays below 2^(E_q+1) * 2^(E_s+1) * 2^(6 - E_q - E_s) = 256 (no E4M3
+// overflow); the score multiplier 2^(E_q - 6) * 2^(E_s) undoes it exactly.
+// A query with qmax < 2^-120 (or non-finite) uses factor 1 on both sides.
+__device__ __forceinline__ float pow2_head(float qmax) {
+  const int e = (int)((__float_as_uint(qmax) >> 23) & 0xffu);
+  return (e < 7 || e == 0xff) ? 1.0f : __uint_as_float((uint32_t)(260 - e) << 23);  // 2^(6 - E_q)
+}
+__device__ __forceinline__ float pow2_head_inv(float qmax) {
+  const int e = (int)((__float_as_uint(qmax) >> 23) & 0xffu);
+  return (e < 7 || e == 0xff) ? 1.0f : __uint_as_float((uint32_t)(e - 6) << 23);  // 2^(E_q - 6)
+}
+// Exponent field of an fp16 maximum, clamped to the normal range [1, 30].
+__device__ __forceinline__ uint32_t f16_exp_field(uint32_t h) {
+  const uint32_t e = (h >> 10) & 31u;
+  return e < 1u ? 1u : (e > 30u ? 30u : e);
+}
+__device__ __forceinline__ float pow2_group(uint32_t e16) { return __uint_as_float((142u - e16) << 23); }      // 2^(-E_s)
+__device__ __forceinline__ float pow2_group_inv(uint32_t e16) { return __uint_as_float((112u + e16) << 23); }  // 2^(E_s)
+
 // 2^x (hardware approximation, flush-to-zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -222,7 +245,7 @@ template <int BITS, bool BF16>
 struct alignas(16) DecodeBarriers {
   using C = DecodeCfg<BITS, BF16>;
   uint64_t stg_full[C::kStages], stg_empty[C::kStages];
-  uint64_t ak_full[C::kNA], ak_empty[C::kNA], av_full[C::kNA], av_empty[C::kNA];
+  uint64_t ak_full[C::kNAK], ak_empty[C::kNAK], av_full[C::kNAV], av_empty[C::kNAV];
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[C::kSlots], s_empty[C::kSlots], p_full[C::kSlots], p_empty[C::kSlots];
   uint64_t o_full[C::kSlots], o_empty[C::kSlots];
@@ -307,11 +330,12 @@ __device__ __forceinline__ float warp_max_redux(float f) { return unkey(__reduce
 
 // Largest of 128 non-negative fp16 values in shared memory; every warp that
 // calls it gets the same value without talking to the other warps.
-__device__ __forceinline__ float max_f16_128(const uint16_t* v) {
+__device__ __forceinline__ uint32_t max_f16_bits_128(const uint16_t* v) {
   uint2 w = *reinterpret_cast<const uint2*>(v + 4 * lane_id());
   uint32_t m = max(max(w.x & 0xffffu, w.x >> 16), max(w.y & 0xffffu, w.y >> 16));
-  return h2f((uint16_t)__reduce_max_sync(FULL, m));
+  return __reduce_max_sync(FULL, m);
 }
+__device__ __forceinline__ float max_f16_128(const uint16_t* v) { return h2f((uint16_t)max_f16_bits_128(v)); }
 
 __device__ __forceinline__ float bf2f(uint16_t bits) { return __uint_as_float((uint32_t)bits << 16); }
 
@@ -384,10 +408,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   // ------------------------------------------------------------ set-up
   if (tid == 0) {
     for (int s = 0; s < C::kStages; ++s) { mbar_init(&sh.stg_full[s], 1); mbar_init(&sh.stg_empty[s], 8); }
-    for (int a = 0; a < C::kNA; ++a) {
-      mbar_init(&sh.ak_full[a], 4); mbar_init(&sh.ak_empty[a], 1);
-      mbar_init(&sh.av_full[a], 4); mbar_init(&sh.av_empty[a], 1);
-    }
+    for (int a = 0; a < C::kNAK; ++a) { mbar_init(&sh.ak_full[a], 4); mbar_init(&sh.ak_empty[a], 1); }
+    for (int a = 0; a < C::kNAV; ++a) { mbar_init(&sh.av_full[a], 4); mbar_init(&sh.av_empty[a], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&sh.q_full[s], 4); mbar_init(&sh.q_empty[s], 1); }
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(&sh.s_full[s], 1); mbar_init(&sh.s_empty[s], 4);
@@ -497,8 +519,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       while (np < ntiles) {
         bool progressed = false;
         if (np < nq) {
-          const int a = np % C::kNA, sl = np % C::kSlots;
-          const uint32_t pa = (uint32_t)(np / C::kNA) & 1u, ps4 = (uint32_t)(np / C::kSlots) & 1u;
+          const int a = np % C::kNAV, sl = np % C::kSlots;
+          const uint32_t pa = (uint32_t)(np / C::kNAV) & 1u, ps4 = (uint32_t)(np / C::kSlots) & 1u;
           if (mbar_test(&sh.av_full[a], pa) && mbar_test(&sh.p_full[sl], ps4) &&
               mbar_test(&sh.o_empty[sl], ps4 ^ 1u)) {
             tc_fence_after();
@@ -517,8 +539,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           }
         }
         if (nq < ntiles) {
-          const int a = nq % C::kNA, sl = nq % C::kSlots, q2 = nq & 1;
-          const uint32_t pa = (uint32_t)(nq / C::kNA) & 1u, ps4 = (uint32_t)(nq / C::kSlots) & 1u,
+          const int a = nq % C::kNAK, sl = nq % C::kSlots, q2 = nq & 1;
+          const uint32_t pa = (uint32_t)(nq / C::kNAK) & 1u, ps4 = (uint32_t)(nq / C::kSlots) & 1u,
                          p2 = (uint32_t)(nq >> 1) & 1u;
           if (mbar_test(&sh.ak_full[a], pa) && mbar_test(&sh.q_full[q2], p2) &&
               mbar_test(&sh.s_empty[sl], ps4 ^ 1u)) {
@@ -561,8 +583,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     const int r = tid;  // tensor-memory lane = A row; also this thread's channel of Q'
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const int qrow = a_pos<BITS, BF16>(r);
-    float qv[4] = {0.f, 0.f, 0.f, 0.f};    // q[b, 4h + i, r]
-    float qmax[4] = {0.f, 0.f, 0.f, 0.f};  // per-unit max |q|
+    float qh[4] = {0.f, 0.f, 0.f, 0.f};  // q[b, 4h + i, r] times the head's prescale
     int seg = -1, slot_seg0 = -2, slot_seg1 = -2;  // Q' slot contents (token-wise K: constant per segment)
     TileIter it;
     if (ntiles > 0) it.init(prefix, B, Hkv, (int)g0);
@@ -586,8 +607,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
     // stage wait, Q' operand and K codes of tile t (it = tile t)
     auto k_part = [&](int t) -> bool {
-      const int s = t % C::kStages, a = t % C::kNA, sl = t & 1;
-      const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNA) & 1u,
+      const int s = t % C::kStages, a = t % C::kNAK, sl = t & 1;
+      const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNAK) & 1u,
                      p2 = (uint32_t)(t >> 1) & 1u;
       KVQ_PT(c0)
       if (!warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) return false;
@@ -597,10 +618,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       if (t == 0 || it.j == 0) {  // new (sequence, kv head): its four query rows
         ++seg;
         const uint16_t* qb = p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) qv[i] = bf2f(qb[i * kHeadDim + r]);
-        float qsum[4];
+        float qmax[4], qsum[4];
         unit_q_stats<4>(qb, false, qmax, qsum);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          qh[i] = bf2f(qb[i * kHeadDim + r]) * (BF16 ? 1.0f : KCW ? pow2_head(qmax[i]) : pow2_prescale(qmax[i]));
       }
       // Q' operand: token-wise K uses q (written once per segment per slot);
       // channel-wise K folds this group's scales into q.
@@ -609,14 +631,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PA(5, c4)
       KVQ_PT(c3)
       if (KCW || (sl ? slot_seg1 : slot_seg0) != seg) {
-        float sd = 1.0f, smax = 1.0f;
-        if (KCW) { sd = h2f(ks[r]); smax = max_f16_128(ks); }
-        float qs[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) qs[i] = BF16 ? 1.0f : pow2_prescale(qmax[i] * smax);
-        float4 v = make_float4(qv[0] * sd * qs[0], qv[1] * sd * qs[1], qv[2] * sd * qs[2], qv[3] * sd * qs[3]);
+        float f = 1.0f;
+        if (KCW) f = BF16 ? h2f(ks[r]) : h2f(ks[r]) * pow2_group(f16_exp_field(max_f16_bits_128(ks)));
+        const float4 v = make_float4(qh[0] * f, qh[1] * f, qh[2] * f, qh[3] * f);
         *reinterpret_cast<uint4*>(qop + sl * C::kBBytes + b_row_off<BF16>(qrow)) =
-            BF16 ? split2_bf16(v) : split3_e4m3(v);
+            BF16 ? split2_bf16(v) : (KCW ? split3_e4m3_via_f16(v) : split3_e4m3(v));
         fence_proxy_async_smem();
         if (sl) slot_seg1 = seg; else slot_seg0 = seg;
       }
@@ -639,8 +658,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
     // V codes of tile t -> A_V[a] (row r = channel r); releases the stage
     auto v_part = [&](int t) -> bool {
-      const int s = t % C::kStages, a = t % C::kNA;
-      const uint32_t pa = (uint32_t)(t / C::kNA) & 1u;
+      const int s = t % C::kStages, a = t % C::kNAV;
+      const uint32_t pa = (uint32_t)(t / C::kNAV) & 1u;
       KVQ_PT(c5)
       if (!warp_wait(&sh.av_empty[a], pa ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(6, c5)
@@ -878,8 +897,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         unit_q_stats<4>(qb, !KCW, qmax, qsum);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          if (KCW) {
+          if (KCW) {  // add[] holds the per-segment part of the score multiplier
             qi[k] = bf2f(qb[k * kHeadDim + i]);
+            add[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_head_inv(qmax[k])) * p.sm_scale_log2;
           } else {  // token-wise K: S = s_l * (q . code) + z_l * sum(q), constant factors per segment
             mult[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_prescale_inv(qmax[k])) * p.sm_scale_log2;
             add[k] = qsum[k] * p.sm_scale_log2;
@@ -918,11 +938,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         const float ks_i = h2f(szp[i]), kz_i = h2f(szp[kBlockTokens + i]);
         vs_t[u] = h2f(szp[2 * kBlockTokens + i]);
         vz_t[u] = h2f(szp[3 * kBlockTokens + i]);
-        if (KCW) {  // this group's Q' prescale (the value the converters used)
-          const float smax = max_f16_128(szp);
+        if (KCW) {  // undo this group's Q' prescale (the factor the converters used)
+          const float fs = BF16 ? 1.0f : pow2_group_inv(f16_exp_field(max_f16_bits_128(szp)));
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mult[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_prescale_inv(qmax[k] * smax)) * p.sm_scale_log2;
+          for (int k = 0; k < 4; ++k) mult[k] = add[k] * fs;
         }
         if (!VCW) vals[kVM + u] = h2f((uint16_t)__reduce_max_sync(FULL, (uint32_t)szp[2 * kBlockTokens + i]));
         tc_wait_ld();

@@ -73,7 +73,7 @@ struct DecodeCfg {
   static constexpr int kStageBytes = 2 * kBlockBytes + 4 * kSzBytes;
   static constexpr int kACols = BF16 ? 64 : 32;  // tensor-memory columns of one 128 x 128 A tile
   static constexpr int kNAK = BF16 ? 1 : 2;      // A tile buffers: K codes
-  static constexpr int kNAV = BF16 ? 1 : 2;      // A tile buffers: V codes
+  static constexpr int kNAV = BF16 ? 1 : 3;      // A tile buffers: V codes (the converters run ahead of PV)
   static constexpr int kSplits = BF16 ? 2 : 3;   // parts of Q' and P'
   static constexpr int kBBytes = BF16 ? 4096 : 2048;  // one B operand (128 K-rows x N=16)
   static constexpr int kKSteps = BF16 ? 8 : 4;
@@ -81,7 +81,7 @@ struct DecodeCfg {
   static constexpr uint32_t kLbo = BF16 ? 256 : 128;  // K-direction core-matrix stride
   static constexpr uint32_t kSbo = 128;               // N-direction core-matrix stride
   static constexpr uint32_t kIdesc = BF16 ? make_idesc(1, 1, 0, 1, 128, 16) : make_idesc(0, 0, 0, 1, 128, 16);
-  static constexpr int kSlots = 4;  // score / probability / output buffers in flight
+  static constexpr int kSlots = BF16 ? 4 : 3;  // score / probability / output buffers in flight
   static constexpr int kColAK = 0;
   static constexpr int kColAV = kNAK * kACols;
   static constexpr int kColS = kColAV + kNAV * kACols;

@@ -700,9 +700,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     uint32_t grp_phase = 0;
     const float kLn2 = 0.69314718055994530942f;
     const float kFix = 67108864.0f;  // 2^26: fixed-point scale of p for integer warp sums
-    // reduction-round payload slots: [0,8) tile maxima, [8,16) channel-wise K
-    // offsets q.z_g, [16,24) channel-wise V previous tiles' sum(p), [24,26)
-    // token-wise V largest scale; value v = tile * 4 + head within a block
+    // reduction-round payload slots: [0,8) score maxima, per tile for
+    // channel-wise K (value tile * 4 + head), per pair for token-wise K (value
+    // head); [8,16) channel-wise K offsets q.z_g (tile * 4 + head); [16,24)
+    // channel-wise V previous tiles' sum(p); 24: token-wise V largest scale
+    // of the pair
     constexpr int kTM = 0, kCG = 8, kWS = 16, kVM = 24, kNV = 26;
     const bool lane_max = (lane < kCG) || (lane >= kVM);  // lane's value combines by max, else by sum
 
@@ -733,11 +735,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
     // One cross-warp round: lane 0 of every warp publishes `vals`, then lane
     // v merges value v over the four warps and the results are broadcast.
-    auto round = [&](const float (&vals)[kNV], float (&res)[kNV]) -> bool {
+    // `used` (bit v = value v) selects the values published and broadcast;
+    // callers pass compile-time masks.
+    auto round = [&](const float (&vals)[kNV], float (&res)[kNV], uint32_t used) -> bool {
       float* red = sh.sw_red[grp_phase][sw];
       if (lane == 0) {
 #pragma unroll
-        for (int v = 0; v < kNV; v += 2) *reinterpret_cast<float2*>(red + v) = make_float2(vals[v], vals[v + 1]);
+        for (int v = 0; v < kNV; v += 2) {
+          const uint32_t two = (used >> v) & 3u;
+          if (two == 3u) *reinterpret_cast<float2*>(red + v) = make_float2(vals[v], vals[v + 1]);
+          else if (two == 1u) red[v] = vals[v];
+          else if (two == 2u) red[v + 1] = vals[v + 1];
+        }
       }
       const uint32_t use = grp_phase;
       if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
@@ -746,7 +755,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const float r2 = sh.sw_red[use][2][v], r3 = sh.sw_red[use][3][v];
       const float mine = lane_max ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : (r0 + r1) + (r2 + r3);
 #pragma unroll
-      for (int k = 0; k < kNV; ++k) res[k] = __shfl_sync(FULL, mine, k);
+      for (int k = 0; k < kNV; ++k) res[k] = ((used >> k) & 1u) ? __shfl_sync(FULL, mine, k) : 0.f;
       return true;
     };
 
@@ -790,7 +799,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       for (int k = 0; k < kNV; ++k) vals[k] = 0.f;
 #pragma unroll
       for (int k = 0; k < 8; ++k) vals[kWS + k] = ws_prev[k];
-      if (!round(vals, res)) return false;
+      if (!round(vals, res, 0xffu << kWS)) return false;
 #pragma unroll
       for (int k = 0; k < 8; ++k) ts[k] = res[kWS + k];
       return true;
@@ -803,7 +812,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       for (int k = 0; k < kNV; ++k) vals[k] = 0.f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) { vals[kCG + k] = warp_sum(lp[k]); vals[kCG + 4 + k] = VCW ? 0.f : warp_sum(zp[k]); }
-      if (!round(vals, res)) return false;
+      if (!round(vals, res, 0xffu << kCG)) return false;
       float out4[4], lse4[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -943,7 +952,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 #pragma unroll
           for (int k = 0; k < 4; ++k) mult[k] = add[k] * fs;
         }
-        if (!VCW) vals[kVM + u] = h2f((uint16_t)__reduce_max_sync(FULL, (uint32_t)szp[2 * kBlockTokens + i]));
         tc_wait_ld();
         tc_fence_before();
         __syncwarp();
@@ -956,11 +964,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           // channel-wise K adds q . z_g once reduced over channels
           const float v = KCW ? a * mult[k] : fmaf(a * mult[k], ks_i, kz_i * add[k]);
           sc[4 * u + k] = valid ? v : -INFINITY;
-          vals[kTM + 4 * u + k] = warp_max_redux(sc[4 * u + k]);
-          if (KCW) vals[kCG + 4 * u + k] = warp_sum(qi[k] * kz_i);
+          if (KCW) {  // the tile's offset q . z_g is still to come: per-tile maxima
+            vals[kTM + 4 * u + k] = warp_max_redux(sc[4 * u + k]);
+            vals[kCG + 4 * u + k] = warp_sum(qi[k] * kz_i);
+          }
         }
       }
       if (!ok) break;
+      if (!KCW) {  // one maximum per head over both tiles
+#pragma unroll
+        for (int k = 0; k < 4; ++k) vals[kTM + k] = warp_max_redux(fmaxf(sc[k], sc[4 + k]));
+      }
+      // token-wise V: largest V scale of the pair (positive: ordered as integers)
+      if (!VCW) vals[kVM] = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(fmaxf(vs_t[0], vs_t[1]))));
       if (VCW) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) vals[kWS + k] = ws_prev[k];
@@ -968,7 +984,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PA(16, s0)
       KVQ_PT(s2)
       float res[kNV];
-      if (!round(vals, res)) { ok = false; break; }
+      constexpr uint32_t kUsed = (KCW ? 0xffffu : 0xfu) | (VCW ? (0xffu << kWS) : (1u << kVM));
+      if (!round(vals, res, kUsed)) { ok = false; break; }
       KVQ_PA(18, s2)
       KVQ_PT(s3)
       // one running-max update for the pair
@@ -977,7 +994,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       for (int k = 0; k < 4; ++k) {
         const float cg0 = KCW ? res[kCG + k] * p.sm_scale_log2 : 0.f;
         const float cg1 = KCW ? res[kCG + 4 + k] * p.sm_scale_log2 : 0.f;
-        const float mn = fmaxf(m[k], fmaxf(res[kTM + k] + cg0, res[kTM + 4 + k] + cg1));
+        const float mt = KCW ? fmaxf(res[kTM + k] + cg0, res[kTM + 4 + k] + cg1) : res[kTM + k];
+        const float mn = fmaxf(m[k], mt);
         alpha[k] = ex2(m[k] - mn);
         m[k] = mn;
         pr[k] = ex2(sc[k] + cg0 - mn);
@@ -991,8 +1009,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         if (u >= n) break;
         const int tt = t + u, sl = tt % C::kSlots;
         const uint32_t p2 = (uint32_t)(tt / C::kSlots) & 1u;
-        const float pscale = VCW ? 256.0f : (BF16 ? 1.0f : pow2_prescale(res[kVM + u]));
-        pv_scale_t[u] = VCW ? (1.0f / 256.0f) : (BF16 ? 1.0f : pow2_prescale_inv(res[kVM + u]));
+        const float pscale = VCW ? 256.0f : (BF16 ? 1.0f : pow2_prescale(res[kVM]));
+        pv_scale_t[u] = VCW ? (1.0f / 256.0f) : (BF16 ? 1.0f : pow2_prescale_inv(res[kVM]));
         const float pmul = VCW ? pscale : vs_t[u] * pscale;
         const float4 pv = make_float4(pr[4 * u] * pmul, pr[4 * u + 1] * pmul, pr[4 * u + 2] * pmul, pr[4 * u + 3] * pmul);
         const uint4 bytes = BF16 ? split2_bf16(pv) : split3_e4m3_via_f16(pv);

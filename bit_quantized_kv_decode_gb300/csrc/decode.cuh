@@ -45,13 +45,23 @@ namespace kvq {
 // KVQ_PROFILE is defined; the library build never defines it).  Probes add
 // into shared memory: a global atomic per probe would stall the next
 // mbarrier arrive, whose release semantics wait for it to complete.
-#ifdef KVQ_PROFILE
+#if defined(KVQ_PROFILE) && !defined(KVQ_TRACE)
 #define KVQ_PT(n) long long kvq_pt_##n = clock64();
 #define KVQ_PA(slot, n) \
   if (p.prof != nullptr && (threadIdx.x & 31) == 0) atomicAdd(&sh.prof[slot], (unsigned long long)(clock64() - kvq_pt_##n));
 #else
 #define KVQ_PT(n)
 #define KVQ_PA(slot, n)
+#endif
+// Optional per-tile event timeline (KVQ_TRACE with KVQ_PROFILE): lane 0 of
+// the recording warp stamps event ev of tile t (a window of tiles) in shared
+// memory; the CTA dumps it to the profiling buffer at exit.
+constexpr int kTrT0 = 200, kTrN = 64, kTrEv = 16;
+#ifdef KVQ_TRACE
+#define KVQ_TR(ev, t) \
+  { if ((threadIdx.x & 31) == 0 && (t) >= kTrT0 && (t) < kTrT0 + kTrN) sh.trace[((t) - kTrT0) * kTrEv + (ev)] = clock64(); }
+#else
+#define KVQ_TR(ev, t) {}
 #endif
 
 constexpr int kDecodeThreads = 320;  // 10 warps
@@ -103,6 +113,15 @@ __device__ __forceinline__ int a_pos(int e) {
     if (BITS == 4) return (e & ~7) + ((e & 3) << 1) + ((e & 7) >> 2);
     return (e & ~15) + ((e & 7) << 1) + ((e & 15) >> 3);
   }
+}
+
+// The used columns of one S / O slot (4 heads x 3 parts; 2 parts for BF16):
+// a single 12- or 8-column load instead of all 16.
+template <bool BF16>
+__device__ __forceinline__ void tmem_ld_parts(uint32_t taddr, uint32_t (&r)[12]) {
+  tmem_ld_32x32b_x8(taddr, r);
+  if (!BF16) tmem_ld_32x32b_x4(taddr + 8, r + 8);
+  else r[8] = r[9] = r[10] = r[11] = 0u;
 }
 
 // Byte offset of B-operand row p (MN-major, no swizzle).
@@ -257,6 +276,9 @@ struct alignas(16) DecodeBarriers {
   int total_tiles;
 #ifdef KVQ_PROFILE
   unsigned long long prof[32];  // cycle accounting, flushed to global memory at exit
+#endif
+#ifdef KVQ_TRACE
+  long long trace[kTrN * kTrEv];
 #endif
 };
 
@@ -420,6 +442,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 #ifdef KVQ_PROFILE
     for (int s = 0; s < 32; ++s) sh.prof[s] = 0ull;
 #endif
+#ifdef KVQ_TRACE
+    for (int j = 0; j < kTrN * kTrEv; ++j) sh.trace[j] = 0;
+#endif
     mbar_init(&sh.drain, 1);
     sh.abort_flag = 0;
     fence_barrier_init();
@@ -499,6 +524,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                              policy);
         issued |= 1u << s;
         issued_par = (issued_par & ~(1u << s)) | (ph << s);
+        KVQ_TR(15, t)
       }
       // never leave a copy in flight: wait for every issued stage to land
       for (int s = 0; s < C::kStages; ++s)
@@ -534,6 +560,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             tc_commit(&sh.av_empty[a]);
             tc_commit(&sh.p_empty[sl]);
             tc_commit(&sh.o_full[sl]);
+            KVQ_TR(8, np)
             ++np;
             progressed = true;
           }
@@ -555,6 +582,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             tc_commit(&sh.ak_empty[a]);
             tc_commit(&sh.q_empty[q2]);
             tc_commit(&sh.s_full[sl]);
+            KVQ_TR(7, nq)
             ++nq;
             progressed = true;
           }
@@ -610,9 +638,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const int s = t % C::kStages, a = t % C::kNAK, sl = t & 1;
       const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNAK) & 1u,
                      p2 = (uint32_t)(t >> 1) & 1u;
+      if (warp == 0) KVQ_TR(0, t)
       KVQ_PT(c0)
       if (!warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) return false;
       KVQ_PA(1, c0)
+      if (warp == 0) KVQ_TR(1, t)
       const unsigned char* st = stages + (size_t)s * C::kStageBytes;
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
       if (t == 0 || it.j == 0) {  // new (sequence, kv head): its four query rows
@@ -642,10 +672,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.q_full[sl]);
       KVQ_PA(4, c3)
+      if (warp == 0) KVQ_TR(2, t)
       // K codes -> A_K[a] (row r = token r)
       KVQ_PT(c1)
       if (!warp_wait(&sh.ak_empty[a], pa ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(2, c1)
+      if (warp == 0) KVQ_TR(3, t)
       KVQ_PT(c2)
       convert_rows(st, tmem + lane_off + C::kColAK + a * C::kACols);
       tc_wait_st();
@@ -653,6 +685,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.ak_full[a]);
       KVQ_PA(7, c2)
+      if (warp == 0) KVQ_TR(4, t)
       return true;
     };
 
@@ -663,6 +696,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PT(c5)
       if (!warp_wait(&sh.av_empty[a], pa ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(6, c5)
+      if (warp == 0) KVQ_TR(5, t)
       KVQ_PT(c6)
       convert_rows(stages + (size_t)s * C::kStageBytes + C::kBlockBytes, tmem + lane_off + C::kColAV + a * C::kACols);
       tc_wait_st();
@@ -673,6 +707,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         mbar_arrive(&sh.stg_empty[s]);
       }
       KVQ_PA(8, c6)
+      if (warp == 0) KVQ_TR(6, t)
       return true;
     };
 
@@ -760,34 +795,43 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     };
 
     // PV epilogue of the previous step's tiles: O = O * alpha + folded partial products
+    // Both partial products are awaited and loaded together (a lone tile is
+    // loaded twice and its copy masked out).
     auto epilogue = [&](const float (&ts)[8]) -> bool {
-      float o_add[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (u >= pend_n) break;
-        const int t = pend + u;
-        const int sl = t % C::kSlots;
-        const uint32_t p2 = (uint32_t)(t / C::kSlots) & 1u;
-        KVQ_PT(e0)
-        if (!warp_wait(&sh.o_full[sl], p2, abort_flag, limit)) return false;
-        KVQ_PA(23, e0)
-        tc_fence_after();
-        uint32_t acc[16];
-        tmem_ld_32x32b_x16(tmem + lane_off + C::kColO + 16 * sl, acc);
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.o_empty[sl]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float o = __uint_as_float(acc[k]) + __uint_as_float(acc[4 + k]);
-          if (!BF16) o += __uint_as_float(acc[8 + k]);
-          o *= pinv_prev[u];
-          o_add[k] += VCW ? fmaf(sv_prev[u], o, zv_prev[u] * ts[4 * u + k]) : o;
-        }
+      const int tA = pend, tB = pend_n > 1 ? pend + 1 : pend;
+      const int oA = tA % C::kSlots, oB = tB % C::kSlots;
+      KVQ_PT(e0)
+      if (!warp_wait(&sh.o_full[oA], (uint32_t)(tA / C::kSlots) & 1u, abort_flag, limit) ||
+          !warp_wait(&sh.o_full[oB], (uint32_t)(tB / C::kSlots) & 1u, abort_flag, limit))
+        return false;
+      KVQ_PA(23, e0)
+      if (sw == 0) { KVQ_TR(13, tA) if (pend_n > 1) KVQ_TR(13, tB) }
+      tc_fence_after();
+      uint32_t acc[2][12];
+      tmem_ld_parts<BF16>(tmem + lane_off + C::kColO + 16 * oA, acc[0]);
+      tmem_ld_parts<BF16>(tmem + lane_off + C::kColO + 16 * oB, acc[1]);
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sh.o_empty[oA]);
+        if (pend_n > 1) mbar_arrive(&sh.o_empty[oB]);
       }
+      if (sw == 0) { KVQ_TR(14, tA) if (pend_n > 1) KVQ_TR(14, tB) }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) O[k] = fmaf(O[k], a_prev[k], o_add[k]);
+      for (int k = 0; k < 4; ++k) {
+        float o[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          o[u] = __uint_as_float(acc[u][k]) + __uint_as_float(acc[u][4 + k]);
+          if (!BF16) o[u] += __uint_as_float(acc[u][8 + k]);
+          o[u] *= pinv_prev[u];
+        }
+        if (pend_n < 2) o[1] = 0.f;
+        const float o_add = VCW ? fmaf(sv_prev[0], o[0], zv_prev[0] * ts[k]) + fmaf(sv_prev[1], o[1], zv_prev[1] * ts[4 + k])
+                                : o[0] + o[1];
+        O[k] = fmaf(O[k], a_prev[k], o_add);
+      }
       return true;
     };
 
@@ -920,57 +964,65 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const int len = lens[it.b];
 
       KVQ_PT(s0)
+      if (sw == 0) { KVQ_TR(10, t) if (n > 1) KVQ_TR(10, t + 1) }
       float sc[8], vs_t[2], vz_t[2], pv_scale_t[2];
       float vals[kNV];
 #pragma unroll
       for (int k = 0; k < kNV; ++k) vals[k] = 0.f;
+      // Both tiles' scores are normally complete well before the step: wait
+      // for both, then load them together so the two tiles' work interleaves
+      // (a lone tile is loaded twice and its copy masked out).
+      const int t1 = n > 1 ? t + 1 : t;
+      const int st0 = t % C::kStages, st1 = t1 % C::kStages, q0 = t % C::kSlots, q1 = t1 % C::kSlots;
+      if (!warp_wait(&sh.s_full[q0], (uint32_t)(t / C::kSlots) & 1u, abort_flag, limit) ||
+          !warp_wait(&sh.s_full[q1], (uint32_t)(t1 / C::kSlots) & 1u, abort_flag, limit) ||
+          !warp_wait(&sh.stg_full[st0], (uint32_t)(t / C::kStages) & 1u, abort_flag, limit) ||
+          !warp_wait(&sh.stg_full[st1], (uint32_t)(t1 / C::kStages) & 1u, abort_flag, limit)) {
+        ok = false;
+        break;
+      }
+      if (sw == 0) { KVQ_TR(9, t) if (n > 1) KVQ_TR(9, t + 1) }
+      tc_fence_after();
+      uint32_t acc[2][12];
+      tmem_ld_parts<BF16>(tmem + lane_off + C::kColS + 16 * q0, acc[0]);
+      tmem_ld_parts<BF16>(tmem + lane_off + C::kColS + 16 * q1, acc[1]);
+      float ks_t[2], kz_t[2], fs_t[2] = {1.f, 1.f};
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        if (u >= n) {  // no second tile: neutral values
-#pragma unroll
-          for (int k = 0; k < 4; ++k) { sc[4 * u + k] = -INFINITY; vals[kTM + 4 * u + k] = -INFINITY; }
-          vs_t[u] = 0.f; vz_t[u] = 0.f;
-          continue;
-        }
-        const int tt = t + u;
-        const int s = tt % C::kStages, sl = tt % C::kSlots;
-        const uint32_t ps = (uint32_t)(tt / C::kStages) & 1u, p2 = (uint32_t)(tt / C::kSlots) & 1u;
-        if (!warp_wait(&sh.s_full[sl], p2, abort_flag, limit) || !warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t acc[16];
-        tmem_ld_32x32b_x16(tmem + lane_off + C::kColS + 16 * sl, acc);
-        const unsigned char* st = stages + (size_t)s * C::kStageBytes;
-        const uint16_t* szp = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
-        const float ks_i = h2f(szp[i]), kz_i = h2f(szp[kBlockTokens + i]);
+        const uint16_t* szp = reinterpret_cast<const uint16_t*>(stages + (size_t)(u ? st1 : st0) * C::kStageBytes +
+                                                                2 * C::kBlockBytes);
+        ks_t[u] = h2f(szp[i]);
+        kz_t[u] = h2f(szp[kBlockTokens + i]);
         vs_t[u] = h2f(szp[2 * kBlockTokens + i]);
         vz_t[u] = h2f(szp[3 * kBlockTokens + i]);
-        if (KCW) {  // undo this group's Q' prescale (the factor the converters used)
-          const float fs = BF16 ? 1.0f : pow2_group_inv(f16_exp_field(max_f16_bits_128(szp)));
+        // channel-wise K: undo this group's Q' prescale (the converters' factor)
+        if (KCW && !BF16) fs_t[u] = pow2_group_inv(f16_exp_field(max_f16_bits_128(szp)));
+      }
+      if (n < 2) { kz_t[1] = 0.f; vs_t[1] = 0.f; vz_t[1] = 0.f; }
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sh.s_empty[q0]);
+        mbar_arrive(&sh.stg_empty[st0]);
+        if (n > 1) { mbar_arrive(&sh.s_empty[q1]); mbar_arrive(&sh.stg_empty[st1]); }
+      }
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mult[k] = add[k] * fs;
-        }
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) { mbar_arrive(&sh.s_empty[sl]); mbar_arrive(&sh.stg_empty[s]); }
-        const bool valid = i < len - (it.j + u) * kBlockTokens;
+      for (int u = 0; u < 2; ++u) {
+        const bool valid = u < n && i < len - (it.j + u) * kBlockTokens;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          float a = __uint_as_float(acc[k]) + __uint_as_float(acc[4 + k]);
-          if (!BF16) a += __uint_as_float(acc[8 + k]);
+          float a = __uint_as_float(acc[u][k]) + __uint_as_float(acc[u][4 + k]);
+          if (!BF16) a += __uint_as_float(acc[u][8 + k]);
           // channel-wise K adds q . z_g once reduced over channels
-          const float v = KCW ? a * mult[k] : fmaf(a * mult[k], ks_i, kz_i * add[k]);
+          const float v = KCW ? a * (add[k] * fs_t[u]) : fmaf(a * mult[k], ks_t[u], kz_t[u] * add[k]);
           sc[4 * u + k] = valid ? v : -INFINITY;
           if (KCW) {  // the tile's offset q . z_g is still to come: per-tile maxima
             vals[kTM + 4 * u + k] = warp_max_redux(sc[4 * u + k]);
-            vals[kCG + 4 * u + k] = warp_sum(qi[k] * kz_i);
+            vals[kCG + 4 * u + k] = warp_sum(qi[k] * kz_t[u]);
           }
         }
       }
-      if (!ok) break;
       if (!KCW) {  // one maximum per head over both tiles
 #pragma unroll
         for (int k = 0; k < 4; ++k) vals[kTM + k] = warp_max_redux(fmaxf(sc[k], sc[4 + k]));
@@ -987,6 +1039,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       constexpr uint32_t kUsed = (KCW ? 0xffffu : 0xfu) | (VCW ? (0xffu << kWS) : (1u << kVM));
       if (!round(vals, res, kUsed)) { ok = false; break; }
       KVQ_PA(18, s2)
+      if (sw == 0) { KVQ_TR(11, t) if (n > 1) KVQ_TR(11, t + 1) }
       KVQ_PT(s3)
       // one running-max update for the pair
       float pr[8], alpha[4];
@@ -1003,26 +1056,34 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         lp[k] = fmaf(lp[k], alpha[k], pr[k] + pr[4 + k]);
         if (!VCW) zp[k] = fmaf(zp[k], alpha[k], fmaf(pr[k], vz_t[0], pr[4 + k] * vz_t[1]));
       }
-      // P' operands (lane i = token i): token-wise V folds s into P
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (u >= n) break;
-        const int tt = t + u, sl = tt % C::kSlots;
-        const uint32_t p2 = (uint32_t)(tt / C::kSlots) & 1u;
-        const float pscale = VCW ? 256.0f : (BF16 ? 1.0f : pow2_prescale(res[kVM]));
-        pv_scale_t[u] = VCW ? (1.0f / 256.0f) : (BF16 ? 1.0f : pow2_prescale_inv(res[kVM]));
-        const float pmul = VCW ? pscale : vs_t[u] * pscale;
-        const float4 pv = make_float4(pr[4 * u] * pmul, pr[4 * u + 1] * pmul, pr[4 * u + 2] * pmul, pr[4 * u + 3] * pmul);
-        const uint4 bytes = BF16 ? split2_bf16(pv) : split3_e4m3_via_f16(pv);
-        if (!warp_wait(&sh.p_empty[sl], p2 ^ 1u, abort_flag, limit)) { ok = false; break; }
-        *reinterpret_cast<uint4*>(pop + sl * C::kBBytes + b_row_off<BF16>(prow)) = bytes;
+      // P' operands (lane i = token i): token-wise V folds s into P; both
+      // buffers are awaited first so the two rows are built together
+      if (!warp_wait(&sh.p_empty[q0], ((uint32_t)(t / C::kSlots) & 1u) ^ 1u, abort_flag, limit) ||
+          !warp_wait(&sh.p_empty[q1], ((uint32_t)(t1 / C::kSlots) & 1u) ^ 1u, abort_flag, limit)) {
+        ok = false;
+        break;
       }
-      if (!ok) break;
+      {
+        const float pscale = VCW ? 256.0f : (BF16 ? 1.0f : pow2_prescale(res[kVM]));
+        const float pinv = VCW ? (1.0f / 256.0f) : (BF16 ? 1.0f : pow2_prescale_inv(res[kVM]));
+        uint4 bytes[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          pv_scale_t[u] = pinv;
+          const float pmul = VCW ? pscale : vs_t[u] * pscale;
+          const float4 pv = make_float4(pr[4 * u] * pmul, pr[4 * u + 1] * pmul, pr[4 * u + 2] * pmul, pr[4 * u + 3] * pmul);
+          bytes[u] = BF16 ? split2_bf16(pv) : split3_e4m3_via_f16(pv);
+        }
+        *reinterpret_cast<uint4*>(pop + q0 * C::kBBytes + b_row_off<BF16>(prow)) = bytes[0];
+        if (n > 1) *reinterpret_cast<uint4*>(pop + q1 * C::kBBytes + b_row_off<BF16>(prow)) = bytes[1];
+      }
       fence_proxy_async_smem();  // both P' rows visible to the tensor core
       __syncwarp();
       if (lane == 0) {
-        for (int u = 0; u < n; ++u) mbar_arrive(&sh.p_full[(t + u) % C::kSlots]);
+        mbar_arrive(&sh.p_full[q0]);
+        if (n > 1) mbar_arrive(&sh.p_full[q1]);
       }
+      if (sw == 0) { KVQ_TR(12, t) if (n > 1) KVQ_TR(12, t + 1) }
       KVQ_PA(19, s3)
 
       // epilogue of the previous step (its sums of p arrived in this round)
@@ -1063,8 +1124,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-#ifdef KVQ_PROFILE
+#if defined(KVQ_PROFILE) && !defined(KVQ_TRACE)
   if (p.prof != nullptr && tid < 32) atomicAdd(&p.prof[blockIdx.x * 32 + tid], sh.prof[tid]);
+#endif
+#ifdef KVQ_TRACE
+  if (p.prof != nullptr)
+    for (int j = tid; j < kTrN * kTrEv; j += kDecodeThreads) p.prof[(size_t)blockIdx.x * kTrN * kTrEv + j] = sh.trace[j];
 #endif
 }
 

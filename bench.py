@@ -224,39 +224,41 @@ def _oracle_unit(args):
     _ = np
 
 
-def oracle_sample(w, seed, n_units, dev=None):
-    """Packed inputs of the first n_units (sequence, kv head) units, packed by the
-    oracle from the workload's own pre-quantization values."""
+def oracle_pack_unit(args):
+    """Packed inputs of one (sequence, kv head) unit, packed by the oracle from the
+    workload's own pre-quantization values (runs in a pool worker)."""
     import numpy as np
     from oracle import kvq_oracle as orc
+    w, seed, u = args
     lens = synth.seq_lens_for(w, seed)
     q = synth.query(w, seed)
     cs = synth.outlier_channels(w, seed)
-    jobs = []
-    for u in range(n_units):
-        b, h = divmod(u, w.num_kv_heads)
-        b %= w.batch
-        n = int(lens[b])
-        k = synth.kv_unit(w, seed, 0, b, h, n, "cpu", cs[h]).numpy()[None, None]
-        v = synth.kv_unit(w, seed, 1, b, h, n, "cpu").numpy()[None, None]
-        kcodes, ks, kz = orc.pack_cache(k, [n], w.bits, w.k_scheme, 0)
-        vcodes, vs, vz = orc.pack_cache(v, [n], w.bits, w.v_scheme, 1)
-        qb = q[b:b + 1, 4 * h:4 * h + 4].contiguous().view(torch.int16).numpy().view(np.uint16)
-        jobs.append((qb, kcodes, ks, kz, vcodes, vs, vz, n, w.bits, w.k_scheme, w.v_scheme))
-    return jobs, lens
+    b, h = divmod(u, w.num_kv_heads)
+    b %= w.batch
+    n = int(lens[b])
+    k = synth.kv_unit(w, seed, 0, b, h, n, "cpu", cs[h]).numpy()[None, None]
+    v = synth.kv_unit(w, seed, 1, b, h, n, "cpu").numpy()[None, None]
+    kcodes, ks, kz = orc.pack_cache(k, [n], w.bits, w.k_scheme, 0)
+    vcodes, vs, vz = orc.pack_cache(v, [n], w.bits, w.v_scheme, 1)
+    qb = q[b:b + 1, 4 * h:4 * h + 4].contiguous().view(torch.int16).numpy().view(np.uint16)
+    return (qb, kcodes, ks, kz, vcodes, vs, vz, n, w.bits, w.k_scheme, w.v_scheme)
+
+
+ORACLE_UNITS = 128  # default sample: about 10 core-seconds of oracle decode on the GPU host
 
 
 class OracleTimer:
     """Times the CPU oracle on a bounded sample of the workload: the first
-    `units` (sequence, kv head) units, packed once by the oracle, then decoded
-    (unpack + dequantize + attend, fp64) by one spawned process per host core."""
+    `units` (sequence, kv head) units, packed once by the oracle (in the pool,
+    untimed), then decoded (unpack + dequantize + attend, fp64) by one spawned
+    process per host core."""
 
     def __init__(self, w, seed, units=None):
         import multiprocessing as mp
         total_units = w.batch * w.num_kv_heads
-        self.units = min(units or min(os.cpu_count() or 1, 16), total_units)
+        self.units = min(units or ORACLE_UNITS, total_units)
         self.cores = max(1, min(os.cpu_count() or 1, 16, self.units))
-        self.jobs, lens = oracle_sample(w, seed, self.units)
+        lens = synth.seq_lens_for(w, seed)
         self.sample_lens = [int(lens[divmod(u, w.num_kv_heads)[0] % w.batch]) for u in range(self.units)]
         self.bytes = sum(((n + 127) // 128) * (2 * (128 * 128 * w.bits // 8) + 2 * 2 * 128 * 2)
                          for n in self.sample_lens)
@@ -269,6 +271,7 @@ class OracleTimer:
             os.environ.pop("OMP_NUM_THREADS", None)
         else:
             os.environ["OMP_NUM_THREADS"] = old
+        self.jobs = self.pool.map(oracle_pack_unit, [(w, seed, u) for u in range(self.units)])
         self.pool.map(_oracle_unit, self.jobs[:self.cores])  # warm-up: imports and first touch
 
     def step(self) -> float:

@@ -56,7 +56,7 @@ namespace kvq {
 // Optional per-tile event timeline (KVQ_TRACE with KVQ_PROFILE): lane 0 of
 // the recording warp stamps event ev of tile t (a window of tiles) in shared
 // memory; the CTA dumps it to the profiling buffer at exit.
-constexpr int kTrT0 = 200, kTrN = 64, kTrEv = 16;
+constexpr int kTrT0 = 200, kTrN = 64, kTrEv = 24;
 #ifdef KVQ_TRACE
 #define KVQ_TR(ev, t) \
   { if ((threadIdx.x & 31) == 0 && (t) >= kTrT0 && (t) < kTrT0 + kTrN) sh.trace[((t) - kTrT0) * kTrEv + (ev)] = clock64(); }
@@ -524,7 +524,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                              policy);
         issued |= 1u << s;
         issued_par = (issued_par & ~(1u << s)) | (ph << s);
-        KVQ_TR(15, t)
+        KVQ_TR(21, t)
       }
       // never leave a copy in flight: wait for every issued stage to land
       for (int s = 0; s < C::kStages; ++s)
@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             tc_commit(&sh.av_empty[a]);
             tc_commit(&sh.p_empty[sl]);
             tc_commit(&sh.o_full[sl]);
-            KVQ_TR(8, np)
+            KVQ_TR(17, np)
             ++np;
             progressed = true;
           }
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             tc_commit(&sh.ak_empty[a]);
             tc_commit(&sh.q_empty[q2]);
             tc_commit(&sh.s_full[sl]);
-            KVQ_TR(7, nq)
+            KVQ_TR(16, nq)
             ++nq;
             progressed = true;
           }
@@ -638,11 +638,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const int s = t % C::kStages, a = t % C::kNAK, sl = t & 1;
       const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNAK) & 1u,
                      p2 = (uint32_t)(t >> 1) & 1u;
-      if (warp == 0) KVQ_TR(0, t)
       KVQ_PT(c0)
       if (!warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) return false;
       KVQ_PA(1, c0)
-      if (warp == 0) KVQ_TR(1, t)
       const unsigned char* st = stages + (size_t)s * C::kStageBytes;
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
       if (t == 0 || it.j == 0) {  // new (sequence, kv head): its four query rows
@@ -672,12 +670,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.q_full[sl]);
       KVQ_PA(4, c3)
-      if (warp == 0) KVQ_TR(2, t)
       // K codes -> A_K[a] (row r = token r)
       KVQ_PT(c1)
       if (!warp_wait(&sh.ak_empty[a], pa ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(2, c1)
-      if (warp == 0) KVQ_TR(3, t)
       KVQ_PT(c2)
       convert_rows(st, tmem + lane_off + C::kColAK + a * C::kACols);
       tc_wait_st();
@@ -685,7 +681,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.ak_full[a]);
       KVQ_PA(7, c2)
-      if (warp == 0) KVQ_TR(4, t)
+      KVQ_TR(0 + warp, t)
       return true;
     };
 
@@ -696,7 +692,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PT(c5)
       if (!warp_wait(&sh.av_empty[a], pa ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(6, c5)
-      if (warp == 0) KVQ_TR(5, t)
       KVQ_PT(c6)
       convert_rows(stages + (size_t)s * C::kStageBytes + C::kBlockBytes, tmem + lane_off + C::kColAV + a * C::kACols);
       tc_wait_st();
@@ -707,7 +702,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         mbar_arrive(&sh.stg_empty[s]);
       }
       KVQ_PA(8, c6)
-      if (warp == 0) KVQ_TR(6, t)
+      KVQ_TR(4 + warp, t)
       return true;
     };
 
@@ -805,7 +800,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           !warp_wait(&sh.o_full[oB], (uint32_t)(tB / C::kSlots) & 1u, abort_flag, limit))
         return false;
       KVQ_PA(23, e0)
-      if (sw == 0) { KVQ_TR(13, tA) if (pend_n > 1) KVQ_TR(13, tB) }
+
       tc_fence_after();
       uint32_t acc[2][12];
       tmem_ld_parts<BF16>(tmem + lane_off + C::kColO + 16 * oA, acc[0]);
@@ -817,7 +812,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         mbar_arrive(&sh.o_empty[oA]);
         if (pend_n > 1) mbar_arrive(&sh.o_empty[oB]);
       }
-      if (sw == 0) { KVQ_TR(14, tA) if (pend_n > 1) KVQ_TR(14, tB) }
+      { KVQ_TR(12 + sw, tA) if (pend_n > 1) KVQ_TR(12 + sw, tB) }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         float o[2];
@@ -964,7 +959,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const int len = lens[it.b];
 
       KVQ_PT(s0)
-      if (sw == 0) { KVQ_TR(10, t) if (n > 1) KVQ_TR(10, t + 1) }
+      if (sw == 0) { KVQ_TR(19, t) if (n > 1) KVQ_TR(19, t + 1) }
       float sc[8], vs_t[2], vz_t[2], pv_scale_t[2];
       float vals[kNV];
 #pragma unroll
@@ -981,7 +976,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         ok = false;
         break;
       }
-      if (sw == 0) { KVQ_TR(9, t) if (n > 1) KVQ_TR(9, t + 1) }
+      if (sw == 0) { KVQ_TR(18, t) if (n > 1) KVQ_TR(18, t + 1) }
       tc_fence_after();
       uint32_t acc[2][12];
       tmem_ld_parts<BF16>(tmem + lane_off + C::kColS + 16 * q0, acc[0]);
@@ -1039,7 +1034,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       constexpr uint32_t kUsed = (KCW ? 0xffffu : 0xfu) | (VCW ? (0xffu << kWS) : (1u << kVM));
       if (!round(vals, res, kUsed)) { ok = false; break; }
       KVQ_PA(18, s2)
-      if (sw == 0) { KVQ_TR(11, t) if (n > 1) KVQ_TR(11, t + 1) }
+      if (sw == 0) { KVQ_TR(20, t) if (n > 1) KVQ_TR(20, t + 1) }
       KVQ_PT(s3)
       // one running-max update for the pair
       float pr[8], alpha[4];
@@ -1083,7 +1078,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         mbar_arrive(&sh.p_full[q0]);
         if (n > 1) mbar_arrive(&sh.p_full[q1]);
       }
-      if (sw == 0) { KVQ_TR(12, t) if (n > 1) KVQ_TR(12, t + 1) }
+      { KVQ_TR(8 + sw, t) if (n > 1) KVQ_TR(8 + sw, t + 1) }
       KVQ_PA(19, s3)
 
       // epilogue of the previous step (its sums of p arrived in this round)

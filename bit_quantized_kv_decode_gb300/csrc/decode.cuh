@@ -297,9 +297,10 @@ __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 // All lanes wait (sleeping inside try_wait until the phase completes); the
 // warp gives up together, after the time limit or when the CTA has been told
 // to abort.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          uint64_t limit_ns) {
-  if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+// The slow path (sleeping waits, time limit, abort check) is out of line so
+// that the hot loops stay compact in the instruction cache.
+static __device__ __noinline__ bool warp_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                            uint64_t limit_ns) {
   uint64_t t0 = 0;
   for (;;) {
     bool ok = mbar_try_wait_sleep(bar, parity, 20000u);
@@ -312,6 +313,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     }
     if (__shfl_sync(FULL, stop, 0)) return false;
   }
+}
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns) {
+  if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+  return warp_wait_slow(bar, parity, abort_flag, limit_ns);
 }
 
 __device__ __forceinline__ void set_abort(volatile int* abort_flag, uint32_t* dev_status) {

@@ -75,15 +75,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall time, or as soon as *abort becomes non-zero, and then
 // returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, const volatile int* abort,
-                                                  uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+// (The waiting loop is out of line: it keeps the callers' hot code compact.)
+static __device__ __noinline__ bool mbar_wait_bounded_slow(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                                    uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (abort != nullptr && *abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_bounded_slow(bar, parity, abort, limit_ns);
 }
 
 // -------------------------------------------------------------- bulk copies

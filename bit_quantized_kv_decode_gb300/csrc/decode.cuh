@@ -399,20 +399,68 @@ struct TileIter {
     h = r / nblk;
     j = r - h * nblk;
   }
-  __device__ __forceinline__ void next(const int* prefix, int B, int Hkv) {
-    if (++j < nblk) return;
-    j = 0;
-    if (++h < Hkv) return;
-    h = 0;
-    do { ++b; } while (b < B && prefix[b + 1] == prefix[b]);
-    if (b < B) nblk = (prefix[b + 1] - prefix[b]) / Hkv;
-  }
+  __device__ __forceinline__ void next(const int* prefix, int B, int Hkv);
 };
+
+// Next (sequence, kv head) unit after (b, h): {b, h, nblk}; out of line (it
+// runs once per unit) to keep the hot loops compact.
+static __device__ __noinline__ int3 next_unit(int b, int h, int nblk, const int* prefix, int B, int Hkv) {
+  if (++h < Hkv) return make_int3(b, h, nblk);
+  h = 0;
+  do { ++b; } while (b < B && prefix[b + 1] == prefix[b]);
+  if (b < B) nblk = (prefix[b + 1] - prefix[b]) / Hkv;
+  return make_int3(b, h, nblk);
+}
+__device__ __forceinline__ void TileIter::next(const int* prefix, int B, int Hkv) {
+  if (++j < nblk) return;
+  j = 0;
+  const int3 u = next_unit(b, h, nblk, prefix, B, Hkv);
+  b = u.x; h = u.y; nblk = u.z;
+}
 
 __device__ __forceinline__ int cta_of_tile(long long t, long long T, int C) {
   return (int)(((t + 1) * C - 1) / T);
 }
 __device__ __forceinline__ long long range_start(int c, long long T, int C) { return (long long)c * T / C; }
+
+// Per-unit set-up, out of line (once per (sequence, kv head)).
+// Converter thread r: q[4h + i, r] times head i's Q' prescale.
+template <bool KCW, bool BF16>
+static __device__ __noinline__ float4 converter_unit_q(const uint16_t* qb, int r) {
+  float qmax[4], qsum[4];
+  unit_q_stats<4>(qb, false, qmax, qsum);
+  float qh[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    qh[i] = bf2f(qb[i * kHeadDim + r]) * (BF16 ? 1.0f : KCW ? pow2_head(qmax[i]) : pow2_prescale(qmax[i]));
+  return make_float4(qh[0], qh[1], qh[2], qh[3]);
+}
+// Softmax thread i: per-head score constants of the unit.  Channel-wise K:
+// add = the unit's part of the score multiplier, qi = q[4h + k, i];
+// token-wise K: S = s_l * (q . code) * mult + z_l * add.
+struct SegConsts {
+  float qi[4], mult[4], add[4];
+};
+template <bool KCW, bool BF16>
+static __device__ __noinline__ SegConsts softmax_unit_consts(const uint16_t* qb, int i, float sm_scale_log2) {
+  using C = DecodeCfg<4, BF16>;  // the code scale does not depend on the bit width
+  float qmax[4], qsum[4];
+  unit_q_stats<4>(qb, !KCW, qmax, qsum);
+  SegConsts c;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (KCW) {
+      c.qi[k] = bf2f(qb[k * kHeadDim + i]);
+      c.mult[k] = 0.f;
+      c.add[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_head_inv(qmax[k])) * sm_scale_log2;
+    } else {
+      c.qi[k] = 0.f;
+      c.mult[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_prescale_inv(qmax[k])) * sm_scale_log2;
+      c.add[k] = qsum[k] * sm_scale_log2;
+    }
+  }
+  return c;
+}
 
 // ================================================================= kernel
 template <int BITS, bool KCW, bool VCW, bool BF16>
@@ -651,12 +699,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
       if (t == 0 || it.j == 0) {  // new (sequence, kv head): its four query rows
         ++seg;
-        const uint16_t* qb = p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim;
-        float qmax[4], qsum[4];
-        unit_q_stats<4>(qb, false, qmax, qsum);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          qh[i] = bf2f(qb[i * kHeadDim + r]) * (BF16 ? 1.0f : KCW ? pow2_head(qmax[i]) : pow2_prescale(qmax[i]));
+        const float4 q4 = converter_unit_q<KCW, BF16>(p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim, r);
+        qh[0] = q4.x; qh[1] = q4.y; qh[2] = q4.z; qh[3] = q4.w;
       }
       // Q' operand: token-wise K uses q (written once per segment per slot);
       // channel-wise K folds this group's scales into q.
@@ -946,19 +990,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       }
       if (seg_first) {
         pb = it.b; ph = it.h; pfirst = ustart >= g0; pus = ustart; pue = uend;
-        const uint16_t* qb = p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim;
-        float qsum[4];
-        unit_q_stats<4>(qb, !KCW, qmax, qsum);
+        const SegConsts sc4 = softmax_unit_consts<KCW, BF16>(
+            p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim, i, p.sm_scale_log2);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (KCW) {  // add[] holds the per-segment part of the score multiplier
-            qi[k] = bf2f(qb[k * kHeadDim + i]);
-            add[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_head_inv(qmax[k])) * p.sm_scale_log2;
-          } else {  // token-wise K: S = s_l * (q . code) + z_l * sum(q), constant factors per segment
-            mult[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_prescale_inv(qmax[k])) * p.sm_scale_log2;
-            add[k] = qsum[k] * p.sm_scale_log2;
-          }
-        }
+        for (int k = 0; k < 4; ++k) { qi[k] = sc4.qi[k]; mult[k] = sc4.mult[k]; add[k] = sc4.add[k]; }
       }
       // this step: tile t and, if it belongs to the same segment, tile t + 1
       const int n = (t + 1 < ntiles && it.j + 1 < it.nblk) ? 2 : 1;

@@ -130,6 +130,13 @@ __device__ __forceinline__ uint32_t b_row_off(int p) {
   return BF16 ? (uint32_t)((p >> 3) * 256 + (p & 7) * 16) : (uint32_t)(p * 16);
 }
 
+// B-operand row factor matching Convert: 2-bit codes at odd positions e are
+// stored as 4 * code, so their Q' / P' rows are scaled by 1/4 (exact).
+template <int BITS, bool BF16>
+__device__ __forceinline__ float odd_quarter(int e) {
+  return (BITS == 2 && !BF16 && (e & 1)) ? 0.25f : 1.0f;
+}
+
 // ---------------------------------------------------------------- operands
 // 4 floats -> 4 E4M3 bytes (element i in byte i), round to nearest, saturate.
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
@@ -242,9 +249,13 @@ struct Convert {
       if (BITS == 4) {  // codes e = 0,2,4,6 then 1,3,5,7 as E4M3 0x0q
         o[0] = x & 0x0F0F0F0Fu;
         o[1] = (x >> 4) & 0x0F0F0F0Fu;
-      } else {  // word k holds codes e = k, k+4, k+8, k+12
-#pragma unroll
-        for (int k = 0; k < 4; ++k) o[k] = (x >> (2 * k)) & 0x03030303u;
+      } else {  // word k holds codes e = k, k+4, k+8, k+12; words 1 and 3 hold 4 * code
+        // (E4M3 byte b is b * 2^-9 exactly for b < 16, so the shift is left to
+        // the B operand: its rows for odd e carry a factor 1/4, see odd_quarter)
+        o[0] = x & 0x03030303u;
+        o[1] = x & 0x0C0C0C0Cu;
+        o[2] = (x >> 4) & 0x03030303u;
+        o[3] = (x >> 4) & 0x0C0C0C0Cu;
       }
     } else {  // exact BF16 integers: bits of (128 + q) minus 128
       const __nv_bfloat162 base = __floats2bfloat162_rn(128.0f, 128.0f);
@@ -340,6 +351,29 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(FULL, v, o);
   return v;
 }
+// Warp sums of eight per-lane values in 9 shuffles (a transposing butterfly):
+// on return lane l holds the sum of value (l >> 2) & 7.
+__device__ __forceinline__ float warp_sum8_transposed(const float (&a)[8]) {
+  const int l = lane_id();
+  const bool b4 = (l & 16) != 0, b3 = (l & 8) != 0, b2 = (l & 4) != 0;
+  float h[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float keep = b4 ? a[4 + j] : a[j], send = b4 ? a[j] : a[4 + j];
+    h[j] = keep + __shfl_xor_sync(FULL, send, 16);
+  }
+  float g[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float keep = b3 ? h[2 + j] : h[j], send = b3 ? h[j] : h[2 + j];
+    g[j] = keep + __shfl_xor_sync(FULL, send, 8);
+  }
+  float f = (b2 ? g[1] : g[0]) + __shfl_xor_sync(FULL, b2 ? g[0] : g[1], 4);
+  f += __shfl_xor_sync(FULL, f, 2);
+  f += __shfl_xor_sync(FULL, f, 1);
+  return f;
+}
+
 __device__ __forceinline__ float warp_maxf(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, o));
@@ -709,8 +743,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PA(5, c4)
       KVQ_PT(c3)
       if (KCW || (sl ? slot_seg1 : slot_seg0) != seg) {
-        float f = 1.0f;
-        if (KCW) f = BF16 ? h2f(ks[r]) : h2f(ks[r]) * pow2_group(f16_exp_field(max_f16_bits_128(ks)));
+        float f = odd_quarter<BITS, BF16>(r);
+        if (KCW) f *= BF16 ? h2f(ks[r]) : h2f(ks[r]) * pow2_group(f16_exp_field(max_f16_bits_128(ks)));
         const float4 v = make_float4(qh[0] * f, qh[1] * f, qh[2] * f, qh[3] * f);
         *reinterpret_cast<uint4*>(qop + sl * C::kBBytes + b_row_off<BF16>(qrow)) =
             BF16 ? split2_bf16(v) : (KCW ? split3_e4m3_via_f16(v) : split3_e4m3(v));
@@ -817,8 +851,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     // v merges value v over the four warps and the results are broadcast.
     // `used` (bit v = value v) selects the values published and broadcast;
     // callers pass compile-time masks.
-    auto round = [&](const float (&vals)[kNV], float (&res)[kNV], uint32_t used) -> bool {
+    auto round = [&](const float (&vals)[kNV], float (&res)[kNV], uint32_t used, bool cg_dist = false,
+                     float cg = 0.f) -> bool {
       float* red = sh.sw_red[grp_phase][sw];
+      if (cg_dist && (lane & 3) == 0) red[kCG + (lane >> 2)] = cg;
+      const uint32_t used_all = used;
+      if (cg_dist) used &= ~(0xffu << kCG);
       if (lane == 0) {
 #pragma unroll
         for (int v = 0; v < kNV; v += 2) {
@@ -835,7 +873,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const float r2 = sh.sw_red[use][2][v], r3 = sh.sw_red[use][3][v];
       const float mine = lane_max ? fmaxf(fmaxf(r0, r1), fmaxf(r2, r3)) : (r0 + r1) + (r2 + r3);
 #pragma unroll
-      for (int k = 0; k < kNV; ++k) res[k] = ((used >> k) & 1u) ? __shfl_sync(FULL, mine, k) : 0.f;
+      for (int k = 0; k < kNV; ++k) res[k] = ((used_all >> k) & 1u) ? __shfl_sync(FULL, mine, k) : 0.f;
       return true;
     };
 
@@ -1055,7 +1093,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           sc[4 * u + k] = valid ? v : -INFINITY;
           if (KCW) {  // the tile's offset q . z_g is still to come: per-tile maxima
             vals[kTM + 4 * u + k] = warp_max_redux(sc[4 * u + k]);
-            vals[kCG + 4 * u + k] = warp_sum(qi[k] * kz_t[u]);
+
           }
         }
       }
@@ -1072,8 +1110,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PA(16, s0)
       KVQ_PT(s2)
       float res[kNV];
+      float cgp = 0.f;
+      if (KCW) {
+        float za[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { za[k] = qi[k] * kz_t[0]; za[4 + k] = qi[k] * kz_t[1]; }
+        cgp = warp_sum8_transposed(za);
+      }
       constexpr uint32_t kUsed = (KCW ? 0xffffu : 0xfu) | (VCW ? (0xffu << kWS) : (1u << kVM));
-      if (!round(vals, res, kUsed)) { ok = false; break; }
+      if (!round(vals, res, kUsed, KCW, cgp)) { ok = false; break; }
       KVQ_PA(18, s2)
       if (sw == 0) { KVQ_TR(20, t) if (n > 1) KVQ_TR(20, t + 1) }
       KVQ_PT(s3)
@@ -1106,7 +1151,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           pv_scale_t[u] = pinv;
-          const float pmul = VCW ? pscale : vs_t[u] * pscale;
+          const float pmul = (VCW ? pscale : vs_t[u] * pscale) * odd_quarter<BITS, BF16>(i);
           const float4 pv = make_float4(pr[4 * u] * pmul, pr[4 * u + 1] * pmul, pr[4 * u + 2] * pmul, pr[4 * u + 3] * pmul);
           bytes[u] = BF16 ? split2_bf16(pv) : split3_e4m3_via_f16(pv);
         }

@@ -213,6 +213,26 @@ __device__ __forceinline__ uint32_t f16_exp_field(uint32_t h) {
 __device__ __forceinline__ float pow2_group(uint32_t e16) { return __uint_as_float((142u - e16) << 23); }      // 2^(-E_s)
 __device__ __forceinline__ float pow2_group_inv(uint32_t e16) { return __uint_as_float((112u + e16) << 23); }  // 2^(E_s)
 
+// P' prescale of one head: with x = (pair maximum - running maximum) in log2
+// units (<= 0) and e_v the exponent of the pair's largest V scale (0 for
+// channel-wise V), E = floor(x) + e_v bounds log2 of the head's largest
+// p * s; the scale 2^(6 - E) keeps max |P'| below 256 and is undone exactly
+// by 2^(E - 6).  E is clamped to [-120, 120] (-inf / NaN x included); the
+// four heads' E are kept as signed bytes of one word.
+__device__ __forceinline__ int p_exponent(float x, int e_v) {
+  const int fx = (x > -100.0f) ? __float2int_rd(x) : -100;
+  const int e = fx + e_v;
+  return e < -120 ? -120 : (e > 120 ? 120 : e);
+}
+__device__ __forceinline__ int p_exp_of(uint32_t packed, int k) { return (int)(packed << (24 - 8 * k)) >> 24; }
+// 2^(6 - E) and 2^(E - 6 + code_log2) for head k of a packed word.
+__device__ __forceinline__ float p_scale(uint32_t packed, int k) {
+  return __uint_as_float((uint32_t)(133 - p_exp_of(packed, k)) << 23);
+}
+__device__ __forceinline__ float p_inverse(uint32_t packed, int k, int code_log2) {
+  return __uint_as_float((uint32_t)(121 + code_log2 + p_exp_of(packed, k)) << 23);
+}
+
 // 2^x (hardware approximation, flush-to-zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -834,13 +854,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     float m[4], lp[4], zp[4], O[4];  // running max (log2 units), partial sum p, partial sum p*z, output
     // deferred epilogue inputs of the previous step (up to two tiles)
     int pend = -1, pend_n = 0;
-    float a_prev[4], ws_prev[8], pinv_prev[2], sv_prev[2], zv_prev[2];
+    float a_prev[4], ws_prev[8], sv_prev[2], zv_prev[2];
+    uint32_t pexp_prev = 0u;  // P' prescale exponents E of the previous step, one signed byte per head
+    constexpr int kCodeLog2 = BF16 ? 0 : 9;  // log2 of the code scale
     float qi[4], qmax[4], mult[4], add[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) { qi[k] = 0.f; qmax[k] = 0.f; mult[k] = 0.f; add[k] = 0.f; a_prev[k] = 0.f; }
 #pragma unroll
     for (int k = 0; k < 8; ++k) ws_prev[k] = 0.f;
-    pinv_prev[0] = pinv_prev[1] = sv_prev[0] = sv_prev[1] = zv_prev[0] = zv_prev[1] = 0.f;
+    sv_prev[0] = sv_prev[1] = zv_prev[0] = zv_prev[1] = 0.f;
     auto reset = [&]() {
 #pragma unroll
       for (int k = 0; k < 4; ++k) { m[k] = -INFINITY; lp[k] = 0.f; zp[k] = 0.f; O[k] = 0.f; }
@@ -908,7 +930,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         for (int u = 0; u < 2; ++u) {
           o[u] = __uint_as_float(acc[u][k]) + __uint_as_float(acc[u][4 + k]);
           if (!BF16) o[u] += __uint_as_float(acc[u][8 + k]);
-          o[u] *= pinv_prev[u];
+          o[u] *= p_inverse(pexp_prev, k, kCodeLog2);
         }
         if (pend_n < 2) o[1] = 0.f;
         const float o_add = VCW ? fmaf(sv_prev[0], o[0], zv_prev[0] * ts[k]) + fmaf(sv_prev[1], o[1], zv_prev[1] * ts[4 + k])
@@ -1039,7 +1061,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
       KVQ_PT(s0)
       if (sw == 0) { KVQ_TR(19, t) if (n > 1) KVQ_TR(19, t + 1) }
-      float sc[8], vs_t[2], vz_t[2], pv_scale_t[2];
+      float sc[8], vs_t[2], vz_t[2];
+      uint32_t pexp = 0u;
       float vals[kNV];
 #pragma unroll
       for (int k = 0; k < kNV; ++k) vals[k] = 0.f;
@@ -1122,14 +1145,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PA(18, s2)
       if (sw == 0) { KVQ_TR(20, t) if (n > 1) KVQ_TR(20, t + 1) }
       KVQ_PT(s3)
-      // one running-max update for the pair
+      // one running-max update for the pair, and each head's P' prescale
+      // exponent from the pair's own largest p (2^(mt - mn)) times the largest
+      // V scale: far from the running max the p values would otherwise sit at
+      // the bottom of the E4M3 range
       float pr[8], alpha[4];
+      const int e_v = VCW ? 0 : (int)((__float_as_uint(res[kVM]) >> 23) & 0xffu) - 127;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float cg0 = KCW ? res[kCG + k] * p.sm_scale_log2 : 0.f;
         const float cg1 = KCW ? res[kCG + 4 + k] * p.sm_scale_log2 : 0.f;
         const float mt = KCW ? fmaxf(res[kTM + k] + cg0, res[kTM + 4 + k] + cg1) : res[kTM + k];
         const float mn = fmaxf(m[k], mt);
+        pexp |= ((uint32_t)(BF16 ? 6 : p_exponent(mt - mn, e_v)) & 0xffu) << (8 * k);
         alpha[k] = ex2(m[k] - mn);
         m[k] = mn;
         pr[k] = ex2(sc[k] + cg0 - mn);
@@ -1145,14 +1173,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         break;
       }
       {
-        const float pscale = VCW ? 256.0f : (BF16 ? 1.0f : pow2_prescale(res[kVM]));
-        const float pinv = VCW ? (1.0f / 256.0f) : (BF16 ? 1.0f : pow2_prescale_inv(res[kVM]));
+        float psc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) psc[k] = BF16 ? 1.0f : p_scale(pexp, k);
         uint4 bytes[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          pv_scale_t[u] = pinv;
-          const float pmul = (VCW ? pscale : vs_t[u] * pscale) * odd_quarter<BITS, BF16>(i);
-          const float4 pv = make_float4(pr[4 * u] * pmul, pr[4 * u + 1] * pmul, pr[4 * u + 2] * pmul, pr[4 * u + 3] * pmul);
+          const float f = (VCW ? 1.0f : vs_t[u]) * odd_quarter<BITS, BF16>(i);
+          const float4 pv = make_float4(pr[4 * u] * (f * psc[0]), pr[4 * u + 1] * (f * psc[1]),
+                                        pr[4 * u + 2] * (f * psc[2]), pr[4 * u + 3] * (f * psc[3]));
           bytes[u] = BF16 ? split2_bf16(pv) : split3_e4m3_via_f16(pv);
         }
         *reinterpret_cast<uint4*>(pop + q0 * C::kBBytes + b_row_off<BF16>(prow)) = bytes[0];
@@ -1180,9 +1209,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       pend_n = n;
 #pragma unroll
       for (int k = 0; k < 4; ++k) a_prev[k] = alpha[k];
+      pexp_prev = pexp;  // per head, both tiles of the pair
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        pinv_prev[u] = C::kCodeInv * pv_scale_t[u];
         sv_prev[u] = vs_t[u];  // channel-wise V: lane i = channel i
         zv_prev[u] = vz_t[u];
         // channel-wise V: this group's per-warp sum(p), in exact fixed point

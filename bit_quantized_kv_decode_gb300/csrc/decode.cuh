@@ -767,7 +767,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         if (KCW) f *= BF16 ? h2f(ks[r]) : h2f(ks[r]) * pow2_group(f16_exp_field(max_f16_bits_128(ks)));
         const float4 v = make_float4(qh[0] * f, qh[1] * f, qh[2] * f, qh[3] * f);
         *reinterpret_cast<uint4*>(qop + sl * C::kBBytes + b_row_off<BF16>(qrow)) =
-            BF16 ? split2_bf16(v) : (KCW ? split3_e4m3_via_f16(v) : split3_e4m3(v));
+            BF16 ? split2_bf16(v) : split3_e4m3(v);
         fence_proxy_async_smem();
         if (sl) slot_seg1 = seg; else slot_seg0 = seg;
       }

@@ -22,7 +22,7 @@ GROUP_Q = 4
 
 __all__ = ["CacheDesc", "AttnDesc", "KvqError", "TOKENWISE", "CHANNELWISE", "OPERANDS_FP8", "OPERANDS_BF16",
            "DEV_BAD_SEQ_LEN", "DEV_BAD_PAGE", "DEV_NONFINITE", "DEV_TIMEOUT", "FLAG_TEST_STALL", "cache_desc",
-           "attn_desc", "cache_bytes", "block_bytes", "alloc_cache", "pack", "dequant", "workspace_size",
+           "attn_desc", "cache_bytes", "block_bytes", "alloc_cache", "pack", "append", "dequant", "workspace_size",
            "decode_attn", "decode_attn_static", "merge", "library"]
 
 
@@ -112,6 +112,39 @@ def pack(desc: CacheDesc, which: int, x: torch.Tensor, seq_lens: Optional[torch.
                             _p(scale), _p(zero), _p(dev_status), _stream())
     _lib.check(st, "kvq_pack")
     return codes, scale, zero
+
+
+def append(desc: CacheDesc, which: int, x_new: torch.Tensor, seq_lens: torch.Tensor, cache, window: torch.Tensor,
+           page_table: Optional[torch.Tensor] = None, max_blocks: Optional[int] = None,
+           dev_status: Optional[torch.Tensor] = None):
+    """Append fp32 x_new [B, Hkv, 128] at positions seq_lens (tokens already
+    cached) to a packed K (which=0) or V (which=1) cache, through the caller's
+    fp32 window [B, Hkv, 128, 128] of each current block; returns the cache.
+    The caller advances seq_lens afterwards."""
+    _need(x_new, "x_new", torch.float32)
+    _need(window, "window", torch.float32)
+    _need(seq_lens, "seq_lens", torch.int32)
+    if x_new.dim() != 3 or x_new.shape[1] != desc.num_kv_heads or x_new.shape[2] != HEAD_DIM:
+        raise ValueError("x_new must be fp32 [batch, num_kv_heads, 128]")
+    B = x_new.shape[0]
+    if tuple(window.shape) != (B, desc.num_kv_heads, BLOCK_TOKENS, HEAD_DIM):
+        raise ValueError("window must be fp32 [batch, num_kv_heads, 128, 128]")
+    if seq_lens.numel() != B:
+        raise ValueError("seq_lens must hold one int32 per sequence")
+    if page_table is not None:
+        _need(page_table, "page_table", torch.int32)
+        mb = page_table.shape[1]
+    elif max_blocks is not None:
+        mb = int(max_blocks)
+    else:
+        raise ValueError("append needs page_table or max_blocks")
+    codes, scale, zero = cache
+    if dev_status is not None:
+        _need(dev_status, "dev_status", (torch.int32, torch.uint32), 1)
+    st = library().kvq_append(ctypes.byref(desc), which, _p(x_new), B, _p(seq_lens), _p(page_table), mb,
+                              _p(window), _p(codes), _p(scale), _p(zero), _p(dev_status), _stream())
+    _lib.check(st, "kvq_append")
+    return cache
 
 
 def dequant(desc: CacheDesc, which: int, cache, batch: int, max_seq_len: int,

@@ -22,7 +22,7 @@ OPERANDS_BF16 = 1
 FLAG_TEST_STALL = 0x1
 
 # Every symbol include/kvq.h declares.
-EXPORTS = ("kvq_status_string", "kvq_version", "kvq_cache_bytes", "kvq_pack", "kvq_dequant",
+EXPORTS = ("kvq_status_string", "kvq_version", "kvq_cache_bytes", "kvq_pack", "kvq_append", "kvq_dequant",
            "kvq_decode_workspace_size", "kvq_decode_attn", "kvq_decode_attn_static", "kvq_merge")
 
 
@@ -69,6 +69,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.kvq_cache_bytes.argtypes = [ctypes.POINTER(CacheDesc), ctypes.POINTER(SZ), ctypes.POINTER(SZ)]
     lib.kvq_pack.restype = I32
     lib.kvq_pack.argtypes = [ctypes.POINTER(CacheDesc), I32, P, I32, I32, P, P, I32, P, P, P, P, P]
+    lib.kvq_append.restype = I32
+    lib.kvq_append.argtypes = [ctypes.POINTER(CacheDesc), I32, P, I32, P, P, I32, P, P, P, P, P, P]
     lib.kvq_dequant.restype = I32
     lib.kvq_dequant.argtypes = [ctypes.POINTER(CacheDesc), I32, P, P, P, I32, I32, P, P, I32, P, P, P]
     lib.kvq_decode_workspace_size.restype = I32

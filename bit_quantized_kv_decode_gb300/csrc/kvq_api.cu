@@ -144,6 +144,31 @@ KVQ_API kvq_status kvq_pack(const kvq_cache_desc* cache, int32_t which, const fl
   return launch_pack(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+KVQ_API kvq_status kvq_append(const kvq_cache_desc* cache, int32_t which, const float* x_new, int32_t batch,
+                              const int32_t* seq_lens, const int32_t* page_table, int32_t max_blocks,
+                              float* window, uint8_t* codes, uint16_t* scale, uint16_t* zero,
+                              uint32_t* dev_status, void* stream) {
+  kvq_status s = check_cache(cache);
+  if (s != KVQ_OK) return s;
+  if (which != 0 && which != 1) return KVQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > 65535 || max_blocks < 1 || cache->num_kv_heads > 65535) return KVQ_ERR_INVALID_ARG;
+  if (page_table == nullptr && (long long)batch * max_blocks > cache->num_pages) return KVQ_ERR_INVALID_ARG;
+  if (!x_new || !window || !seq_lens || !codes || !scale || !zero || !aligned16(x_new) || !aligned16(window) ||
+      !aligned16(codes) || !aligned16(scale) || !aligned16(zero))
+    return KVQ_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(page_table) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  s = check_device(nullptr);
+  if (s != KVQ_OK) return s;
+  PackParams p{};
+  p.x = x_new; p.window = window; p.seq_lens = seq_lens; p.page_table = page_table;
+  p.codes = codes; p.scale = scale; p.zero = zero; p.dev_status = dev_status;
+  p.bits = cache->bits; p.k_scheme = cache->k_scheme; p.v_scheme = cache->v_scheme; p.which = which;
+  p.num_kv_heads = cache->num_kv_heads; p.num_pages = cache->num_pages;
+  p.batch = batch; p.max_seq_len = max_blocks * kBlockTokens; p.max_blocks = max_blocks; p.max_blocks_needed = 1;
+  return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 KVQ_API kvq_status kvq_dequant(const kvq_cache_desc* cache, int32_t which, const uint8_t* codes,
                                const uint16_t* scale, const uint16_t* zero, int32_t batch, int32_t max_seq_len,
                                const int32_t* seq_lens, const int32_t* page_table, int32_t max_blocks,

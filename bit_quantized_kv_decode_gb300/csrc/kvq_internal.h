@@ -19,7 +19,8 @@ __device__ __forceinline__ void report(uint32_t* dev_status, uint32_t bits) {
 }
 
 struct PackParams {
-  const float* x;
+  const float* x;    // pack: [batch][kv heads][max_seq_len][128]; append: the new tokens [batch][kv heads][128]
+  float* window;     // append only: [batch][kv heads][128][128] raw rows of each current block
   const int32_t* seq_lens;
   const int32_t* page_table;
   uint8_t* codes;
@@ -71,6 +72,7 @@ struct DecodeParams {
 
 size_t pack_smem_bytes();
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
+cudaError_t launch_append(const PackParams& p, cudaStream_t stream);
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int rows, int splits, int head_dim, float* out,
                          float* lse, cudaStream_t stream);

@@ -81,21 +81,17 @@ __device__ __forceinline__ bool block_geometry(const PackParams& p, int b, int j
   return true;
 }
 
-__global__ void __launch_bounds__(kThreads) pack_kernel(PackParams p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+// Quantize and pack one block of KV head h: the nv valid token rows at src
+// (fp32, 128 channels each) into page `page`.
+__device__ void pack_block(const PackParams& p, const float* src, int page, int nv, int h, unsigned char* smem_raw) {
   float* xs = reinterpret_cast<float*>(smem_raw);                                    // [128][kPitch]
   uint8_t* cs = reinterpret_cast<uint8_t*>(xs + kBlockTokens * kPitch);             // [128 tok][128 ch]
   uint16_t* s_out = reinterpret_cast<uint16_t*>(cs + kBlockTokens * kHeadDim);     // [128]
   uint16_t* z_out = s_out + kBlockTokens;                                          // [128]
-
-  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  int page, nv;
-  if (!block_geometry(p, b, j, &page, &nv)) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int qmax = (1 << p.bits) - 1;
 
   // Stage the valid tokens of the tile (rows t < nv).
-  const float* src = p.x + (((size_t)b * p.num_kv_heads + h) * p.max_seq_len + (size_t)j * kBlockTokens) * kHeadDim;
   for (int i = tid; i < nv * (kHeadDim / 4); i += kThreads) {
     int t = i / (kHeadDim / 4), c4 = (i % (kHeadDim / 4)) * 4;
     float4 v = *reinterpret_cast<const float4*>(src + (size_t)t * kHeadDim + c4);
@@ -178,6 +174,41 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(PackParams p) {
   }
 }
 
+__global__ void __launch_bounds__(kThreads) pack_kernel(PackParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  int page, nv;
+  if (!block_geometry(p, b, j, &page, &nv)) return;
+  const float* src = p.x + (((size_t)b * p.num_kv_heads + h) * p.max_seq_len + (size_t)j * kBlockTokens) * kHeadDim;
+  pack_block(p, src, page, nv, h, smem_raw);
+}
+
+// Append one token per sequence: the token at position len = seq_lens[b]
+// goes into row len % 128 of the caller's window of the current block, and
+// the block is quantized and packed again from the window's len % 128 + 1
+// valid rows (the same rule as a partial last block of kvq_pack).  One CTA
+// per (KV head h, sequence b).
+__global__ void __launch_bounds__(kThreads) append_kernel(PackParams p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int len = p.seq_lens[b];
+  if (len < 0 || len >= p.max_blocks * kBlockTokens) {
+    if (h == 0 && threadIdx.x == 0) report(p.dev_status, KVQ_DEV_BAD_SEQ_LEN);
+    return;
+  }
+  const int j = len / kBlockTokens, r = len % kBlockTokens;
+  const int page = p.page_table ? p.page_table[(size_t)b * p.max_blocks + j] : b * p.max_blocks + j;
+  if (page < 0 || page >= p.num_pages) {
+    if (h == 0 && threadIdx.x == 0) report(p.dev_status, KVQ_DEV_BAD_PAGE);
+    return;
+  }
+  float* win = p.window + ((size_t)b * p.num_kv_heads + h) * kBlockTokens * kHeadDim;
+  const float* xn = p.x + ((size_t)b * p.num_kv_heads + h) * kHeadDim;
+  if (threadIdx.x < kHeadDim) win[(size_t)r * kHeadDim + threadIdx.x] = xn[threadIdx.x];
+  __syncthreads();  // the new row is visible to the whole CTA
+  pack_block(p, win, page, r + 1, h, smem_raw);
+}
+
 __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantParams p) {
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
@@ -233,6 +264,15 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   dim3 grid(p.max_blocks_needed, p.num_kv_heads, p.batch);
   pack_kernel<<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const PackParams& p, cudaStream_t stream) {
+  const size_t smem = pack_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.num_kv_heads, p.batch);
+  append_kernel<<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

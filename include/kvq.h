@@ -143,6 +143,35 @@ KVQ_API kvq_status kvq_pack(const kvq_cache_desc* cache, int32_t which, const fl
                             uint32_t* dev_status, void* stream);
 
 /*
+ * Append one token per sequence to a packed K (which = 0) or V (which = 1)
+ * cache, for a decode loop that grows the cache step by step.  The new token
+ * of sequence b sits at position seq_lens[b] (the tokens already cached); it
+ * is stored in row seq_lens[b] % 128 of the caller's window of that
+ * sequence's current 128-token block, and the block is quantized and packed
+ * again from the window's valid rows (seq_lens[b] % 128 + 1 of them), so the
+ * cache equals what kvq_pack makes of the whole sequence: a channel-wise
+ * group spans the block's valid tokens, as for a partial last block.  The
+ * caller then advances seq_lens[b] by one; when a block fills, the next
+ * block's rows overwrite the window from row 0 (no reset needed).  A cache
+ * that starts from kvq_pack of a prefix needs the prefix's partial last block
+ * copied into the window first.
+ *   x_new      fp32 [batch][num_kv_heads][128], 16-byte aligned
+ *   seq_lens   int32 [batch], each in [0, max_blocks * 128)
+ *   page_table int32 [batch][max_blocks] or NULL (contiguous; then
+ *              batch * max_blocks <= num_pages)
+ *   window     fp32 [batch][num_kv_heads][128][128], caller-owned (one for
+ *              K, one for V), 16-byte aligned
+ *   codes, scale, zero: the cache arrays (only the current block's page is
+ *              written)
+ * Device errors as kvq_pack (KVQ_DEV_BAD_SEQ_LEN when seq_lens[b] is out of
+ * range: that sequence is skipped).
+ */
+KVQ_API kvq_status kvq_append(const kvq_cache_desc* cache, int32_t which, const float* x_new, int32_t batch,
+                              const int32_t* seq_lens, const int32_t* page_table, int32_t max_blocks,
+                              float* window, uint8_t* codes, uint16_t* scale, uint16_t* zero,
+                              uint32_t* dev_status, void* stream);
+
+/*
  * Read a packed K or V cache back as fp32 x_hat = s * code + z (exact, one
  * rounding).  x_hat: fp32 [batch][num_kv_heads][max_seq_len][128]; positions
  * at or past seq_lens[b] are written as 0.  Other arguments as kvq_pack.

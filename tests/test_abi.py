@@ -97,6 +97,12 @@ def test_validation_precedes_device(lib):
     assert lib.kvq_decode_attn(ctypes.byref(d), *args) == 1
     # merge: bad head_dim
     assert lib.kvq_merge(fake, fake, 4, 2, 130, fake, fake, None) == 1
+    # append: which out of range, missing window, misaligned x_new, contiguous cache too small
+    app = [fake, 1, fake, fake, 2, fake, fake, fake, fake, None, None]
+    assert lib.kvq_append(ctypes.byref(c), 2, *app) == 1
+    assert lib.kvq_append(ctypes.byref(c), 0, fake, 1, fake, fake, 2, None, fake, fake, fake, None, None) == 1
+    assert lib.kvq_append(ctypes.byref(c), 0, P(0x10004), 1, fake, fake, 2, fake, fake, fake, fake, None, None) == 1
+    assert lib.kvq_append(ctypes.byref(small), 0, fake, 2, fake, None, 2, fake, fake, fake, fake, None, None) == 1
 
 
 def test_no_device_reports_device_error(lib):

@@ -159,7 +159,7 @@ def time_steps(fn, steps: int, warmup: int, stream):
     return sum(per) / len(per), per
 
 
-def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=True):
+def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=True, mode=0):
     import bit_quantized_kv_decode_gb300 as kvq
     c = build_cache(w, seed, dev, k_scheme, v_scheme)
     desc = c["desc"]
@@ -171,7 +171,7 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
     stream = torch.cuda.current_stream()
 
     def step():
-        kvq.decode_attn(desc, c["q"], c["k"], c["v"], c["lens"], c["pt"], c["max_blocks"], out=out, lse=lse,
+        kvq.decode_attn(desc, c["q"], c["k"], c["v"], c["lens"], c["pt"], c["max_blocks"], mode=mode, out=out, lse=lse,
                         workspace=ws, dev_status=status)
 
     t_wall0 = time.time()
@@ -194,7 +194,7 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
         def e2e_step():
             q_d.copy_(q_h, non_blocking=True)
             lens_d.copy_(lens_h, non_blocking=True)
-            kvq.decode_attn(desc, q_d, c["k"], c["v"], lens_d, c["pt"], c["max_blocks"], out=out, lse=lse,
+            kvq.decode_attn(desc, q_d, c["k"], c["v"], lens_d, c["pt"], c["max_blocks"], mode=mode, out=out, lse=lse,
                             workspace=ws, dev_status=status)
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
@@ -385,6 +385,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiler captures)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--operands", choices=("fp8", "bf16"), default="fp8",
+                    help="tensor-core operand mode: fp8 (default) or the bf16 mode")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     w = synth.WORKLOADS[args.workload]
@@ -402,7 +404,8 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world)
-    res = measure_kvq(w, args.seed + rank, args.steps, args.warmup, dev, e2e=not args.no_e2e)
+    mode = 1 if args.operands == "bf16" else 0
+    res = measure_kvq(w, args.seed + rank, args.steps, args.warmup, dev, e2e=not args.no_e2e, mode=mode)
     barrier(world)
     ms = max_over_ranks(res["ms"], world, dev)
     e2e_ms = max_over_ranks(res["e2e_ms"], world, dev) if "e2e_ms" in res else float("nan")
@@ -410,7 +413,8 @@ def main():
     if not args.no_extra and w.name == DEFAULT_WORKLOAD and args.batch is None:
         w2 = synth.WORKLOADS["b128_l32k_int2"]
         for ks, vs in ((1, 0), (0, 0), (0, 1), (1, 1)):
-            r2 = measure_kvq(w2, args.seed + rank, max(20, args.steps // 4), args.warmup, dev, ks, vs, e2e=False)
+            r2 = measure_kvq(w2, args.seed + rank, max(20, args.steps // 4), args.warmup, dev, ks, vs, e2e=False,
+                             mode=mode)
             ms2 = max_over_ranks(r2["ms"], world, dev)
             extra.append({"workload": w2.name, "k_scheme": SCHEME_NAMES[ks], "v_scheme": SCHEME_NAMES[vs],
                           "ms_per_step": ms2, "GB/s": r2["bytes"] / (ms2 / 1e3) / 1e9,
@@ -429,11 +433,14 @@ def main():
         "metric": "effective KV-access HBM GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "latency_us": ms * 1e3,
         "pct_of_peak": 100.0 * achieved / peak, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp8 (e4m3 tensor-core operands, fp32 accumulate)", "data": "synthetic",
-        "config": dict(config_of(w), l2="each step reads %.2f GB > 129 MB L2; no flush needed" % (res["bytes"] / 1e9)),
+        "vs_baseline": None, "data": "synthetic",
+        "dtype": ("bf16 (tensor-core operands, fp32 accumulate)" if mode else
+                  "fp8 (e4m3 tensor-core operands, fp32 accumulate)"),
+        "config": dict(config_of(w), l2="each step reads %.2f GB > 129 MB L2; no flush needed" % (res["bytes"] / 1e9),
+                       **({"operands": "bf16 (exact BF16 codes, 2-part BF16 Q'/P')"} if mode else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs", "kernel": "kvq::decode_kernel",
-                     "traffic": profile_traffic(w.name),
+                     "traffic": None if mode else profile_traffic(w.name),
                      "algorithmic_bytes_per_launch": res["bytes"],
                      "duration_source": "CUDA events around each kvq_decode_attn call (counter memset + kernel)"},
         "e2e": ({"value": total_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,

@@ -224,7 +224,13 @@ __device__ __forceinline__ int p_exponent(float x, int e_v) {
   const int e = fx + e_v;
   return e < -120 ? -120 : (e > 120 ? 120 : e);
 }
-__device__ __forceinline__ int p_exp_of(uint32_t packed, int k) { return (int)(packed << (24 - 8 * k)) >> 24; }
+// Signed byte k of a packed word, sign-extended (one byte permute: selector
+// nibbles k for byte 0 and 8 + k, "replicate the sign of byte k", above it).
+__device__ __forceinline__ int p_exp_of(uint32_t packed, int k) {
+  int r;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(r) : "r"(packed), "r"(k | ((8 | k) << 4) | ((8 | k) << 8) | ((8 | k) << 12)));
+  return r;
+}
 // 2^(6 - E) and 2^(E - 6 + code_log2) for head k of a packed word.
 __device__ __forceinline__ float p_scale(uint32_t packed, int k) {
   return __uint_as_float((uint32_t)(133 - p_exp_of(packed, k)) << 23);
@@ -260,22 +266,27 @@ __device__ __forceinline__ uint4 split3_e4m3_via_f16(float4 v) {
   return make_uint4(w[0], w[1], w[2], 0u);
 }
 
-// Converted code words of one packed 32-bit word.
+// Converted code words of one packed 32-bit word.  `mul` = 2^28 and
+// `m1` = 2^32 - 1 arrive as run-time values: x >> 4 is taken as the high
+// word of x * 2^28 and x - y as x + y * m1, integer multiply-adds that issue
+// on the FMA pipe, which the converter warps leave mostly idle, while the
+// masks stay on the ALU pipe.
 template <int BITS, bool BF16>
 struct Convert {
   static constexpr int kOut = BF16 ? (BITS == 4 ? 4 : 8) : (BITS == 4 ? 2 : 4);
-  __device__ __forceinline__ static void run(uint32_t x, uint32_t* o) {
+  __device__ __forceinline__ static void run(uint32_t x, uint32_t* o, uint32_t mul, uint32_t m1) {
     if (!BF16) {
       if (BITS == 4) {  // codes e = 0,2,4,6 then 1,3,5,7 as E4M3 0x0q
         o[0] = x & 0x0F0F0F0Fu;
-        o[1] = (x >> 4) & 0x0F0F0F0Fu;
+        o[1] = __umulhi(x + o[0] * m1, mul);  // high nibbles (low ones cleared), shifted down
       } else {  // word k holds codes e = k, k+4, k+8, k+12; words 1 and 3 hold 4 * code
         // (E4M3 byte b is b * 2^-9 exactly for b < 16, so the shift is left to
         // the B operand: its rows for odd e carry a factor 1/4, see odd_quarter)
+        const uint32_t y = __umulhi(x, mul);  // x >> 4
         o[0] = x & 0x03030303u;
         o[1] = x & 0x0C0C0C0Cu;
-        o[2] = (x >> 4) & 0x03030303u;
-        o[3] = (x >> 4) & 0x0C0C0C0Cu;
+        o[2] = y & 0x03030303u;
+        o[3] = y & 0x0C0C0C0Cu;
       }
     } else {  // exact BF16 integers: bits of (128 + q) minus 128
       const __nv_bfloat162 base = __floats2bfloat162_rn(128.0f, 128.0f);
@@ -402,13 +413,12 @@ __device__ __forceinline__ float warp_maxf(float v) {
 
 __device__ __forceinline__ float h2f(uint16_t bits) { return __half2float(__ushort_as_half(bits)); }
 
-// Order-preserving integer key of a float, so that maxima can use redux.sync.
-__device__ __forceinline__ int fkey(float f) {
-  int b = __float_as_int(f);
-  return b ^ ((b >> 31) & 0x7fffffff);
+// Warp maximum of a float in one instruction (NaN inputs are ignored).
+__device__ __forceinline__ float warp_max_redux(float f) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(f));
+  return r;
 }
-__device__ __forceinline__ float unkey(int k) { return __int_as_float(k ^ ((k >> 31) & 0x7fffffff)); }
-__device__ __forceinline__ float warp_max_redux(float f) { return unkey(__reduce_max_sync(FULL, fkey(f))); }
 
 // Largest of 128 non-negative fp16 values in shared memory; every warp that
 // calls it gets the same value without talking to the other warps.
@@ -735,7 +745,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           uint4 v = *reinterpret_cast<const uint4*>(blk + ((size_t)(ps2 * kPerPass + c) * kBlockTokens + r) * 16);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) Convert<BITS, BF16>::run(w[i], &o[(4 * c + i) * Convert<BITS, BF16>::kOut]);
+          for (int i = 0; i < 4; ++i)
+            Convert<BITS, BF16>::run(w[i], &o[(4 * c + i) * Convert<BITS, BF16>::kOut], p.nibble_mul, p.minus_one);
         }
         tmem_st_32x32b_x32(col + 32 * ps2, o);
       }

@@ -249,6 +249,8 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
   const float sm_scale = desc->sm_scale > 0.0f ? desc->sm_scale : 1.0f / std::sqrt((float)kHeadDim);
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.flags = desc->flags;
+  p.nibble_mul = 1u << 28;
+  p.minus_one = 0xffffffffu;
   p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
 #ifdef KVQ_PROFILE
   p.prof = g_prof_counters;

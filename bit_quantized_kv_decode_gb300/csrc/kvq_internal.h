@@ -67,6 +67,11 @@ struct DecodeParams {
   float sm_scale_log2;  // sm_scale * log2(e)
   uint32_t flags;
   uint64_t wait_limit_ns;
+  // 2^28 and 2^32 - 1, passed at run time so that the compiler keeps the
+  // code unpacking's shift and subtraction as integer multiply-adds (the
+  // FMA pipe) instead of turning them back into shifts and logic ops (the
+  // ALU pipe, the busier of the two in the converter warps)
+  uint32_t nibble_mul, minus_one;
   unsigned long long* prof;  // cycle counters [grid][32] in profiling builds, else null
 };
 

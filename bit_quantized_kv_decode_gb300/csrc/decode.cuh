@@ -362,6 +362,21 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return warp_wait_slow(bar, parity, abort_flag, limit_ns);
 }
 
+// Two or four phases: one overlapped probe of all of them, then (rarely) the
+// one-by-one slow path.
+__device__ __forceinline__ bool warp_wait2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
+                                           volatile int* abort_flag, uint64_t limit_ns) {
+  if (__all_sync(FULL, mbar_try_wait2(b0, p0, b1, p1))) return true;
+  return warp_wait_slow(b0, p0, abort_flag, limit_ns) && warp_wait_slow(b1, p1, abort_flag, limit_ns);
+}
+__device__ __forceinline__ bool warp_wait4(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, uint64_t* b2,
+                                           uint32_t p2, uint64_t* b3, uint32_t p3, volatile int* abort_flag,
+                                           uint64_t limit_ns) {
+  if (__all_sync(FULL, mbar_try_wait4(b0, p0, b1, p1, b2, p2, b3, p3))) return true;
+  return warp_wait_slow(b0, p0, abort_flag, limit_ns) && warp_wait_slow(b1, p1, abort_flag, limit_ns) &&
+         warp_wait_slow(b2, p2, abort_flag, limit_ns) && warp_wait_slow(b3, p3, abort_flag, limit_ns);
+}
+
 __device__ __forceinline__ void set_abort(volatile int* abort_flag, uint32_t* dev_status) {
   *abort_flag = 1;
   report(dev_status, KVQ_DEV_TIMEOUT);
@@ -424,8 +439,8 @@ __device__ __forceinline__ float warp_max_redux(float f) {
 // calls it gets the same value without talking to the other warps.
 __device__ __forceinline__ uint32_t max_f16_bits_128(const uint16_t* v) {
   uint2 w = *reinterpret_cast<const uint2*>(v + 4 * lane_id());
-  uint32_t m = max(max(w.x & 0xffffu, w.x >> 16), max(w.y & 0xffffu, w.y >> 16));
-  return __reduce_max_sync(FULL, m);
+  const uint32_t m = __vmaxu2(w.x, w.y);  // two 16-bit maxima at once
+  return __reduce_max_sync(FULL, max(m & 0xffffu, m >> 16));
 }
 __device__ __forceinline__ float max_f16_128(const uint16_t* v) { return h2f((uint16_t)max_f16_bits_128(v)); }
 
@@ -665,8 +680,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         if (np < nq) {
           const int a = np % C::kNAV, sl = np % C::kSlots;
           const uint32_t pa = (uint32_t)(np / C::kNAV) & 1u, ps4 = (uint32_t)(np / C::kSlots) & 1u;
-          if (mbar_test(&sh.av_full[a], pa) && mbar_test(&sh.p_full[sl], ps4) &&
-              mbar_test(&sh.o_empty[sl], ps4 ^ 1u)) {
+          if (mbar_test3(&sh.av_full[a], pa, &sh.p_full[sl], ps4, &sh.o_empty[sl], ps4 ^ 1u)) {
             tc_fence_after();
             const uint32_t b0 = smem_u32(pop + sl * C::kBBytes);
 #pragma unroll
@@ -687,8 +701,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           const int a = nq % C::kNAK, sl = nq % C::kSlots, q2 = nq & 1;
           const uint32_t pa = (uint32_t)(nq / C::kNAK) & 1u, ps4 = (uint32_t)(nq / C::kSlots) & 1u,
                          p2 = (uint32_t)(nq >> 1) & 1u;
-          if (mbar_test(&sh.ak_full[a], pa) && mbar_test(&sh.q_full[q2], p2) &&
-              mbar_test(&sh.s_empty[sl], ps4 ^ 1u)) {
+          if (mbar_test3(&sh.ak_full[a], pa, &sh.q_full[q2], p2, &sh.s_empty[sl], ps4 ^ 1u)) {
             tc_fence_after();
             const uint32_t b0 = smem_u32(qop + q2 * C::kBBytes);
 #pragma unroll
@@ -758,7 +771,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNAK) & 1u,
                      p2 = (uint32_t)(t >> 1) & 1u;
       KVQ_PT(c0)
-      if (!warp_wait(&sh.stg_full[s], ps, abort_flag, limit)) return false;
+      if (!warp_wait2(&sh.stg_full[s], ps, &sh.q_empty[sl], p2 ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(1, c0)
       const unsigned char* st = stages + (size_t)s * C::kStageBytes;
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
@@ -770,7 +783,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       // Q' operand: token-wise K uses q (written once per segment per slot);
       // channel-wise K folds this group's scales into q.
       KVQ_PT(c4)
-      if (!warp_wait(&sh.q_empty[sl], p2 ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(5, c4)
       KVQ_PT(c3)
       if (KCW || (sl ? slot_seg1 : slot_seg0) != seg) {
@@ -917,8 +929,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const int tA = pend, tB = pend_n > 1 ? pend + 1 : pend;
       const int oA = tA % C::kSlots, oB = tB % C::kSlots;
       KVQ_PT(e0)
-      if (!warp_wait(&sh.o_full[oA], (uint32_t)(tA / C::kSlots) & 1u, abort_flag, limit) ||
-          !warp_wait(&sh.o_full[oB], (uint32_t)(tB / C::kSlots) & 1u, abort_flag, limit))
+      if (!warp_wait2(&sh.o_full[oA], (uint32_t)(tA / C::kSlots) & 1u, &sh.o_full[oB], (uint32_t)(tB / C::kSlots) & 1u,
+                      abort_flag, limit))
         return false;
       KVQ_PA(23, e0)
 
@@ -1082,10 +1094,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       // (a lone tile is loaded twice and its copy masked out).
       const int t1 = n > 1 ? t + 1 : t;
       const int st0 = t % C::kStages, st1 = t1 % C::kStages, q0 = t % C::kSlots, q1 = t1 % C::kSlots;
-      if (!warp_wait(&sh.s_full[q0], (uint32_t)(t / C::kSlots) & 1u, abort_flag, limit) ||
-          !warp_wait(&sh.s_full[q1], (uint32_t)(t1 / C::kSlots) & 1u, abort_flag, limit) ||
-          !warp_wait(&sh.stg_full[st0], (uint32_t)(t / C::kStages) & 1u, abort_flag, limit) ||
-          !warp_wait(&sh.stg_full[st1], (uint32_t)(t1 / C::kStages) & 1u, abort_flag, limit)) {
+      if (!warp_wait4(&sh.s_full[q0], (uint32_t)(t / C::kSlots) & 1u, &sh.s_full[q1], (uint32_t)(t1 / C::kSlots) & 1u,
+                      &sh.stg_full[st0], (uint32_t)(t / C::kStages) & 1u, &sh.stg_full[st1],
+                      (uint32_t)(t1 / C::kStages) & 1u, abort_flag, limit)) {
         ok = false;
         break;
       }
@@ -1178,11 +1189,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       }
       // P' operands (lane i = token i): token-wise V folds s into P; both
       // buffers are awaited first so the two rows are built together
-      if (!warp_wait(&sh.p_empty[q0], ((uint32_t)(t / C::kSlots) & 1u) ^ 1u, abort_flag, limit) ||
-          !warp_wait(&sh.p_empty[q1], ((uint32_t)(t1 / C::kSlots) & 1u) ^ 1u, abort_flag, limit)) {
+      if (!warp_wait2(&sh.p_empty[q0], ((uint32_t)(t / C::kSlots) & 1u) ^ 1u, &sh.p_empty[q1],
+                      ((uint32_t)(t1 / C::kSlots) & 1u) ^ 1u, abort_flag, limit)) {
         ok = false;
         break;
       }
+      if (sw == 0) { KVQ_TR(23, t) if (n > 1) KVQ_TR(23, t + 1) }
       {
         float psc[4];
 #pragma unroll
@@ -1216,6 +1228,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         if (!epilogue(ts)) { ok = false; break; }
       }
       KVQ_PA(22, s6)
+      if (sw == 0) { KVQ_TR(22, t) if (n > 1) KVQ_TR(22, t + 1) }
       pend = t;
       pend_n = n;
 #pragma unroll

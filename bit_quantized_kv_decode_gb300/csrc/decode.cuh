@@ -771,7 +771,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNAK) & 1u,
                      p2 = (uint32_t)(t >> 1) & 1u;
       KVQ_PT(c0)
-      if (!warp_wait2(&sh.stg_full[s], ps, &sh.q_empty[sl], p2 ^ 1u, abort_flag, limit)) return false;
+      if (!warp_wait4(&sh.stg_full[s], ps, &sh.q_empty[sl], p2 ^ 1u, &sh.ak_empty[a], pa ^ 1u, &sh.ak_empty[a], pa ^ 1u,
+                      abort_flag, limit))
+        return false;
       KVQ_PA(1, c0)
       const unsigned char* st = stages + (size_t)s * C::kStageBytes;
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
@@ -799,7 +801,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PA(4, c3)
       // K codes -> A_K[a] (row r = token r)
       KVQ_PT(c1)
-      if (!warp_wait(&sh.ak_empty[a], pa ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(2, c1)
       KVQ_PT(c2)
       convert_rows(st, tmem + lane_off + C::kColAK + a * C::kACols);
@@ -1138,7 +1139,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           sc[4 * u + k] = valid ? v : -INFINITY;
           if (KCW) {  // the tile's offset q . z_g is still to come: per-tile maxima
             vals[kTM + 4 * u + k] = warp_max_redux(sc[4 * u + k]);
-
           }
         }
       }

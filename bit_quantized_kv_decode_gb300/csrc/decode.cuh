@@ -64,15 +64,23 @@ constexpr int kTrT0 = 200, kTrN = 64, kTrEv = 24;
 #define KVQ_TR(ev, t) {}
 #endif
 
-constexpr int kDecodeThreads = 320;  // 10 warps
+constexpr int kDecodeThreads = 384;  // 12 warps: three warpgroups (warps 10, 11 only complete the third)
 constexpr int kMaxBatch = 1024;      // sequences per call (prefix table in shared memory)
 constexpr uint32_t FULL = 0xffffffffu;
 
-// Warp roles.
+// Warp roles.  Registers are rebalanced per warpgroup at the start of the
+// role code (setmaxnreg): the launch gives every thread kRegsLaunch; the
+// loader / MMA warpgroup gives back down to kRegsLight, and the converter and
+// softmax warpgroups take them (kRegsConvert, kRegsSoftmax).  The three add
+// up to the launch total, so the increases never wait on registers that
+// will not come.
 constexpr int kWarpConvert0 = 0;  // warps 0-3: KV codes -> tensor memory, Q' operand
 constexpr int kWarpSoftmax0 = 4;  // warps 4-7: fold, online softmax, P' operand, epilogue (two tiles per step)
 constexpr int kWarpLoad = 8;      // packed tiles HBM -> shared memory
 constexpr int kWarpMma = 9;       // tcgen05.mma issue, tensor memory owner
+constexpr int kRegsLaunch = 80, kRegsLight = 32, kRegsSoftmax = 112, kRegsConvert = 96;
+static_assert(128 * kRegsConvert + 128 * kRegsSoftmax + 128 * kRegsLight == kDecodeThreads * kRegsLaunch,
+              "setmaxnreg split must add up to the launch allocation");
 
 template <int BITS, bool BF16>
 struct DecodeCfg {
@@ -356,23 +364,61 @@ static __device__ __noinline__ bool warp_wait_slow(uint64_t* bar, uint32_t parit
     if (__shfl_sync(FULL, stop, 0)) return false;
   }
 }
+// The same loop written in place, for code that runs under a changed
+// register budget (setmaxnreg), where no calls can be made.  Kept small:
+// several phases share one copy (their barriers and parities go through a
+// small local array, touched only on this rare path).
+template <int N>
+__device__ __forceinline__ bool warp_wait_slow_inline(uint64_t* const (&bars)[N], const uint32_t (&pars)[N],
+                                                      volatile int* abort_flag, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+  for (int k = 0; k < N; ++k) {
+    for (;;) {
+      if (__all_sync(FULL, mbar_try_wait_sleep(bars[k], pars[k], 20000u))) break;
+      const bool stop = (*abort_flag != 0) || (globaltimer_ns() - t0 > limit_ns);
+      if (__any_sync(FULL, stop)) return false;  // the warp gives up together
+    }
+  }
+  return true;
+}
+
+// IL: slow path written in place (true) or out of line (false).
+template <bool IL = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint64_t limit_ns) {
   if (__all_sync(FULL, mbar_try_wait(bar, parity))) return true;
+  if (IL) {
+    uint64_t* const bars[1] = {bar};
+    const uint32_t pars[1] = {parity};
+    return warp_wait_slow_inline<1>(bars, pars, abort_flag, limit_ns);
+  }
   return warp_wait_slow(bar, parity, abort_flag, limit_ns);
 }
 
 // Two or four phases: one overlapped probe of all of them, then (rarely) the
 // one-by-one slow path.
+template <bool IL = false>
 __device__ __forceinline__ bool warp_wait2(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1,
                                            volatile int* abort_flag, uint64_t limit_ns) {
   if (__all_sync(FULL, mbar_try_wait2(b0, p0, b1, p1))) return true;
+  if (IL) {
+    uint64_t* const bars[2] = {b0, b1};
+    const uint32_t pars[2] = {p0, p1};
+    return warp_wait_slow_inline<2>(bars, pars, abort_flag, limit_ns);
+  }
   return warp_wait_slow(b0, p0, abort_flag, limit_ns) && warp_wait_slow(b1, p1, abort_flag, limit_ns);
 }
+template <bool IL = false>
 __device__ __forceinline__ bool warp_wait4(uint64_t* b0, uint32_t p0, uint64_t* b1, uint32_t p1, uint64_t* b2,
                                            uint32_t p2, uint64_t* b3, uint32_t p3, volatile int* abort_flag,
                                            uint64_t limit_ns) {
   if (__all_sync(FULL, mbar_try_wait4(b0, p0, b1, p1, b2, p2, b3, p3))) return true;
+  if (IL) {
+    uint64_t* const bars[4] = {b0, b1, b2, b3};
+    const uint32_t pars[4] = {p0, p1, p2, p3};
+    return warp_wait_slow_inline<4>(bars, pars, abort_flag, limit_ns);
+  }
   return warp_wait_slow(b0, p0, abort_flag, limit_ns) && warp_wait_slow(b1, p1, abort_flag, limit_ns) &&
          warp_wait_slow(b2, p2, abort_flag, limit_ns) && warp_wait_slow(b3, p3, abort_flag, limit_ns);
 }
@@ -383,11 +429,12 @@ __device__ __forceinline__ void set_abort(volatile int* abort_flag, uint32_t* de
 }
 
 // A four-warp group barrier on an mbarrier (count 4), bounded.
+template <bool IL = false>
 __device__ __forceinline__ bool group_sync(uint64_t* bar, uint32_t& phase, volatile int* abort_flag,
                                            uint64_t limit_ns) {
   __syncwarp();
   if (lane_id() == 0) mbar_arrive(bar);
-  bool ok = warp_wait(bar, phase, abort_flag, limit_ns);
+  bool ok = warp_wait<IL>(bar, phase, abort_flag, limit_ns);
   phase ^= 1u;
   return ok;
 }
@@ -478,22 +525,27 @@ struct TileIter {
     h = r / nblk;
     j = r - h * nblk;
   }
+  template <bool IL = false>
   __device__ __forceinline__ void next(const int* prefix, int B, int Hkv);
 };
 
 // Next (sequence, kv head) unit after (b, h): {b, h, nblk}; out of line (it
 // runs once per unit) to keep the hot loops compact.
-static __device__ __noinline__ int3 next_unit(int b, int h, int nblk, const int* prefix, int B, int Hkv) {
+__device__ __forceinline__ int3 next_unit_inline(int b, int h, int nblk, const int* prefix, int B, int Hkv) {
   if (++h < Hkv) return make_int3(b, h, nblk);
   h = 0;
   do { ++b; } while (b < B && prefix[b + 1] == prefix[b]);
   if (b < B) nblk = (prefix[b + 1] - prefix[b]) / Hkv;
   return make_int3(b, h, nblk);
 }
+static __device__ __noinline__ int3 next_unit(int b, int h, int nblk, const int* prefix, int B, int Hkv) {
+  return next_unit_inline(b, h, nblk, prefix, B, Hkv);
+}
+template <bool IL>
 __device__ __forceinline__ void TileIter::next(const int* prefix, int B, int Hkv) {
   if (++j < nblk) return;
   j = 0;
-  const int3 u = next_unit(b, h, nblk, prefix, B, Hkv);
+  const int3 u = IL ? next_unit_inline(b, h, nblk, prefix, B, Hkv) : next_unit(b, h, nblk, prefix, B, Hkv);
   b = u.x; h = u.y; nblk = u.z;
 }
 
@@ -521,7 +573,7 @@ struct SegConsts {
   float qi[4], mult[4], add[4];
 };
 template <bool KCW, bool BF16>
-static __device__ __noinline__ SegConsts softmax_unit_consts(const uint16_t* qb, int i, float sm_scale_log2) {
+static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* qb, int i, float sm_scale_log2) {
   using C = DecodeCfg<4, BF16>;  // the code scale does not depend on the bit width
   float qmax[4], qsum[4];
   unit_q_stats<4>(qb, !KCW, qmax, qsum);
@@ -620,18 +672,37 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   const long long g1 = active ? range_start(cta + 1, T, Cn) : 0;
   const int ntiles = (int)(g1 - g0);
 
-  // ============================================================= loader
-  if (warp == kWarpLoad) {
-    if (lane == 0 && ntiles > 0) {
+  // Each role leaves through finish_cta() and returns: code after the role
+  // branches would be shared by warps with different register budgets.
+  auto finish_cta = [&]() {
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::kTmemCols);
+    }
+#if defined(KVQ_PROFILE) && !defined(KVQ_TRACE)
+    if (p.prof != nullptr && tid < 32) atomicAdd(&p.prof[blockIdx.x * 32 + tid], sh.prof[tid]);
+#endif
+#ifdef KVQ_TRACE
+    if (p.prof != nullptr)
+      for (int j = tid; j < kTrN * kTrEv; j += kDecodeThreads) p.prof[(size_t)blockIdx.x * kTrN * kTrEv + j] = sh.trace[j];
+#endif
+  };
+
+  if (warp >= kWarpLoad) {
+    setmaxnreg_dec<kRegsLight>();
+    // ========================================================== loader
+    if (warp == kWarpLoad && lane == 0 && ntiles > 0) {
       const uint64_t policy = l2_policy_evict_first();
       uint32_t issued = 0u, issued_par = 0u;  // per stage: a copy was issued / its phase parity
       TileIter it;
       it.init(prefix, B, Hkv, (int)g0);
-      for (int t = 0; t < ntiles; ++t, it.next(prefix, B, Hkv)) {
+      for (int t = 0; t < ntiles; ++t, it.next<true>(prefix, B, Hkv)) {
         const int s = t % C::kStages;
         const uint32_t ph = (uint32_t)(t / C::kStages) & 1u;
         KVQ_PT(le)
-        if (!mbar_wait_bounded(&sh.stg_empty[s], ph ^ 1u, abort_flag, limit)) {
+        if (!mbar_wait_bounded<true>(&sh.stg_empty[s], ph ^ 1u, abort_flag, limit)) {
           set_abort(abort_flag, p.dev_status);
           break;
         }
@@ -661,16 +732,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       }
       // never leave a copy in flight: wait for every issued stage to land
       for (int s = 0; s < C::kStages; ++s)
-        if (issued & (1u << s)) mbar_wait_bounded(&sh.stg_full[s], (issued_par >> s) & 1u, nullptr, limit);
+        if (issued & (1u << s)) mbar_wait_bounded<true>(&sh.stg_full[s], (issued_par >> s) & 1u, nullptr, limit);
     }
-  }
   // ================================================================ MMA
   // Issues QK^T of tile nq and PV of tile np in whatever order their inputs
   // become ready (non-blocking tests), so neither product waits behind the
   // other.  QK^T(t): A = K codes, B = Q', D = S slot.  PV(t): A = V codes,
   // B = P', D = O slot.
-  else if (warp == kWarpMma) {
-    if (lane == 0 && ntiles > 0) {
+    else if (warp == kWarpMma && lane == 0 && ntiles > 0) {
       bool ok = true;
       int nq = 0, np = 0;
       uint64_t idle_since = 0;
@@ -732,13 +801,16 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       if (!ok) set_abort(abort_flag, p.dev_status);
       // drain: all issued MMAs complete before tensor memory is released
       tc_commit(&sh.drain);
-      mbar_wait_bounded(&sh.drain, 0, nullptr, limit);
+      mbar_wait_bounded<true>(&sh.drain, 0, nullptr, limit);
     }
+    finish_cta();
+    return;
   }
   // ========================================================== converters
   // Software-pipelined: Q' and K of tile t + 1 are produced before V of tile
   // t, so QK^T runs a tile ahead and never waits behind an earlier PV.
   else if (warp < kWarpSoftmax0) {
+    setmaxnreg_inc<kRegsConvert>();
     const int r = tid;  // tensor-memory lane = A row; also this thread's channel of Q'
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const int qrow = a_pos<BITS, BF16>(r);
@@ -771,7 +843,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNAK) & 1u,
                      p2 = (uint32_t)(t >> 1) & 1u;
       KVQ_PT(c0)
-      if (!warp_wait4(&sh.stg_full[s], ps, &sh.q_empty[sl], p2 ^ 1u, &sh.ak_empty[a], pa ^ 1u, &sh.ak_empty[a], pa ^ 1u,
+      if (!warp_wait4<true>(&sh.stg_full[s], ps, &sh.q_empty[sl], p2 ^ 1u, &sh.ak_empty[a], pa ^ 1u, &sh.ak_empty[a], pa ^ 1u,
                       abort_flag, limit))
         return false;
       KVQ_PA(1, c0)
@@ -818,7 +890,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const int s = t % C::kStages, a = t % C::kNAV;
       const uint32_t pa = (uint32_t)(t / C::kNAV) & 1u;
       KVQ_PT(c5)
-      if (!warp_wait(&sh.av_empty[a], pa ^ 1u, abort_flag, limit)) return false;
+      if (!warp_wait<true>(&sh.av_empty[a], pa ^ 1u, abort_flag, limit)) return false;
       KVQ_PA(6, c5)
       KVQ_PT(c6)
       convert_rows(stages + (size_t)s * C::kStageBytes + C::kBlockBytes, tmem + lane_off + C::kColAV + a * C::kACols);
@@ -845,12 +917,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       ok = v_part(t);
     }
     if (!ok) set_abort(abort_flag, p.dev_status);
+    finish_cta();
+    return;
   }
   // ============================================================= softmax
   // Two tiles of one (sequence, kv head) per step: the fixed per-step costs
   // (waits, the cross-warp reduction round, bookkeeping) are paid once per
   // pair, and both tiles share one running-max update.
   else {
+    setmaxnreg_inc<kRegsSoftmax>();
     const int i = tid - kWarpSoftmax0 * 32;  // tensor-memory lane: token (scores) / channel (output)
     const int sw = warp - kWarpSoftmax0;     // warp = lane quarter
     const uint32_t lane_off = (uint32_t)(sw * 32) << 16;
@@ -913,7 +988,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         }
       }
       const uint32_t use = grp_phase;
-      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
+      if (!group_sync<true>(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
       const int v = lane < kNV ? lane : 0;
       const float r0 = sh.sw_red[use][0][v], r1 = sh.sw_red[use][1][v];
       const float r2 = sh.sw_red[use][2][v], r3 = sh.sw_red[use][3][v];
@@ -930,7 +1005,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const int tA = pend, tB = pend_n > 1 ? pend + 1 : pend;
       const int oA = tA % C::kSlots, oB = tB % C::kSlots;
       KVQ_PT(e0)
-      if (!warp_wait2(&sh.o_full[oA], (uint32_t)(tA / C::kSlots) & 1u, &sh.o_full[oB], (uint32_t)(tB / C::kSlots) & 1u,
+      if (!warp_wait2<true>(&sh.o_full[oA], (uint32_t)(tA / C::kSlots) & 1u, &sh.o_full[oB], (uint32_t)(tB / C::kSlots) & 1u,
                       abort_flag, limit))
         return false;
       KVQ_PA(23, e0)
@@ -1012,13 +1087,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         if (i == k) p.part_lse[((size_t)cta * 2 + slot) * kGroupQ + k] = lse4[k];
       }
       __threadfence();
-      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
+      if (!group_sync<true>(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
       const int u = b * Hkv + h;
       if (i == 0) {
         int old = atomicAdd(&p.counters[u], 1);
         sh.flag = (old == c_last - c_first) ? 1 : 0;
       }
-      if (!group_sync(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
+      if (!group_sync<true>(&sh.sw_grp, grp_phase, abort_flag, limit)) return false;
       if (!sh.flag) return true;
       __threadfence();
       float mx[4], den[4], acc[4];
@@ -1095,7 +1170,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       // (a lone tile is loaded twice and its copy masked out).
       const int t1 = n > 1 ? t + 1 : t;
       const int st0 = t % C::kStages, st1 = t1 % C::kStages, q0 = t % C::kSlots, q1 = t1 % C::kSlots;
-      if (!warp_wait4(&sh.s_full[q0], (uint32_t)(t / C::kSlots) & 1u, &sh.s_full[q1], (uint32_t)(t1 / C::kSlots) & 1u,
+      if (!warp_wait4<true>(&sh.s_full[q0], (uint32_t)(t / C::kSlots) & 1u, &sh.s_full[q1], (uint32_t)(t1 / C::kSlots) & 1u,
                       &sh.stg_full[st0], (uint32_t)(t / C::kStages) & 1u, &sh.stg_full[st1],
                       (uint32_t)(t1 / C::kStages) & 1u, abort_flag, limit)) {
         ok = false;
@@ -1119,6 +1194,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         if (KCW && !BF16) fs_t[u] = pow2_group_inv(f16_exp_field(max_f16_bits_128(szp)));
       }
       if (n < 2) { kz_t[1] = 0.f; vs_t[1] = 0.f; vz_t[1] = 0.f; }
+      // what does not depend on the scores runs while their loads are in flight:
+      // token-wise V: largest V scale of the pair (positive: ordered as integers);
+      // channel-wise K: the offsets q . z_g, reduced over this warp's channels
+      if (!VCW) vals[kVM] = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(fmaxf(vs_t[0], vs_t[1]))));
+      float cgp = 0.f;
+      if (KCW) {
+        float za[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { za[k] = qi[k] * kz_t[0]; za[4 + k] = qi[k] * kz_t[1]; }
+        cgp = warp_sum8_transposed(za);
+      }
       tc_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -1146,8 +1232,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 #pragma unroll
         for (int k = 0; k < 4; ++k) vals[kTM + k] = warp_max_redux(fmaxf(sc[k], sc[4 + k]));
       }
-      // token-wise V: largest V scale of the pair (positive: ordered as integers)
-      if (!VCW) vals[kVM] = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(fmaxf(vs_t[0], vs_t[1]))));
       if (VCW) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) vals[kWS + k] = ws_prev[k];
@@ -1155,13 +1239,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PA(16, s0)
       KVQ_PT(s2)
       float res[kNV];
-      float cgp = 0.f;
-      if (KCW) {
-        float za[8];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) { za[k] = qi[k] * kz_t[0]; za[4 + k] = qi[k] * kz_t[1]; }
-        cgp = warp_sum8_transposed(za);
-      }
       constexpr uint32_t kUsed = (KCW ? 0xffffu : 0xfu) | (VCW ? (0xffu << kWS) : (1u << kVM));
       if (!round(vals, res, kUsed, KCW, cgp)) { ok = false; break; }
       KVQ_PA(18, s2)
@@ -1189,7 +1266,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       }
       // P' operands (lane i = token i): token-wise V folds s into P; both
       // buffers are awaited first so the two rows are built together
-      if (!warp_wait2(&sh.p_empty[q0], ((uint32_t)(t / C::kSlots) & 1u) ^ 1u, &sh.p_empty[q1],
+      if (!warp_wait2<true>(&sh.p_empty[q0], ((uint32_t)(t / C::kSlots) & 1u) ^ 1u, &sh.p_empty[q1],
                       ((uint32_t)(t1 / C::kSlots) & 1u) ^ 1u, abort_flag, limit)) {
         ok = false;
         break;
@@ -1244,33 +1321,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           ws_prev[4 * u + k] = VCW ? (float)__reduce_add_sync(FULL, __float2uint_rn(pr[4 * u + k] * kFix)) * (1.0f / kFix)
                                    : 0.f;
       }
-      for (int u = 0; u < n; ++u) it.next(prefix, B, Hkv);
+      for (int u = 0; u < n; ++u) it.next<true>(prefix, B, Hkv);
       t += n;
     }
     if (ok && pend_n > 0) ok = drain() && finalize(pb, ph, pfirst, pue <= g1, pus, pue);
     if (!ok && ntiles > 0) set_abort(abort_flag, p.dev_status);
+    finish_cta();
   }
-
-  // ------------------------------------------------------------ teardown
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kWarpMma) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
-  }
-#if defined(KVQ_PROFILE) && !defined(KVQ_TRACE)
-  if (p.prof != nullptr && tid < 32) atomicAdd(&p.prof[blockIdx.x * 32 + tid], sh.prof[tid]);
-#endif
-#ifdef KVQ_TRACE
-  if (p.prof != nullptr)
-    for (int j = tid; j < kTrN * kTrEv; j += kDecodeThreads) p.prof[(size_t)blockIdx.x * kTrN * kTrEv + j] = sh.trace[j];
-#endif
 }
 
 template <int BITS, bool KCW, bool VCW, bool BF16>
 cudaError_t launch_decode_instance(const DecodeParams& p, cudaStream_t stream) {
   constexpr size_t smem = decode_smem_layout_bytes<BITS, BF16>();
   auto kern = decode_kernel<BITS, KCW, VCW, BF16>;
+  // The register split inside the kernel assumes exactly kRegsLaunch
+  // registers per thread at launch; with fewer, the softmax warpgroup's
+  // increase could never be granted.  Refuse to launch such a build.
+  static const bool regs_ok = [&] {
+    cudaFuncAttributes a{};
+    return cudaFuncGetAttributes(&a, kern) == cudaSuccess && a.numRegs == kRegsLaunch;
+  }();
+  if (!regs_ok) return cudaErrorInvalidConfiguration;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<p.num_ctas, kDecodeThreads, smem, stream>>>(p);

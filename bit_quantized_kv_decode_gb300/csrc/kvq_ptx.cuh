@@ -133,10 +133,35 @@ static __device__ __noinline__ bool mbar_wait_bounded_slow(uint64_t* bar, uint32
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
+// IL: the waiting loop written in place (for code under a changed register
+// budget, where no calls can be made) instead of out of line.
+template <bool IL = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, const volatile int* abort,
                                                   uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (IL) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+      if ((abort != nullptr && *abort) || globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
   return mbar_wait_bounded_slow(bar, parity, abort, limit_ns);
+}
+
+// ------------------------------------------------------- register budgets
+// Per-warpgroup register count change (all four warps of the warpgroup run
+// it); the count is a multiple of 8 in [24, 256].  An increase waits until
+// other warpgroups have released enough registers.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N) : "memory");
 }
 
 // -------------------------------------------------------------- bulk copies

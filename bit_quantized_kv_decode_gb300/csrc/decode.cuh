@@ -78,7 +78,7 @@ constexpr int kWarpConvert0 = 0;  // warps 0-3: KV codes -> tensor memory, Q' op
 constexpr int kWarpSoftmax0 = 4;  // warps 4-7: fold, online softmax, P' operand, epilogue (two tiles per step)
 constexpr int kWarpLoad = 8;      // packed tiles HBM -> shared memory
 constexpr int kWarpMma = 9;       // tcgen05.mma issue, tensor memory owner
-constexpr int kRegsLaunch = 80, kRegsLight = 32, kRegsSoftmax = 112, kRegsConvert = 96;
+constexpr int kRegsLaunch = 80, kRegsLight = 24, kRegsSoftmax = 112, kRegsConvert = 104;
 static_assert(128 * kRegsConvert + 128 * kRegsSoftmax + 128 * kRegsLight == kDecodeThreads * kRegsLaunch,
               "setmaxnreg split must add up to the launch allocation");
 

@@ -55,8 +55,9 @@ def cache_desc(bits: int, k_scheme: int, v_scheme: int, num_kv_heads: int, num_p
 
 
 def attn_desc(cache: CacheDesc, batch: int, max_blocks: int, mode: int = OPERANDS_FP8, sm_scale: float = 0.0,
-              num_ctas: int = 0, flags: int = 0) -> AttnDesc:
-    return AttnDesc(cache, batch, GROUP_Q * cache.num_kv_heads, max_blocks, mode, sm_scale, num_ctas, flags)
+              num_ctas: int = 0, flags: int = 0, num_q_heads: Optional[int] = None) -> AttnDesc:
+    hq = GROUP_Q * cache.num_kv_heads if num_q_heads is None else num_q_heads
+    return AttnDesc(cache, batch, hq, max_blocks, mode, sm_scale, num_ctas, flags)
 
 
 def block_bytes(bits: int) -> int:

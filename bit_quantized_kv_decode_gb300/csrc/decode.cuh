@@ -493,17 +493,21 @@ __device__ __forceinline__ float max_f16_128(const uint16_t* v) { return h2f((ui
 
 __device__ __forceinline__ float bf2f(uint16_t bits) { return __uint_as_float((uint32_t)bits << 16); }
 
-// Per-(sequence, kv head) query statistics, computed by each warp on its own
-// (identical in every warp): qmax[h] = max_d |q[h, d]|, qsum[h] = sum_d q[h, d]
-// for NH consecutive query heads starting at qb (16-byte aligned rows of 128
-// bf16).
+// Per-unit query statistics, computed by each warp on its own (identical in
+// every warp): qmax[h] = max_d |q[h, d]|, qsum[h] = sum_d q[h, d] for the
+// unit's `rows` consecutive query heads starting at qb (16-byte aligned rows
+// of 128 bf16); heads rows..NH-1 do not exist (fewer query heads per KV head)
+// and read as zero.
 template <int NH>
-__device__ __forceinline__ void unit_q_stats(const uint16_t* qb, bool need_sum, float (&qmax)[NH], float (&qsum)[NH]) {
+__device__ __forceinline__ void unit_q_stats(const uint16_t* qb, int rows, bool need_sum, float (&qmax)[NH],
+                                             float (&qsum)[NH]) {
 #pragma unroll
   for (int h = 0; h < NH; ++h) {
-    uint2 w = *reinterpret_cast<const uint2*>(qb + h * kHeadDim + 4 * lane_id());
-    float x0 = bf2f((uint16_t)(w.x & 0xffffu)), x1 = bf2f((uint16_t)(w.x >> 16));
-    float x2 = bf2f((uint16_t)(w.y & 0xffffu)), x3 = bf2f((uint16_t)(w.y >> 16));
+    // an empty slot re-reads row 0 (always valid memory) and is zeroed: no branch
+    const float keep = h < rows ? 1.0f : 0.0f;
+    uint2 w = *reinterpret_cast<const uint2*>(qb + (h < rows ? h : 0) * kHeadDim + 4 * lane_id());
+    float x0 = bf2f((uint16_t)(w.x & 0xffffu)) * keep, x1 = bf2f((uint16_t)(w.x >> 16)) * keep;
+    float x2 = bf2f((uint16_t)(w.y & 0xffffu)) * keep, x3 = bf2f((uint16_t)(w.y >> 16)) * keep;
     float m = fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(x2), fabsf(x3)));
     qmax[h] = __uint_as_float(__reduce_max_sync(FULL, __float_as_uint(m)));
     qsum[h] = need_sum ? warp_sum((x0 + x1) + (x2 + x3)) : 0.0f;
@@ -554,34 +558,38 @@ __device__ __forceinline__ int cta_of_tile(long long t, long long T, int C) {
 }
 __device__ __forceinline__ long long range_start(int c, long long T, int C) { return (long long)c * T / C; }
 
-// Per-unit set-up, out of line (once per (sequence, kv head)).
-// Converter thread r: q[4h + i, r] times head i's Q' prescale.
+// Per-unit set-up, out of line (once per unit).
+// Converter thread r: q[i, r] of the unit's query head i times that head's Q'
+// prescale (0 for the head slots a unit with fewer than 4 heads leaves empty).
 template <bool KCW, bool BF16>
-static __device__ __noinline__ float4 converter_unit_q(const uint16_t* qb, int r) {
+static __device__ __noinline__ float4 converter_unit_q(const uint16_t* qb, int rows, int r) {
   float qmax[4], qsum[4];
-  unit_q_stats<4>(qb, false, qmax, qsum);
+  unit_q_stats<4>(qb, rows, false, qmax, qsum);
   float qh[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
-    qh[i] = bf2f(qb[i * kHeadDim + r]) * (BF16 ? 1.0f : KCW ? pow2_head(qmax[i]) : pow2_prescale(qmax[i]));
+    qh[i] = bf2f(qb[(i < rows ? i : 0) * kHeadDim + r]) * (i < rows ? 1.0f : 0.0f) *
+            (BF16 ? 1.0f : KCW ? pow2_head(qmax[i]) : pow2_prescale(qmax[i]));
   return make_float4(qh[0], qh[1], qh[2], qh[3]);
 }
 // Softmax thread i: per-head score constants of the unit.  Channel-wise K:
-// add = the unit's part of the score multiplier, qi = q[4h + k, i];
-// token-wise K: S = s_l * (q . code) * mult + z_l * add.
+// add = the unit's part of the score multiplier, qi = q[k, i] of the unit's
+// head k; token-wise K: S = s_l * (q . code) * mult + z_l * add.  Empty head
+// slots get zero constants (their scores are 0 and never written out).
 struct SegConsts {
   float qi[4], mult[4], add[4];
 };
 template <bool KCW, bool BF16>
-static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* qb, int i, float sm_scale_log2) {
+static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* qb, int rows, int i,
+                                                               float sm_scale_log2) {
   using C = DecodeCfg<4, BF16>;  // the code scale does not depend on the bit width
   float qmax[4], qsum[4];
-  unit_q_stats<4>(qb, !KCW, qmax, qsum);
+  unit_q_stats<4>(qb, rows, !KCW, qmax, qsum);
   SegConsts c;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     if (KCW) {
-      c.qi[k] = bf2f(qb[k * kHeadDim + i]);
+      c.qi[k] = bf2f(qb[(k < rows ? k : 0) * kHeadDim + i]) * (k < rows ? 1.0f : 0.0f);
       c.mult[k] = 0.f;
       c.add[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_head_inv(qmax[k])) * sm_scale_log2;
     } else {
@@ -594,7 +602,9 @@ static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* 
 }
 
 // ================================================================= kernel
-template <int BITS, bool KCW, bool VCW, bool BF16>
+// GQ4: exactly 4 query heads per KV head (one unit per KV head, no empty
+// head slots); the other groupings (1, 2, 8) take the run-time values in p.
+template <int BITS, bool KCW, bool VCW, bool BF16, bool GQ4>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeParams p) {
   using C = DecodeCfg<BITS, BF16>;
   using Bars = DecodeBarriers<BITS, BF16>;
@@ -607,7 +617,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   int* lens = prefix + (kMaxBatch + 1);           // [B] validated sequence lengths
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int B = p.batch, Hkv = p.num_kv_heads;
+  // Units: (sequence, unit head) pairs.  A unit holds up to 4 query heads
+  // (gq) of one KV head; with 8 query heads per KV head there are two units
+  // per KV head (unit head u reads KV head u >> kv_shift).
+  const int B = p.batch, Hkv = GQ4 ? p.num_kv_heads : p.units_per_seq;
+  const int gq = GQ4 ? kGroupQ : p.gq, kv_shift = GQ4 ? 0 : p.kv_shift;
   const int cta = blockIdx.x;
   volatile int* abort_flag = &sh.abort_flag;
   const uint64_t limit = p.wait_limit_ns;
@@ -713,7 +727,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           report(p.dev_status, KVQ_DEV_BAD_PAGE);
           page = 0;
         }
-        const size_t blk = (size_t)page * Hkv + it.h;
+        const size_t blk = (size_t)page * p.num_kv_heads + (it.h >> kv_shift);
         unsigned char* st = stages + (size_t)s * C::kStageBytes;
         mbar_arrive_expect_tx(&sh.stg_full[s], C::kStageBytes);
         bulk_g2s_evict_first(st, p.k_codes + blk * C::kBlockBytes, C::kBlockBytes, &sh.stg_full[s], policy);
@@ -851,7 +865,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       const uint16_t* ks = reinterpret_cast<const uint16_t*>(st + 2 * C::kBlockBytes);
       if (t == 0 || it.j == 0) {  // new (sequence, kv head): its four query rows
         ++seg;
-        const float4 q4 = converter_unit_q<KCW, BF16>(p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim, r);
+        const float4 q4 =
+            converter_unit_q<KCW, BF16>(p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * gq) * kHeadDim, gq, r);
         qh[0] = q4.x; qh[1] = q4.y; qh[2] = q4.z; qh[3] = q4.w;
       }
       // Q' operand: token-wise K uses q (written once per segment per slot);
@@ -1068,10 +1083,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         out4[k] = (O[k] + z) / l;
         lse4[k] = (m[k] + __log2f(l)) * kLn2;
       }
-      const size_t row0 = (size_t)b * p.num_q_heads + (size_t)h * kGroupQ;
+      const size_t row0 = (size_t)b * p.num_q_heads + (size_t)h * gq;
       if (first_global && last_global) {  // whole (sequence, head) in this CTA
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
+          if (k >= gq) break;  // empty head slots
           p.out[(row0 + k) * kHeadDim + i] = out4[k];
           if (i == k) p.lse[row0 + k] = lse4[k];
         }
@@ -1115,6 +1131,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
+        if (k >= gq) break;
         p.out[(row0 + k) * kHeadDim + i] = acc[k] / den[k];
         if (i == k) p.lse[row0 + k] = mx[k] + __logf(den[k]);
       }
@@ -1150,7 +1167,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       if (seg_first) {
         pb = it.b; ph = it.h; pfirst = ustart >= g0; pus = ustart; pue = uend;
         const SegConsts sc4 = softmax_unit_consts<KCW, BF16>(
-            p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * kGroupQ) * kHeadDim, i, p.sm_scale_log2);
+            p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * gq) * kHeadDim, gq, i, p.sm_scale_log2);
 #pragma unroll
         for (int k = 0; k < 4; ++k) { qi[k] = sc4.qi[k]; mult[k] = sc4.mult[k]; add[k] = sc4.add[k]; }
       }
@@ -1330,10 +1347,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   }
 }
 
-template <int BITS, bool KCW, bool VCW, bool BF16>
+template <int BITS, bool KCW, bool VCW, bool BF16, bool GQ4>
 cudaError_t launch_decode_instance(const DecodeParams& p, cudaStream_t stream) {
   constexpr size_t smem = decode_smem_layout_bytes<BITS, BF16>();
-  auto kern = decode_kernel<BITS, KCW, VCW, BF16>;
+  auto kern = decode_kernel<BITS, KCW, VCW, BF16, GQ4>;
   // The register split inside the kernel assumes exactly kRegsLaunch
   // registers per thread at launch; with fewer, the softmax warpgroup's
   // increase could never be granted.  Refuse to launch such a build.

@@ -1,20 +1,29 @@
-// Decode-attention kernel instances for 4-bit caches (all K/V scheme pairs, both operand modes).
+// Decode-attention kernel instances for 4-bit caches (all K/V scheme pairs, both operand modes);
+// GQ4 selects 4 query heads per KV head (this file) or the other groupings
+// (decode_i4_g.cu, which defines GQ4 false before including this one).
 #include "decode.cuh"
+
+#ifndef KVQ_GQ4
+#define KVQ_GQ4 true
+#define KVQ_FN launch_decode_i4
+#endif
 
 namespace kvq {
 
-cudaError_t launch_decode_i4(int k_scheme, int v_scheme, int mode, const DecodeParams& p, cudaStream_t s) {
+constexpr bool GQ4 = KVQ_GQ4;
+
+cudaError_t KVQ_FN(int k_scheme, int v_scheme, int mode, const DecodeParams& p, cudaStream_t s) {
   const bool kcw = k_scheme == KVQ_CHANNELWISE, vcw = v_scheme == KVQ_CHANNELWISE, bf16 = mode == KVQ_OPERANDS_BF16;
   if (!bf16) {
-    if (!kcw && !vcw) return launch_decode_instance<4, false, false, false>(p, s);
-    if (!kcw && vcw) return launch_decode_instance<4, false, true, false>(p, s);
-    if (kcw && !vcw) return launch_decode_instance<4, true, false, false>(p, s);
-    return launch_decode_instance<4, true, true, false>(p, s);
+    if (!kcw && !vcw) return launch_decode_instance<4, false, false, false, GQ4>(p, s);
+    if (!kcw && vcw) return launch_decode_instance<4, false, true, false, GQ4>(p, s);
+    if (kcw && !vcw) return launch_decode_instance<4, true, false, false, GQ4>(p, s);
+    return launch_decode_instance<4, true, true, false, GQ4>(p, s);
   }
-  if (!kcw && !vcw) return launch_decode_instance<4, false, false, true>(p, s);
-  if (!kcw && vcw) return launch_decode_instance<4, false, true, true>(p, s);
-  if (kcw && !vcw) return launch_decode_instance<4, true, false, true>(p, s);
-  return launch_decode_instance<4, true, true, true>(p, s);
+  if (!kcw && !vcw) return launch_decode_instance<4, false, false, true, GQ4>(p, s);
+  if (!kcw && vcw) return launch_decode_instance<4, false, true, true, GQ4>(p, s);
+  if (kcw && !vcw) return launch_decode_instance<4, true, false, true, GQ4>(p, s);
+  return launch_decode_instance<4, true, true, true, GQ4>(p, s);
 }
 
 }  // namespace kvq

@@ -52,10 +52,24 @@ struct WorkspaceLayout {
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-WorkspaceLayout workspace_layout(int batch, int kv_heads, int num_ctas) {
+// Query heads per KV head the kernel takes (1, 2, 4 or 8; 0 otherwise) and
+// the work units per sequence: a unit holds up to 4 query heads of one KV
+// head, so 8 query heads per KV head make two units per KV head.
+int heads_per_kv(const kvq_attn_desc* d) {
+  const int hkv = d->cache.num_kv_heads;
+  if (hkv < 1 || d->num_q_heads % hkv != 0) return 0;
+  const int g = d->num_q_heads / hkv;
+  return (g == 1 || g == 2 || g == 4 || g == 8) ? g : 0;
+}
+int units_per_seq(const kvq_attn_desc* d) {
+  const int g = heads_per_kv(d);
+  return g > kGroupQ ? d->cache.num_kv_heads * (g / kGroupQ) : d->cache.num_kv_heads;
+}
+
+WorkspaceLayout workspace_layout(int batch, int units, int num_ctas) {
   WorkspaceLayout w;
   w.counters = 0;
-  w.part_lse = round_up((size_t)batch * kv_heads * kCounterGroups * sizeof(int), 256);
+  w.part_lse = round_up((size_t)batch * units * kCounterGroups * sizeof(int), 256);
   w.part_o = w.part_lse + round_up((size_t)num_ctas * 2 * kGroupQ * sizeof(float), 256);
   w.total = w.part_o + round_up((size_t)num_ctas * 2 * kGroupQ * kHeadDim * sizeof(float), 256);
   return w;
@@ -67,17 +81,17 @@ kvq_status check_attn(const kvq_attn_desc* d) {
   if (s != KVQ_OK) return s;
   if (d->batch < 1 || d->max_blocks < 1 || d->num_q_heads < 1) return KVQ_ERR_INVALID_ARG;
   if (d->batch > kMaxBatchDecode) return KVQ_ERR_UNSUPPORTED;
-  if (d->num_q_heads != kGroupQ * d->cache.num_kv_heads) return KVQ_ERR_UNSUPPORTED;
+  if (heads_per_kv(d) == 0) return KVQ_ERR_UNSUPPORTED;  // 1, 2, 4 or 8 query heads per KV head
   if (d->operand_mode != KVQ_OPERANDS_FP8 && d->operand_mode != KVQ_OPERANDS_BF16) return KVQ_ERR_INVALID_ARG;
   if (d->num_ctas < 0 || (d->flags & ~KVQ_FLAG_TEST_STALL) != 0) return KVQ_ERR_INVALID_ARG;
   if (!(std::isfinite(d->sm_scale))) return KVQ_ERR_INVALID_ARG;
-  if ((long long)d->batch * d->cache.num_kv_heads * d->max_blocks > (1LL << 30)) return KVQ_ERR_UNSUPPORTED;
+  if ((long long)d->batch * units_per_seq(d) * d->max_blocks > (1LL << 30)) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
 int resolve_ctas(const kvq_attn_desc* d, int sm_count) {
   long long want = d->num_ctas > 0 ? d->num_ctas : (long long)decode_ctas_per_sm() * sm_count;
-  long long tiles_bound = (long long)d->batch * d->cache.num_kv_heads * d->max_blocks;
+  long long tiles_bound = (long long)d->batch * units_per_seq(d) * d->max_blocks;
   if (want > tiles_bound) want = tiles_bound;
   return (int)(want < 1 ? 1 : want);
 }
@@ -202,7 +216,7 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* 
     if (s != KVQ_OK) return s;
   }
   const int ctas = resolve_ctas(desc, sm);
-  *bytes = workspace_layout(desc->batch, desc->cache.num_kv_heads, ctas).total;
+  *bytes = workspace_layout(desc->batch, units_per_seq(desc), ctas).total;
   return KVQ_OK;
 }
 
@@ -228,12 +242,12 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
   s = check_device(&sm);
   if (s != KVQ_OK) return s;
   const int ctas = resolve_ctas(desc, sm);
-  const WorkspaceLayout w = workspace_layout(desc->batch, desc->cache.num_kv_heads, ctas);
+  const WorkspaceLayout w = workspace_layout(desc->batch, units_per_seq(desc), ctas);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVQ_ERR_WORKSPACE;
   if (workspace_bytes < w.total) return KVQ_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  if (cudaMemsetAsync(ws + w.counters, 0, (size_t)desc->batch * desc->cache.num_kv_heads * kCounterGroups * sizeof(int),
+  if (cudaMemsetAsync(ws + w.counters, 0, (size_t)desc->batch * units_per_seq(desc) * kCounterGroups * sizeof(int),
                       st) !=
       cudaSuccess)
     return KVQ_ERR_CUDA;
@@ -246,6 +260,12 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
   p.part_o = reinterpret_cast<float*>(ws + w.part_o);
   p.batch = desc->batch; p.num_kv_heads = desc->cache.num_kv_heads; p.num_q_heads = desc->num_q_heads;
   p.max_blocks = desc->max_blocks; p.num_pages = desc->cache.num_pages; p.num_ctas = ctas;
+  {
+    const int g = heads_per_kv(desc);
+    p.gq = g < kGroupQ ? g : kGroupQ;
+    p.units_per_seq = units_per_seq(desc);
+    p.kv_shift = g > kGroupQ ? 1 : 0;
+  }
   const float sm_scale = desc->sm_scale > 0.0f ? desc->sm_scale : 1.0f / std::sqrt((float)kHeadDim);
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.flags = desc->flags;

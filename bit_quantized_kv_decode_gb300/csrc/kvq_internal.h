@@ -63,6 +63,11 @@ struct DecodeParams {
   float* part_o;        // [num_ctas][2][4][128]
   float* part_lse;      // [num_ctas][2][4]
   int batch, num_kv_heads, num_q_heads, max_blocks, num_pages;
+  // units of work: up to 4 query heads of one KV head each.  gq = query heads
+  // per unit (1, 2 or 4); units_per_seq = units per sequence (num_kv_heads,
+  // or 2 * num_kv_heads with 8 query heads per KV head); unit head u reads KV
+  // head u >> kv_shift.
+  int gq, units_per_seq, kv_shift;
   int num_ctas;
   float sm_scale_log2;  // sm_scale * log2(e)
   uint32_t flags;

@@ -98,7 +98,8 @@ typedef struct kvq_cache_desc {
 typedef struct kvq_attn_desc {
   kvq_cache_desc cache;
   int32_t batch;        /* sequences (>= 1) */
-  int32_t num_q_heads;  /* must be 4 * num_kv_heads */
+  int32_t num_q_heads;  /* 1, 2, 4 or 8 times num_kv_heads (query head h reads
+                           KV head h / (num_q_heads / num_kv_heads)) */
   int32_t max_blocks;   /* page_table row length; contiguous: blocks per sequence */
   int32_t operand_mode; /* kvq_operand_mode */
   float sm_scale;       /* <= 0 selects 1/sqrt(head_dim) */

@@ -67,8 +67,17 @@ def test_workspace_size_host_only(lib):
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
     # counters (one per sequence x kv head) + part lse + part out, each 256-byte aligned
     assert n.value == 128 * 8 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
-    bad = _lib.AttnDesc(_cache(4), 128, 16, 256, 0, 0.0, 304, 0)  # GQA 2 is not built
+    bad = _lib.AttnDesc(_cache(4), 128, 24, 256, 0, 0.0, 304, 0)  # 3 query heads per KV head: not built
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
+    bad = _lib.AttnDesc(_cache(4), 128, 20, 256, 0, 0.0, 304, 0)  # not a multiple of the KV heads
+    assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
+    for hq in (8, 16):  # 1 and 2 query heads per KV head: one unit per KV head
+        d = _lib.AttnDesc(_cache(4, pages=128 * 256), 128, hq, 256, 0, 0.0, 304, 0)
+        assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+        assert n.value == 128 * 8 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
+    d = _lib.AttnDesc(_cache(4, pages=128 * 256), 128, 64, 256, 0, 0.0, 304, 0)  # 8: two units per KV head
+    assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+    assert n.value == 128 * 16 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
     bad = _lib.AttnDesc(_cache(4), 0, 32, 256, 0, 0.0, 304, 0)
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
     bad = _lib.AttnDesc(_cache(4), 2048, 32, 256, 0, 0.0, 304, 0)

@@ -40,6 +40,33 @@ def test_schemes_ragged(bits, kcw, vcw, mode):
     assert_attention_close(pb, res, mode)
 
 
+@pytest.mark.parametrize("gq", [1, 2, 8])
+@pytest.mark.parametrize("kcw,vcw", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_query_heads_per_kv_head(gq, kcw, vcw):
+    """1, 2 and 8 query heads per KV head (8 = two work units per KV head) on
+    a ragged batch, both operand modes."""
+    bits = 4 if kcw != vcw else 2
+    w = synth.shrink(synth.WORKLOADS["tiny"], batch=3, num_kv_heads=2, num_q_heads=gq * 2, bits=bits,
+                     k_scheme=kcw, v_scheme=vcw, max_seq_len=1024)
+    pb = make_problem(w, seed=300 + 4 * gq + 2 * kcw + vcw, lens=[1000, 129, 1])
+    for mode in (0, 1):
+        res = run_gpu(pb, mode=mode)
+        assert res["status"] == 0
+        assert_attention_close(pb, res, mode)
+
+
+@pytest.mark.parametrize("gq", [1, 8])
+def test_query_heads_split_merge(gq):
+    """Units cut by CTA ranges merge correctly with 1 and 8 query heads per KV head."""
+    w = synth.shrink(synth.WORKLOADS["tiny"], batch=2, num_kv_heads=2, num_q_heads=gq * 2, bits=4, k_scheme=1,
+                     v_scheme=0, max_seq_len=2048)
+    pb = make_problem(w, seed=400 + gq, lens=[2048, 1500])
+    for num_ctas in (3, 7):
+        res = run_gpu(pb, mode=1, num_ctas=num_ctas)
+        assert res["status"] == 0
+        assert_attention_close(pb, res, 1)
+
+
 @pytest.mark.parametrize("num_ctas", [1, 2, 3, 5, 8, 17])
 def test_split_ranges_merge(num_ctas):
     """Tile ranges cut (sequence, head) units in many places; merges must agree."""

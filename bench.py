@@ -163,7 +163,7 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
     import bit_quantized_kv_decode_gb300 as kvq
     c = build_cache(w, seed, dev, k_scheme, v_scheme)
     desc = c["desc"]
-    ad = kvq.attn_desc(desc, w.batch, c["max_blocks"])
+    ad = kvq.attn_desc(desc, w.batch, c["max_blocks"], num_q_heads=w.num_q_heads)
     ws = torch.empty(kvq.workspace_size(ad), dtype=torch.uint8, device=dev)
     out = torch.empty(w.batch, w.num_q_heads, 128, dtype=torch.float32, device=dev)
     lse = torch.empty(w.batch, w.num_q_heads, dtype=torch.float32, device=dev)
@@ -385,6 +385,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch (smaller cases for profiler captures)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--q-per-kv", type=int, choices=(1, 2, 4, 8), default=None,
+                    help="query heads per KV head (the workloads use 4); 8 reads every KV block twice")
     ap.add_argument("--operands", choices=("fp8", "bf16"), default="fp8",
                     help="tensor-core operand mode: fp8 (default) or the bf16 mode")
     args = ap.parse_args()
@@ -392,6 +394,8 @@ def main():
     w = synth.WORKLOADS[args.workload]
     if args.batch is not None:
         w = synth.shrink(w, batch=args.batch, name=f"{w.name}_b{args.batch}")
+    if args.q_per_kv is not None and args.q_per_kv * w.num_kv_heads != w.num_q_heads:
+        w = synth.shrink(w, num_q_heads=args.q_per_kv * w.num_kv_heads, name=f"{w.name}_g{args.q_per_kv}")
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -410,7 +414,7 @@ def main():
     ms = max_over_ranks(res["ms"], world, dev)
     e2e_ms = max_over_ranks(res["e2e_ms"], world, dev) if "e2e_ms" in res else float("nan")
     extra = []
-    if not args.no_extra and w.name == DEFAULT_WORKLOAD and args.batch is None:
+    if not args.no_extra and w.name == DEFAULT_WORKLOAD:
         w2 = synth.WORKLOADS["b128_l32k_int2"]
         for ks, vs in ((1, 0), (0, 0), (0, 1), (1, 1)):
             r2 = measure_kvq(w2, args.seed + rank, max(20, args.steps // 4), args.warmup, dev, ks, vs, e2e=False,

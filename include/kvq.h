@@ -194,7 +194,9 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* 
  * each 128-token group's partial product by s and adds z * sum(p) of that
  * group ([SUM] 限界と未検証の範囲: per-group application).  Work is split
  * over persistent CTAs in equal tile ranges; a sequence/head cut between
- * CTAs is merged on the device by log-sum-exp.
+ * CTAs is merged on the device by log-sum-exp.  Query heads per KV head:
+ * 1, 2, 4 or 8 (a work unit takes up to 4 query heads of one KV head, so
+ * with 8 each KV block is read twice).
  *   q        bf16 [batch][num_q_heads][128]
  *   k_codes, v_codes, k_scale, k_zero, v_scale, v_zero: cache arrays
  *   seq_lens int32 [batch], each in [0, max_blocks*128]
@@ -222,7 +224,8 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
  * fixed 4 MiB device array owned by the library, held on every device that
  * loads the library until the process exits.  Returns KVQ_ERR_WORKSPACE when
  * a call needs more scratch than that (batch * num_kv_heads * 4 bytes of
- * counters plus 4 KiB per CTA); kvq_decode_attn with a caller workspace then
+ * counters, twice that with 8 query heads per KV head, plus 4 KiB per CTA);
+ * kvq_decode_attn with a caller workspace then
  * remains available.  The first call on each device looks up the array's
  * address once (this may load the module): make it before any stream
  * capture.  Every call on a device shares the array and the counters are

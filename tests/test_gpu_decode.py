@@ -67,6 +67,24 @@ def test_query_heads_split_merge(gq):
         assert_attention_close(pb, res, 1)
 
 
+@pytest.mark.parametrize("bits,kcw,vcw", [(4, 1, 0), (2, 0, 1)])
+def test_maximum_batch(bits, kcw, vcw):
+    """The largest batch a call takes (1024 sequences), ragged 0..300 tokens
+    with empty ones: every sequence checked against the oracle."""
+    B = 1024
+    lens = np.random.default_rng(500 + bits).integers(0, 301, size=B)
+    lens[::97] = 0
+    w = synth.shrink(synth.WORKLOADS["tiny"], batch=B, num_kv_heads=1, num_q_heads=4, bits=bits, k_scheme=kcw,
+                     v_scheme=vcw, max_seq_len=300)
+    pb = make_problem(w, seed=600 + bits, lens=lens.tolist())
+    for mode in (0, 1):
+        res = run_gpu(pb, mode=mode)
+        assert res["status"] == 0
+        empty = np.flatnonzero(lens == 0)
+        assert np.all(res["out"][empty] == 0) and np.all(np.isneginf(res["lse"][empty]))
+        assert_attention_close(pb, res, mode)
+
+
 @pytest.mark.parametrize("num_ctas", [1, 2, 3, 5, 8, 17])
 def test_split_ranges_merge(num_ctas):
     """Tile ranges cut (sequence, head) units in many places; merges must agree."""

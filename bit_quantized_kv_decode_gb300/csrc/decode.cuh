@@ -186,16 +186,17 @@ __device__ __forceinline__ uint4 split2_bf16(float4 v) {
   return r;
 }
 
-// Power of two 2^k with m * 2^k in [128, 256) (1 for m == 0 or non-normal).
+// Power of two 2^k with m * 2^k in [128, 256); 1 when m < 2^-120 (the
+// factor would leave the fp32 exponent range) or m is non-finite.
 __device__ __forceinline__ float pow2_prescale(float m) {
   int e = (int)((__float_as_uint(m) >> 23) & 0xffu);
-  if (e == 0 || e == 0xff) return 1.0f;
+  if (e < 7 || e == 0xff) return 1.0f;
   return __uint_as_float((uint32_t)(261 - e) << 23);  // 2^(7 - (e - 127))
 }
 // 1 / pow2_prescale(m), exactly (no division).
 __device__ __forceinline__ float pow2_prescale_inv(float m) {
   int e = (int)((__float_as_uint(m) >> 23) & 0xffu);
-  if (e == 0 || e == 0xff) return 1.0f;
+  if (e < 7 || e == 0xff) return 1.0f;
   return __uint_as_float((uint32_t)(e - 7) << 23);  // 2^((e - 127) - 7)
 }
 
@@ -314,6 +315,9 @@ template <int BITS, bool BF16>
 struct alignas(16) DecodeBarriers {
   using C = DecodeCfg<BITS, BF16>;
   uint64_t stg_full[C::kStages], stg_empty[C::kStages];
+  // *_empty of the A buffers, Q' slots and P' slots are committed only by
+  // kernels that do not wait on the product's own full barrier instead (see
+  // kLeanCommits in decode_kernel)
   uint64_t ak_full[C::kNAK], ak_empty[C::kNAK], av_full[C::kNAV], av_empty[C::kNAV];
   uint64_t q_full[2], q_empty[2];
   uint64_t s_full[C::kSlots], s_empty[C::kSlots], p_full[C::kSlots], p_empty[C::kSlots];
@@ -608,6 +612,11 @@ template <int BITS, bool KCW, bool VCW, bool BF16, bool GQ4>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeParams p) {
   using C = DecodeCfg<BITS, BF16>;
   using Bars = DecodeBarriers<BITS, BF16>;
+  // Lean commits: each product commits only its full barrier (S or O slot)
+  // and the buffers it read are reused on that phase.  Measured faster with
+  // token-wise K (INT2: +6% K-tw/V-tw, +2% K-tw/V-cw) and slower with
+  // channel-wise K (-3%), which keeps the separate release barriers.
+  constexpr bool kLeanCommits = !KCW;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* stages = smem_raw;
   unsigned char* qop = stages + (size_t)C::kStages * C::kStageBytes;  // [2][kBBytes]
@@ -772,8 +781,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
               uint32_t d = tmem + C::kColO + 16 * sl, av = tmem + C::kColAV + a * C::kACols + 8 * k;
               if (BF16) mma_f16_ts(d, av, bd, C::kIdesc, k > 0); else mma_f8f6f4_ts(d, av, bd, C::kIdesc, k > 0);
             }
-            tc_commit(&sh.av_empty[a]);
-            tc_commit(&sh.p_empty[sl]);
+            if (!kLeanCommits) {
+              tc_commit(&sh.av_empty[a]);
+              tc_commit(&sh.p_empty[sl]);
+            }
             tc_commit(&sh.o_full[sl]);
             KVQ_TR(17, np)
             ++np;
@@ -793,8 +804,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
               uint32_t d = tmem + C::kColS + 16 * sl, ak = tmem + C::kColAK + a * C::kACols + 8 * k;
               if (BF16) mma_f16_ts(d, ak, bd, C::kIdesc, k > 0); else mma_f8f6f4_ts(d, ak, bd, C::kIdesc, k > 0);
             }
-            tc_commit(&sh.ak_empty[a]);
-            tc_commit(&sh.q_empty[q2]);
+            if (!kLeanCommits) {
+              tc_commit(&sh.ak_empty[a]);
+              tc_commit(&sh.q_empty[q2]);
+            }
             tc_commit(&sh.s_full[sl]);
             KVQ_TR(16, nq)
             ++nq;
@@ -851,14 +864,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       }
     };
 
-    // stage wait, Q' operand and K codes of tile t (it = tile t)
+    // stage wait, Q' operand and K codes of tile t (it = tile t).  A_K[a] and
+    // Q' slot t & 1 are free once QK^T(t - kNAK) has completed; with lean
+    // commits that is the phase of its S slot (kNAK <= 2, and the products
+    // complete in issue order).
     auto k_part = [&](int t) -> bool {
       const int s = t % C::kStages, a = t % C::kNAK, sl = t & 1;
       const uint32_t ps = (uint32_t)(t / C::kStages) & 1u, pa = (uint32_t)(t / C::kNAK) & 1u,
                      p2 = (uint32_t)(t >> 1) & 1u;
+      const int tp = t - C::kNAK;
       KVQ_PT(c0)
-      if (!warp_wait4<true>(&sh.stg_full[s], ps, &sh.q_empty[sl], p2 ^ 1u, &sh.ak_empty[a], pa ^ 1u, &sh.ak_empty[a], pa ^ 1u,
-                      abort_flag, limit))
+      if (kLeanCommits ? (tp < 0 ? !warp_wait<true>(&sh.stg_full[s], ps, abort_flag, limit)
+                                 : !warp_wait2<true>(&sh.stg_full[s], ps, &sh.s_full[tp % C::kSlots],
+                                                     (uint32_t)(tp / C::kSlots) & 1u, abort_flag, limit))
+                       : !warp_wait4<true>(&sh.stg_full[s], ps, &sh.q_empty[sl], p2 ^ 1u, &sh.ak_empty[a], pa ^ 1u,
+                                           &sh.ak_empty[a], pa ^ 1u, abort_flag, limit))
         return false;
       KVQ_PA(1, c0)
       const unsigned char* st = stages + (size_t)s * C::kStageBytes;
@@ -900,12 +920,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       return true;
     };
 
-    // V codes of tile t -> A_V[a] (row r = channel r); releases the stage
+    // V codes of tile t -> A_V[a] (row r = channel r); releases the stage.
+    // A_V[a] is free once PV(t - kNAV) has completed (lean commits: the phase
+    // of its O slot).
     auto v_part = [&](int t) -> bool {
       const int s = t % C::kStages, a = t % C::kNAV;
       const uint32_t pa = (uint32_t)(t / C::kNAV) & 1u;
+      const int tp = t - C::kNAV;
       KVQ_PT(c5)
-      if (!warp_wait<true>(&sh.av_empty[a], pa ^ 1u, abort_flag, limit)) return false;
+      if (kLeanCommits ? (tp >= 0 && !warp_wait<true>(&sh.o_full[tp % C::kSlots], (uint32_t)(tp / C::kSlots) & 1u,
+                                                      abort_flag, limit))
+                       : !warp_wait<true>(&sh.av_empty[a], pa ^ 1u, abort_flag, limit))
+        return false;
       KVQ_PA(6, c5)
       KVQ_PT(c6)
       convert_rows(stages + (size_t)s * C::kStageBytes + C::kBlockBytes, tmem + lane_off + C::kColAV + a * C::kACols);
@@ -1271,9 +1297,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       // Channel-wise K with token-wise V: the pair's P' buffers are awaited
       // with the round's barrier (one barrier round trip less; measured +1%
       // there, -1% for the other scheme pairs, which wait after the update)
+      // (with lean commits the P' slot of tile t is free at the previous
+      // phase of its O slot: PV(t - kSlots) has completed; on a fresh barrier
+      // that phase reads as complete)
       constexpr bool kPWaitInRound = KCW && !VCW;
       const uint32_t pe0 = ((uint32_t)(t / C::kSlots) & 1u) ^ 1u, pe1 = ((uint32_t)(t1 / C::kSlots) & 1u) ^ 1u;
-      if (!(kPWaitInRound ? round(vals, res, kUsed, KCW, cgp, &sh.p_empty[q0], pe0, &sh.p_empty[q1], pe1)
+      uint64_t* const pb0 = kLeanCommits ? &sh.o_full[q0] : &sh.p_empty[q0];
+      uint64_t* const pb1 = kLeanCommits ? &sh.o_full[q1] : &sh.p_empty[q1];
+      if (!(kPWaitInRound ? round(vals, res, kUsed, KCW, cgp, pb0, pe0, pb1, pe1)
                           : round(vals, res, kUsed, KCW, cgp))) {
         ok = false;
         break;
@@ -1303,7 +1334,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       }
       // P' operands (lane i = token i): token-wise V folds s into P; both
       // buffers are awaited first so the two rows are built together
-      if (!kPWaitInRound && !warp_wait2<true>(&sh.p_empty[q0], pe0, &sh.p_empty[q1], pe1, abort_flag, limit)) {
+      if (!kPWaitInRound && !warp_wait2<true>(pb0, pe0, pb1, pe1, abort_flag, limit)) {
         ok = false;
         break;
       }

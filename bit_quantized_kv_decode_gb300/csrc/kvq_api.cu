@@ -27,6 +27,8 @@ kvq_status check_cache(const kvq_cache_desc* c) {
   return KVQ_OK;
 }
 
+}  // namespace
+
 // Checks the current device without launching anything.
 kvq_status check_device(int* sm_count) {
   int dev = 0;
@@ -45,6 +47,8 @@ kvq_status check_device(int* sm_count) {
   }
   return KVQ_OK;
 }
+
+namespace {
 
 struct WorkspaceLayout {
   size_t counters, part_lse, part_o, total;

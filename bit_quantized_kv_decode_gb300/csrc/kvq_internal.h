@@ -80,6 +80,10 @@ struct DecodeParams {
   unsigned long long* prof;  // cycle counters [grid][32] in profiling builds, else null
 };
 
+// KVQ_OK when the current device is an sm_103 GPU (and its SM count in
+// *sm_count when non-null), else KVQ_ERR_DEVICE; launches nothing.
+kvq_status check_device(int* sm_count);
+
 size_t pack_smem_bytes();
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 cudaError_t launch_append(const PackParams& p, cudaStream_t stream);

@@ -226,11 +226,14 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
  * a call needs more scratch than that (batch * num_kv_heads * 4 bytes of
  * counters, twice that with 8 query heads per KV head, plus 4 KiB per CTA);
  * kvq_decode_attn with a caller workspace then
- * remains available.  The first call on each device looks up the array's
- * address once (this may load the module): make it before any stream
- * capture.  Every call on a device shares the array and the counters are
- * cleared on the stream at each call, so calls whose kernels may overlap on
- * the GPU (unordered streams) race.  Allocates nothing.
+ * remains available.  Every call on a stream that is not being captured
+ * looks up the array's address on the current device (the first such call
+ * loads the module); a call inside a stream capture reuses the address of
+ * the last uncaptured call on that device, so make one ordinary call on each
+ * device before any capture, and again after a device reset.  Every call on a
+ * device shares the array and the counters are cleared on the stream at each
+ * call, so calls whose kernels may overlap on the GPU (unordered streams)
+ * race.  Allocates nothing.
  */
 KVQ_API kvq_status kvq_decode_attn_static(const kvq_attn_desc* desc, const uint16_t* q, const uint8_t* k_codes,
                                           const uint16_t* k_scale, const uint16_t* k_zero, const uint8_t* v_codes,

@@ -29,7 +29,11 @@ class Problem:
     ref: dict                           # oracle results
 
 
-def make_problem(w: synth.Workload, seed: int, lens=None, paged: Optional[bool] = None) -> Problem:
+def make_problem(w: synth.Workload, seed: int, lens=None, paged: Optional[bool] = None, q=None, k=None, v=None,
+                 sm_scale: Optional[float] = None) -> Problem:
+    """A seeded problem of workload w and the oracle's results for it.  q, k
+    and v replace the synthetic values when given (bf16 [B, Hq, D] and fp32
+    [B, Hkv, L, D] CPU tensors); sm_scale=None is the default 1/sqrt(D)."""
     lens_t = torch.tensor(lens, dtype=torch.int32) if lens is not None else synth.seq_lens_for(w, seed)
     L = max(1, int(lens_t.max()))
     max_blocks = (L + 127) // 128
@@ -39,16 +43,18 @@ def make_problem(w: synth.Workload, seed: int, lens=None, paged: Optional[bool] 
         num_pages = max(num_pages, 1)
     else:
         pt, num_pages = None, w.batch * max_blocks
-    q = synth.query(w, seed)
-    k = synth.kv_full(w, seed, 0, lens_t)
-    v = synth.kv_full(w, seed, 1, lens_t)
+    q = synth.query(w, seed) if q is None else q
+    k = synth.kv_full(w, seed, 0, lens_t) if k is None else k
+    v = synth.kv_full(w, seed, 1, lens_t) if v is None else v
     if k.shape[2] < L:  # all-empty batch
         k = torch.zeros(w.batch, w.num_kv_heads, L, w.head_dim)
         v = torch.zeros_like(k)
     qb = q.view(torch.int16).numpy().view(np.uint16)
     ref = orc.reference_decode(qb, k.numpy(), v.numpy(), lens_t.numpy(), w.bits, w.k_scheme, w.v_scheme,
-                               None if pt is None else pt.numpy(), num_pages)
-    return Problem(w, seed, lens_t, q, k, v, pt, num_pages, max_blocks, ref)
+                               None if pt is None else pt.numpy(), num_pages, sm_scale=sm_scale)
+    pb = Problem(w, seed, lens_t, q, k, v, pt, num_pages, max_blocks, ref)
+    pb.sm_scale = 0.0 if sm_scale is None else float(sm_scale)
+    return pb
 
 
 def run_gpu(pb: Problem, mode: int = 0, num_ctas: int = 0, flags: int = 0):
@@ -62,7 +68,8 @@ def run_gpu(pb: Problem, mode: int = 0, num_ctas: int = 0, flags: int = 0):
     kc = kvq.pack(desc, 0, pb.k.to(dev), lens, pt, pb.max_blocks, dev_status=status)
     vc = kvq.pack(desc, 1, pb.v.to(dev), lens, pt, pb.max_blocks, dev_status=status)
     out, lse = kvq.decode_attn(desc, pb.q.to(dev), kc, vc, lens, pt, pb.max_blocks, mode=mode,
-                               num_ctas=num_ctas, dev_status=status, flags=flags)
+                               sm_scale=getattr(pb, "sm_scale", 0.0), num_ctas=num_ctas, dev_status=status,
+                               flags=flags)
     torch.cuda.synchronize()
     return dict(out=out.cpu().double().numpy(), lse=lse.cpu().double().numpy(), k_cache=kc, v_cache=vc,
                 status=int(status.item()), desc=desc)

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import kvq_synth as synth
-from tests.kvq_testlib import TOL, LSE_TOL, make_problem, run_gpu
+from tests.kvq_testlib import LSE_TOL, TOL, assert_attention_close, make_problem, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -47,8 +47,11 @@ def test_static_scratch_matches_workspace_entry_point_twice():
         assert int(st.item()) == 0
         o = out.cpu().double()
         l_ = lse.cpu().double()
+        # against the workspace entry point ...
         assert float((o - ref_o).abs().max()) <= TOL[0] * rms
         assert float((l_ - ref_l).abs().max()) <= LSE_TOL[0]
+        # ... and against the oracle, element by element
+        assert_attention_close(pb, {"out": o.numpy(), "lse": l_.numpy()}, 0)
 
 
 def test_static_scratch_rejects_oversized_calls():

@@ -248,6 +248,17 @@ __device__ __forceinline__ float p_inverse(uint32_t packed, int k, int code_log2
   return __uint_as_float((uint32_t)(121 + code_log2 + p_exp_of(packed, k)) << 23);
 }
 
+// Packed pairs of fp32 values (two heads at once): one sm_100-family
+// instruction per pair instead of two, with the same IEEE round-to-nearest
+// results as the scalar operations.
+__device__ __forceinline__ float2 f2u(uint32_t a, uint32_t b) {
+  return make_float2(__uint_as_float(a), __uint_as_float(b));
+}
+__device__ __forceinline__ float2 f2s(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
 // 2^x (hardware approximation, flush-to-zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -1075,18 +1086,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       }
       { KVQ_TR(12 + sw, tA) if (pend_n > 1) KVQ_TR(12 + sw, tB) }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float o[2];
+      for (int k = 0; k < 4; k += 2) {  // heads k, k + 1
+        const float2 pinv = make_float2(p_inverse(pexp_prev, k, kCodeLog2), p_inverse(pexp_prev, k + 1, kCodeLog2));
+        float2 o[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          o[u] = __uint_as_float(acc[u][k]) + __uint_as_float(acc[u][4 + k]);
-          if (!BF16) o[u] += __uint_as_float(acc[u][8 + k]);
-          o[u] *= p_inverse(pexp_prev, k, kCodeLog2);
+          o[u] = add2(f2u(acc[u][k], acc[u][k + 1]), f2u(acc[u][4 + k], acc[u][5 + k]));
+          if (!BF16) o[u] = add2(o[u], f2u(acc[u][8 + k], acc[u][9 + k]));
+          o[u] = mul2(o[u], pinv);
         }
-        if (pend_n < 2) o[1] = 0.f;
-        const float o_add = VCW ? fmaf(sv_prev[0], o[0], zv_prev[0] * ts[k]) + fmaf(sv_prev[1], o[1], zv_prev[1] * ts[4 + k])
-                                : o[0] + o[1];
-        O[k] = fmaf(O[k], a_prev[k], o_add);
+        if (pend_n < 2) o[1] = f2s(0.f);
+        const float2 o_add =
+            VCW ? add2(fma2(f2s(sv_prev[0]), o[0], mul2(f2s(zv_prev[0]), make_float2(ts[k], ts[k + 1]))),
+                       fma2(f2s(sv_prev[1]), o[1], mul2(f2s(zv_prev[1]), make_float2(ts[4 + k], ts[5 + k]))))
+                : add2(o[0], o[1]);
+        const float2 o2 = fma2(make_float2(O[k], O[k + 1]), make_float2(a_prev[k], a_prev[k + 1]), o_add);
+        O[k] = o2.x;
+        O[k + 1] = o2.y;
       }
       return true;
     };
@@ -1270,15 +1286,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const bool valid = u < n && i < len - (it.j + u) * kBlockTokens;
+        const float2 ks2 = f2s(ks_t[u]), kz2 = f2s(kz_t[u]), fs2 = f2s(fs_t[u]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float a = __uint_as_float(acc[u][k]) + __uint_as_float(acc[u][4 + k]);
-          if (!BF16) a += __uint_as_float(acc[u][8 + k]);
+        for (int k = 0; k < 4; k += 2) {  // heads k, k + 1
+          float2 a = add2(f2u(acc[u][k], acc[u][k + 1]), f2u(acc[u][4 + k], acc[u][5 + k]));
+          if (!BF16) a = add2(a, f2u(acc[u][8 + k], acc[u][9 + k]));
           // channel-wise K adds q . z_g once reduced over channels
-          const float v = KCW ? a * (add[k] * fs_t[u]) : fmaf(a * mult[k], ks_t[u], kz_t[u] * add[k]);
-          sc[4 * u + k] = valid ? v : -INFINITY;
+          const float2 addk = make_float2(add[k], add[k + 1]);
+          const float2 v = KCW ? mul2(a, mul2(addk, fs2))
+                               : fma2(mul2(a, make_float2(mult[k], mult[k + 1])), ks2, mul2(kz2, addk));
+          sc[4 * u + k] = valid ? v.x : -INFINITY;
+          sc[4 * u + k + 1] = valid ? v.y : -INFINITY;
           if (KCW) {  // the tile's offset q . z_g is still to come: per-tile maxima
             vals[kTM + 4 * u + k] = warp_max_redux(sc[4 * u + k]);
+            vals[kTM + 4 * u + k + 1] = warp_max_redux(sc[4 * u + k + 1]);
           }
         }
       }
@@ -1319,18 +1340,39 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       float pr[8], alpha[4];
       const int e_v = VCW ? 0 : (int)((__float_as_uint(res[kVM]) >> 23) & 0xffu) - 127;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float cg0 = KCW ? res[kCG + k] * p.sm_scale_log2 : 0.f;
-        const float cg1 = KCW ? res[kCG + 4 + k] * p.sm_scale_log2 : 0.f;
-        const float mt = KCW ? fmaxf(res[kTM + k] + cg0, res[kTM + 4 + k] + cg1) : res[kTM + k];
-        const float mn = fmaxf(m[k], mt);
-        pexp |= ((uint32_t)(BF16 ? 6 : p_exponent(mt - mn, e_v)) & 0xffu) << (8 * k);
-        alpha[k] = ex2(m[k] - mn);
-        m[k] = mn;
-        pr[k] = ex2(sc[k] + cg0 - mn);
-        pr[4 + k] = ex2(sc[4 + k] + cg1 - mn);
-        lp[k] = fmaf(lp[k], alpha[k], pr[k] + pr[4 + k]);
-        if (!VCW) zp[k] = fmaf(zp[k], alpha[k], fmaf(pr[k], vz_t[0], pr[4 + k] * vz_t[1]));
+      for (int k = 0; k < 4; k += 2) {  // heads k, k + 1
+        const float2 cg0 = KCW ? mul2(make_float2(res[kCG + k], res[kCG + k + 1]), f2s(p.sm_scale_log2)) : f2s(0.f);
+        const float2 cg1 =
+            KCW ? mul2(make_float2(res[kCG + 4 + k], res[kCG + 5 + k]), f2s(p.sm_scale_log2)) : f2s(0.f);
+        float2 mn;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float c0 = h ? cg0.y : cg0.x, c1 = h ? cg1.y : cg1.x;
+          const float mt = KCW ? fmaxf(res[kTM + k + h] + c0, res[kTM + 4 + k + h] + c1) : res[kTM + k + h];
+          const float mnh = fmaxf(m[k + h], mt);
+          pexp |= ((uint32_t)(BF16 ? 6 : p_exponent(mt - mnh, e_v)) & 0xffu) << (8 * (k + h));
+          alpha[k + h] = ex2(m[k + h] - mnh);
+          m[k + h] = mnh;
+          if (h) mn.y = mnh; else mn.x = mnh;
+        }
+        const float2 nmn = make_float2(-mn.x, -mn.y);
+        const float2 x0 = KCW ? add2(add2(make_float2(sc[k], sc[k + 1]), cg0), nmn) : add2(make_float2(sc[k], sc[k + 1]), nmn);
+        const float2 x1 =
+            KCW ? add2(add2(make_float2(sc[4 + k], sc[5 + k]), cg1), nmn) : add2(make_float2(sc[4 + k], sc[5 + k]), nmn);
+        pr[k] = ex2(x0.x);
+        pr[k + 1] = ex2(x0.y);
+        pr[4 + k] = ex2(x1.x);
+        pr[5 + k] = ex2(x1.y);
+        const float2 p0 = make_float2(pr[k], pr[k + 1]), p1 = make_float2(pr[4 + k], pr[5 + k]);
+        const float2 al = make_float2(alpha[k], alpha[k + 1]);
+        const float2 l2 = fma2(make_float2(lp[k], lp[k + 1]), al, add2(p0, p1));
+        lp[k] = l2.x;
+        lp[k + 1] = l2.y;
+        if (!VCW) {
+          const float2 z2 = fma2(make_float2(zp[k], zp[k + 1]), al, fma2(p0, f2s(vz_t[0]), mul2(p1, f2s(vz_t[1]))));
+          zp[k] = z2.x;
+          zp[k + 1] = z2.y;
+        }
       }
       // P' operands (lane i = token i): token-wise V folds s into P; both
       // buffers are awaited first so the two rows are built together
@@ -1346,9 +1388,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         uint4 bytes[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const float f = (VCW ? 1.0f : vs_t[u]) * odd_quarter<BITS, BF16>(i);
-          const float4 pv = make_float4(pr[4 * u] * (f * psc[0]), pr[4 * u + 1] * (f * psc[1]),
-                                        pr[4 * u + 2] * (f * psc[2]), pr[4 * u + 3] * (f * psc[3]));
+          const float2 f = f2s((VCW ? 1.0f : vs_t[u]) * odd_quarter<BITS, BF16>(i));
+          const float2 lo = mul2(make_float2(pr[4 * u], pr[4 * u + 1]), mul2(f, make_float2(psc[0], psc[1])));
+          const float2 hi = mul2(make_float2(pr[4 * u + 2], pr[4 * u + 3]), mul2(f, make_float2(psc[2], psc[3])));
+          const float4 pv = make_float4(lo.x, lo.y, hi.x, hi.y);
           bytes[u] = BF16 ? split2_bf16(pv) : split3_e4m3_via_f16(pv);
         }
         *reinterpret_cast<uint4*>(pop + q0 * C::kBBytes + b_row_off<BF16>(prow)) = bytes[0];

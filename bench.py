@@ -170,7 +170,7 @@ def rotation_sets(w, seed) -> int:
     return 1 if per_step > L2_BYTES else max(8, -(-2 * L2_BYTES // per_step))
 
 
-def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=True, mode=0, sets=None):
+def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=True, mode=0, sets=None, flags=0):
     import bit_quantized_kv_decode_gb300 as kvq
     sets = rotation_sets(w, seed) if sets is None else sets
     # every copy holds the same inputs (the same seed): only the addresses differ
@@ -189,7 +189,7 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
         ci = cs[turn[0] % sets]
         turn[0] += 1
         kvq.decode_attn(desc, ci["q"], ci["k"], ci["v"], ci["lens"], ci["pt"], ci["max_blocks"], mode=mode, out=out,
-                        lse=lse, workspace=ws, dev_status=status)
+                        lse=lse, workspace=ws, dev_status=status, flags=flags)
 
     t_wall0 = time.time()
     ms, per = time_steps(step, steps, warmup, stream)
@@ -456,6 +456,15 @@ def main():
             extra.append({"workload": w2.name, "k_scheme": SCHEME_NAMES[ks], "v_scheme": SCHEME_NAMES[vs],
                           "ms_per_step": ms2, "GB/s": r2["bytes"] / (ms2 / 1e3) / 1e9,
                           "latency_us": ms2 * 1e3})
+    e2m1 = []  # the 2-bit sweep again with the V codes placed as E2M1 in shared memory
+    if not args.no_extra and w.name == DEFAULT_WORKLOAD and mode == 0:
+        w2 = synth.WORKLOADS["b128_l32k_int2"]
+        for ks, vs in ((1, 0), (0, 0), (0, 1), (1, 1)):
+            r2 = measure_kvq(w2, args.seed + rank, 20, args.warmup, dev, ks, vs, e2e=False, flags=kvq.FLAG_E2M1_V)
+            ms2 = max_over_ranks(r2["ms"], world, dev)
+            e2m1.append({"workload": w2.name, "k_scheme": SCHEME_NAMES[ks], "v_scheme": SCHEME_NAMES[vs],
+                         "v_operand": "E2M1 (code / 2) in shared memory", "ms_per_step": ms2,
+                         "GB/s": r2["bytes"] / (ms2 / 1e3) / 1e9, "latency_us": ms2 * 1e3})
     configs = []
     if not args.no_extra and w.name == DEFAULT_WORKLOAD:
         for name in ("b8_l4k_int2", "paged_ragged_int2"):
@@ -480,7 +489,7 @@ def main():
     total_bytes = res["bytes"] * world
     value = total_bytes / (ms / 1e3) / 1e9
     achieved = res["bytes"] / (ms / 1e3) / 1e9
-    for e in extra + configs:
+    for e in extra + configs + e2m1:
         e["frac_of_peak"] = e["GB/s"] / peak
     line = {
         "metric": "effective KV-access HBM GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
@@ -501,6 +510,7 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": clk,
         "int2_sweep": extra,
+        "int2_sweep_e2m1_v": e2m1,
         "other_configs": configs,
     }
     if not args.no_cpu_baseline and world == 1:

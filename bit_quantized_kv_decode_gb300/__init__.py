@@ -13,7 +13,7 @@ from typing import Optional, Tuple
 import torch
 
 from . import _lib
-from ._lib import (CHANNELWISE, DEV_BAD_PAGE, DEV_BAD_SEQ_LEN, DEV_NONFINITE, DEV_TIMEOUT, FLAG_TEST_STALL,
+from ._lib import (CHANNELWISE, DEV_BAD_PAGE, DEV_BAD_SEQ_LEN, DEV_NONFINITE, DEV_TIMEOUT, FLAG_E2M1_V, FLAG_TEST_STALL,
                    OPERANDS_BF16, OPERANDS_FP8, TOKENWISE, AttnDesc, CacheDesc, KvqError)
 
 BLOCK_TOKENS = 128
@@ -21,7 +21,7 @@ HEAD_DIM = 128
 GROUP_Q = 4
 
 __all__ = ["CacheDesc", "AttnDesc", "KvqError", "TOKENWISE", "CHANNELWISE", "OPERANDS_FP8", "OPERANDS_BF16",
-           "DEV_BAD_SEQ_LEN", "DEV_BAD_PAGE", "DEV_NONFINITE", "DEV_TIMEOUT", "FLAG_TEST_STALL", "cache_desc",
+           "DEV_BAD_SEQ_LEN", "DEV_BAD_PAGE", "DEV_NONFINITE", "DEV_TIMEOUT", "FLAG_TEST_STALL", "FLAG_E2M1_V", "cache_desc",
            "attn_desc", "cache_bytes", "block_bytes", "alloc_cache", "pack", "append", "dequant", "workspace_size",
            "decode_attn", "decode_attn_static", "merge", "library"]
 

@@ -20,6 +20,7 @@ CHANNELWISE = 1
 OPERANDS_FP8 = 0
 OPERANDS_BF16 = 1
 FLAG_TEST_STALL = 0x1
+FLAG_E2M1_V = 0x2
 
 # Every symbol include/kvq.h declares.
 EXPORTS = ("kvq_status_string", "kvq_version", "kvq_cache_bytes", "kvq_pack", "kvq_append", "kvq_dequant",

@@ -82,11 +82,16 @@ constexpr int kRegsLaunch = 80, kRegsLight = 24, kRegsSoftmax = 112, kRegsConver
 static_assert(128 * kRegsConvert + 128 * kRegsSoftmax + 128 * kRegsLight == kDecodeThreads * kRegsLaunch,
               "setmaxnreg split must add up to the launch allocation");
 
-template <int BITS, bool BF16>
+// E2V: 2-bit V codes as E2M1 values (code / 2) in shared memory (the
+// KVQ_FLAG_E2M1_V placement); otherwise codes are E4M3 bytes in tensor memory.
+template <int BITS, bool BF16, bool E2V = false>
 struct DecodeCfg {
   static constexpr int kBlockBytes = kBlockTokens * kHeadDim * BITS / 8;  // 8192 / 4096
   static constexpr int kChunks = kHeadDim * BITS / 8 / 16;                // 16-byte chunks per row
-  static constexpr int kStages = (BITS == 4) ? 4 : 6;
+  static constexpr bool kE2V = E2V;
+  static_assert(!E2V || (BITS == 2 && !BF16), "E2M1 placement: 2-bit codes, FP8 operands");
+  // (four stages with the E2M1 tiles: two CTAs per SM must still fit)
+  static constexpr int kStages = (BITS == 4) ? 4 : (E2V ? 4 : 6);
   static constexpr int kSzBytes = kBlockTokens * 2;                       // one fp16 [128] array
   static constexpr int kStageBytes = 2 * kBlockBytes + 4 * kSzBytes;
   static constexpr int kACols = BF16 ? 64 : 32;  // tensor-memory columns of one 128 x 128 A tile
@@ -105,15 +110,25 @@ struct DecodeCfg {
   static constexpr int kColS = kColAV + kNAV * kACols;
   static constexpr int kColO = kColS + 16 * kSlots;
   static constexpr int kTmemCols = 256;
-  static constexpr float kCodeInv = BF16 ? 1.0f : 512.0f;  // code = operand value * kCodeInv
+  // code = operand value * code scale (E4M3: code * 2^-9; E2M1: code / 2)
+  static constexpr float kCodeInv = BF16 ? 1.0f : 512.0f;  // K: code = operand value * 2^9
+  static constexpr int kVCodeLog2 = BF16 ? 0 : (E2V ? 1 : 9);
+  static constexpr uint32_t kIdescV = E2V ? make_idesc(5, 0, 0, 1, 128, 16) : kIdesc;  // A = E2M1, B = E4M3
+  // E2M1 tiles in shared memory: canonical K-major layout without swizzle;
+  // a 16-byte unit holds 16 codes of one row as packed nibbles (8 bytes) and
+  // 8 bytes of padding; K-groups of 16 codes kALbo apart, 8-row groups kASbo
+  static constexpr uint32_t kALbo = 2048, kASbo = 128;
+  static constexpr int kASmBytes = 16384;  // one 128 x 128 tile
+  static constexpr int kASmTiles = E2V ? kNAV : 0;
   static_assert(kColO + 16 * kSlots <= kTmemCols, "tensor memory budget");
 };
 
 // Position of element e (channel of a K row, token of a V row) along the
 // contraction dimension of the A operand, i.e. where the converter's masks
 // put it.  The B operand rows (Q' channels, P' tokens) use the same order.
-template <int BITS, bool BF16>
+template <int BITS, bool BF16, bool E2 = false>
 __device__ __forceinline__ int a_pos(int e) {
+  if (E2) return (e & ~15) + ((e & 1) << 3) + ((e & 15) >> 1);  // even codes, then odd codes
   if (!BF16) {
     if (BITS == 4) return (e & ~7) + ((e & 1) << 2) + ((e & 7) >> 1);
     return (e & ~15) + ((e & 3) << 2) + ((e & 15) >> 2);
@@ -140,9 +155,9 @@ __device__ __forceinline__ uint32_t b_row_off(int p) {
 
 // B-operand row factor matching Convert: 2-bit codes at odd positions e are
 // stored as 4 * code, so their Q' / P' rows are scaled by 1/4 (exact).
-template <int BITS, bool BF16>
+template <int BITS, bool BF16, bool E2 = false>
 __device__ __forceinline__ float odd_quarter(int e) {
-  return (BITS == 2 && !BF16 && (e & 1)) ? 0.25f : 1.0f;
+  return (BITS == 2 && !BF16 && !E2 && (e & 1)) ? 0.25f : 1.0f;
 }
 
 // ---------------------------------------------------------------- operands
@@ -322,9 +337,9 @@ struct Convert {
 };
 
 // ------------------------------------------------------------ shared state
-template <int BITS, bool BF16>
+template <int BITS, bool BF16, bool E2V>
 struct alignas(16) DecodeBarriers {
-  using C = DecodeCfg<BITS, BF16>;
+  using C = DecodeCfg<BITS, BF16, E2V>;
   uint64_t stg_full[C::kStages], stg_empty[C::kStages];
   // *_empty of the A buffers, Q' slots and P' slots are committed only by
   // kernels that do not wait on the product's own full barrier instead (see
@@ -347,11 +362,11 @@ struct alignas(16) DecodeBarriers {
 #endif
 };
 
-template <int BITS, bool BF16>
+template <int BITS, bool BF16, bool E2V>
 constexpr size_t decode_smem_layout_bytes() {
-  using C = DecodeCfg<BITS, BF16>;
+  using C = DecodeCfg<BITS, BF16, E2V>;
   size_t b = (size_t)C::kStages * C::kStageBytes + (2 + C::kSlots) * (size_t)C::kBBytes +
-             sizeof(DecodeBarriers<BITS, BF16>) +
+             (size_t)C::kASmTiles * C::kASmBytes + sizeof(DecodeBarriers<BITS, BF16, E2V>) +
              (2 * kMaxBatch + 1) * sizeof(int) + 1024;
   return b < 80 * 1024 ? 80 * 1024 : b;  // >= 80 KB keeps at most two CTAs per SM
 }
@@ -596,8 +611,7 @@ struct SegConsts {
 };
 template <bool KCW, bool BF16>
 static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* qb, int rows, int i,
-                                                               float sm_scale_log2) {
-  using C = DecodeCfg<4, BF16>;  // the code scale does not depend on the bit width
+                                                               float sm_scale_log2, float code_inv) {
   float qmax[4], qsum[4];
   unit_q_stats<4>(qb, rows, !KCW, qmax, qsum);
   SegConsts c;
@@ -606,10 +620,10 @@ static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* 
     if (KCW) {
       c.qi[k] = bf2f(qb[(k < rows ? k : 0) * kHeadDim + i]) * (k < rows ? 1.0f : 0.0f);
       c.mult[k] = 0.f;
-      c.add[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_head_inv(qmax[k])) * sm_scale_log2;
+      c.add[k] = code_inv * (BF16 ? 1.0f : pow2_head_inv(qmax[k])) * sm_scale_log2;
     } else {
       c.qi[k] = 0.f;
-      c.mult[k] = C::kCodeInv * (BF16 ? 1.0f : pow2_prescale_inv(qmax[k])) * sm_scale_log2;
+      c.mult[k] = code_inv * (BF16 ? 1.0f : pow2_prescale_inv(qmax[k])) * sm_scale_log2;
       c.add[k] = qsum[k] * sm_scale_log2;
     }
   }
@@ -619,10 +633,10 @@ static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* 
 // ================================================================= kernel
 // GQ4: exactly 4 query heads per KV head (one unit per KV head, no empty
 // head slots); the other groupings (1, 2, 8) take the run-time values in p.
-template <int BITS, bool KCW, bool VCW, bool BF16, bool GQ4>
+template <int BITS, bool KCW, bool VCW, bool BF16, bool GQ4, bool E2V>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeParams p) {
-  using C = DecodeCfg<BITS, BF16>;
-  using Bars = DecodeBarriers<BITS, BF16>;
+  using C = DecodeCfg<BITS, BF16, E2V>;
+  using Bars = DecodeBarriers<BITS, BF16, E2V>;
   // Lean commits: each product commits only its full barrier (S or O slot)
   // and the buffers it read are reused on that phase.  Measured faster with
   // token-wise K (INT2: +6% K-tw/V-tw, +2% K-tw/V-cw) and slower with
@@ -632,7 +646,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   unsigned char* stages = smem_raw;
   unsigned char* qop = stages + (size_t)C::kStages * C::kStageBytes;  // [2][kBBytes]
   unsigned char* pop = qop + 2 * C::kBBytes;                          // [kSlots][kBBytes]
-  Bars& sh = *reinterpret_cast<Bars*>(pop + C::kSlots * C::kBBytes);
+  unsigned char* asm_tiles = pop + C::kSlots * C::kBBytes;             // [kASmTiles][kASmBytes] E2M1 codes
+  Bars& sh = *reinterpret_cast<Bars*>(asm_tiles + C::kASmTiles * C::kASmBytes);
   int* prefix = reinterpret_cast<int*>(&sh + 1);  // [B + 1] tile offsets
   int* lens = prefix + (kMaxBatch + 1);           // [B] validated sequence lengths
 
@@ -678,7 +693,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     lens[b] = len;
   }
   // operand columns nobody writes (N = 12..15, or 8..15 for BF16) stay zero
-  for (int i = tid; i < (2 + C::kSlots) * C::kBBytes / 16; i += kDecodeThreads)
+  // (and the padding half of every E2M1 unit, which the converters never write)
+  for (int i = tid; i < ((2 + C::kSlots) * C::kBBytes + C::kASmTiles * C::kASmBytes) / 16; i += kDecodeThreads)
     reinterpret_cast<uint4*>(qop)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (warp == kWarpMma) { tmem_alloc(&sh.tmem_base, C::kTmemCols); tmem_relinquish(); }
   __syncthreads();
@@ -790,7 +806,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             for (int k = 0; k < C::kKSteps; ++k) {
               uint64_t bd = make_smem_desc(b0 + k * C::kKStepBBytes, C::kLbo, C::kSbo);
               uint32_t d = tmem + C::kColO + 16 * sl, av = tmem + C::kColAV + a * C::kACols + 8 * k;
-              if (BF16) mma_f16_ts(d, av, bd, C::kIdesc, k > 0); else mma_f8f6f4_ts(d, av, bd, C::kIdesc, k > 0);
+              if (C::kE2V)  // A = E2M1 tile in shared memory; K-step k = K-groups 2k, 2k + 1
+                mma_f8f6f4_ss(d, make_smem_desc(smem_u32(asm_tiles + a * C::kASmBytes) + 2 * k * C::kALbo, C::kALbo,
+                                                C::kASbo),
+                              bd, C::kIdescV, k > 0);
+              else if (BF16) mma_f16_ts(d, av, bd, C::kIdesc, k > 0);
+              else mma_f8f6f4_ts(d, av, bd, C::kIdesc, k > 0);
             }
             if (!kLeanCommits) {
               tc_commit(&sh.av_empty[a]);
@@ -813,7 +834,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             for (int k = 0; k < C::kKSteps; ++k) {
               uint64_t bd = make_smem_desc(b0 + k * C::kKStepBBytes, C::kLbo, C::kSbo);
               uint32_t d = tmem + C::kColS + 16 * sl, ak = tmem + C::kColAK + a * C::kACols + 8 * k;
-              if (BF16) mma_f16_ts(d, ak, bd, C::kIdesc, k > 0); else mma_f8f6f4_ts(d, ak, bd, C::kIdesc, k > 0);
+              if (BF16) mma_f16_ts(d, ak, bd, C::kIdesc, k > 0);
+              else mma_f8f6f4_ts(d, ak, bd, C::kIdesc, k > 0);
             }
             if (!kLeanCommits) {
               tc_commit(&sh.ak_empty[a]);
@@ -872,6 +894,23 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             Convert<BITS, BF16>::run(w[i], &o[(4 * c + i) * Convert<BITS, BF16>::kOut], p.nibble_mul, p.minus_one);
         }
         tmem_st_32x32b_x32(col + 32 * ps2, o);
+      }
+    };
+    // 2-bit codes of one packed row -> E2M1 (code / 2) nibbles in a shared-
+    // memory tile: per 32-bit word (16 codes) the even codes (x & 0x33333333)
+    // then the odd ones ((x >> 2) & 0x33333333), 3 operations per 16 codes
+    // (rag-lover.com summary of arXiv 2611.09722, "解説": 2-bit codes in the
+    // low bits of an E2M1 element read as q / 2).
+    auto convert_rows_e2m1 = [&](const unsigned char* blk, unsigned char* tile) {
+      unsigned char* row = tile + (r >> 3) * C::kASbo + (r & 7) * 16;
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(blk + ((size_t)c * kBlockTokens + r) * 16);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)  // K-group 4c + i holds codes 16 (4c + i) ... + 15
+          *reinterpret_cast<uint2*>(row + (4 * c + i) * C::kALbo) =
+              make_uint2(w[i] & 0x33333333u, (w[i] >> 2) & 0x33333333u);
       }
     };
 
@@ -945,9 +984,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         return false;
       KVQ_PA(6, c5)
       KVQ_PT(c6)
-      convert_rows(stages + (size_t)s * C::kStageBytes + C::kBlockBytes, tmem + lane_off + C::kColAV + a * C::kACols);
-      tc_wait_st();
-      tc_fence_before();
+      if (C::kE2V) {
+        convert_rows_e2m1(stages + (size_t)s * C::kStageBytes + C::kBlockBytes, asm_tiles + a * C::kASmBytes);
+        fence_proxy_async_smem();  // visible to the tensor core
+      } else {
+        convert_rows(stages + (size_t)s * C::kStageBytes + C::kBlockBytes, tmem + lane_off + C::kColAV + a * C::kACols);
+        tc_wait_st();
+        tc_fence_before();
+      }
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&sh.av_full[a]);
@@ -981,7 +1025,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     const int i = tid - kWarpSoftmax0 * 32;  // tensor-memory lane: token (scores) / channel (output)
     const int sw = warp - kWarpSoftmax0;     // warp = lane quarter
     const uint32_t lane_off = (uint32_t)(sw * 32) << 16;
-    const int prow = a_pos<BITS, BF16>(i);
+    const int prow = a_pos<BITS, BF16, C::kE2V>(i);
     uint32_t grp_phase = 0;
     const float kLn2 = 0.69314718055994530942f;
     const float kFix = 67108864.0f;  // 2^26: fixed-point scale of p for integer warp sums
@@ -1007,7 +1051,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     int pend = -1, pend_n = 0;
     float a_prev[4], ws_prev[8], sv_prev[2], zv_prev[2];
     uint32_t pexp_prev = 0u;  // P' prescale exponents E of the previous step, one signed byte per head
-    constexpr int kCodeLog2 = BF16 ? 0 : 9;  // log2 of the code scale
+    constexpr int kCodeLog2 = C::kVCodeLog2;  // log2 of the V code scale
     float qi[4], qmax[4], mult[4], add[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) { qi[k] = 0.f; qmax[k] = 0.f; mult[k] = 0.f; add[k] = 0.f; a_prev[k] = 0.f; }
@@ -1220,7 +1264,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       if (seg_first) {
         pb = it.b; ph = it.h; pfirst = ustart >= g0; pus = ustart; pue = uend;
         const SegConsts sc4 = softmax_unit_consts<KCW, BF16>(
-            p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * gq) * kHeadDim, gq, i, p.sm_scale_log2);
+            p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * gq) * kHeadDim, gq, i, p.sm_scale_log2,
+            C::kCodeInv);
 #pragma unroll
         for (int k = 0; k < 4; ++k) { qi[k] = sc4.qi[k]; mult[k] = sc4.mult[k]; add[k] = sc4.add[k]; }
       }
@@ -1388,7 +1433,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         uint4 bytes[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const float2 f = f2s((VCW ? 1.0f : vs_t[u]) * odd_quarter<BITS, BF16>(i));
+          const float2 f = f2s((VCW ? 1.0f : vs_t[u]) * odd_quarter<BITS, BF16, C::kE2V>(i));
           const float2 lo = mul2(make_float2(pr[4 * u], pr[4 * u + 1]), mul2(f, make_float2(psc[0], psc[1])));
           const float2 hi = mul2(make_float2(pr[4 * u + 2], pr[4 * u + 3]), mul2(f, make_float2(psc[2], psc[3])));
           const float4 pv = make_float4(lo.x, lo.y, hi.x, hi.y);
@@ -1440,10 +1485,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   }
 }
 
-template <int BITS, bool KCW, bool VCW, bool BF16, bool GQ4>
+template <int BITS, bool KCW, bool VCW, bool BF16, bool GQ4, bool E2V = false>
 cudaError_t launch_decode_instance(const DecodeParams& p, cudaStream_t stream) {
-  constexpr size_t smem = decode_smem_layout_bytes<BITS, BF16>();
-  auto kern = decode_kernel<BITS, KCW, VCW, BF16, GQ4>;
+  constexpr size_t smem = decode_smem_layout_bytes<BITS, BF16, E2V>();
+  static_assert(smem <= 113 * 1024, "two CTAs per SM");
+  auto kern = decode_kernel<BITS, KCW, VCW, BF16, GQ4, E2V>;
   // The register split inside the kernel assumes exactly kRegsLaunch
   // registers per thread at launch; with fewer, the softmax warpgroup's
   // increase could never be granted.  Refuse to launch such a build.

@@ -87,7 +87,10 @@ kvq_status check_attn(const kvq_attn_desc* d) {
   if (d->batch > kMaxBatchDecode) return KVQ_ERR_UNSUPPORTED;
   if (heads_per_kv(d) == 0) return KVQ_ERR_UNSUPPORTED;  // 1, 2, 4 or 8 query heads per KV head
   if (d->operand_mode != KVQ_OPERANDS_FP8 && d->operand_mode != KVQ_OPERANDS_BF16) return KVQ_ERR_INVALID_ARG;
-  if (d->num_ctas < 0 || (d->flags & ~KVQ_FLAG_TEST_STALL) != 0) return KVQ_ERR_INVALID_ARG;
+  if (d->num_ctas < 0 || (d->flags & ~(KVQ_FLAG_TEST_STALL | KVQ_FLAG_E2M1_V)) != 0) return KVQ_ERR_INVALID_ARG;
+  if ((d->flags & KVQ_FLAG_E2M1_V) &&
+      (d->cache.bits != 2 || d->operand_mode != KVQ_OPERANDS_FP8 || heads_per_kv(d) != kGroupQ))
+    return KVQ_ERR_UNSUPPORTED;  // the E2M1 placement is built for these only
   if (!(std::isfinite(d->sm_scale))) return KVQ_ERR_INVALID_ARG;
   if ((long long)d->batch * units_per_seq(d) * d->max_blocks > (1LL << 30)) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;

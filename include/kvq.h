@@ -104,12 +104,21 @@ typedef struct kvq_attn_desc {
   int32_t operand_mode; /* kvq_operand_mode */
   float sm_scale;       /* <= 0 selects 1/sqrt(head_dim) */
   int32_t num_ctas;     /* persistent CTAs; 0 = two per SM */
-  uint32_t flags;       /* 0, or KVQ_FLAG_TEST_STALL */
+  uint32_t flags;       /* 0 or KVQ_FLAG_* bits */
 } kvq_attn_desc;
 
 /* Test hook: the loader withholds one tile so that every waiting stage runs
  * into its time limit; the call must end with KVQ_DEV_TIMEOUT set. */
 #define KVQ_FLAG_TEST_STALL 0x1u
+/* 2-bit caches: feed the V codes to the tensor cores as E2M1 values
+ * (code / 2, two 2-bit fields per nibble taken with one mask each) staged in
+ * shared memory -- the placement of the rag-lover.com summary of arXiv
+ * 2611.09722, section "解説" -- instead of the default E4M3 bytes
+ * (code * 2^-9) written to tensor memory.  Same results within the FP8
+ * tolerance; slower on GB300 (more shared-memory stores, fewer load stages).
+ * Requires bits = 2, KVQ_OPERANDS_FP8 and 4 query heads per KV head, else
+ * KVQ_ERR_UNSUPPORTED. */
+#define KVQ_FLAG_E2M1_V 0x2u
 
 /* Human-readable name of a status code (static storage). */
 KVQ_API const char* kvq_status_string(kvq_status status);

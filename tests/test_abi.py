@@ -86,6 +86,22 @@ def test_workspace_size_host_only(lib):
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
 
 
+def test_e2m1_flag_validation(lib):
+    """The E2M1 V placement is built for 2-bit caches, FP8 operands and 4
+    query heads per KV head; other combinations and unknown flag bits are
+    rejected on the host."""
+    n = ctypes.c_size_t()
+    ok = _lib.AttnDesc(_cache(2, 1, 0), 8, 32, 32, 0, 0.0, 304, _lib.FLAG_E2M1_V)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(ok), ctypes.byref(n)) == 0
+    for d in (_lib.AttnDesc(_cache(4, 1, 0), 8, 32, 32, 0, 0.0, 304, _lib.FLAG_E2M1_V),   # 4-bit codes
+              _lib.AttnDesc(_cache(2, 1, 0), 8, 32, 32, 1, 0.0, 304, _lib.FLAG_E2M1_V),   # BF16 operands
+              _lib.AttnDesc(_cache(2, 1, 0), 8, 64, 32, 0, 0.0, 304, _lib.FLAG_E2M1_V),   # 8 query heads per KV head
+              _lib.AttnDesc(_cache(2, 1, 0), 8, 16, 32, 0, 0.0, 304, _lib.FLAG_E2M1_V)):  # 2 query heads per KV head
+        assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 2
+    bad = _lib.AttnDesc(_cache(2, 1, 0), 8, 32, 32, 0, 0.0, 304, 0x4)  # unknown flag bit
+    assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
+
+
 def test_validation_precedes_device(lib):
     """Bad arguments are rejected on the host (no device needed)."""
     c = _cache(4)

@@ -40,6 +40,18 @@ def test_schemes_ragged(bits, kcw, vcw, mode):
     assert_attention_close(pb, res, mode)
 
 
+@pytest.mark.parametrize("kcw,vcw", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_e2m1_v_placement(kcw, vcw):
+    """2-bit V codes fed as E2M1 values from shared memory (KVQ_FLAG_E2M1_V)
+    on a ragged batch, whole units and units split over CTAs."""
+    import bit_quantized_kv_decode_gb300 as kvq
+    pb = make_problem(_w(2, kcw, vcw), seed=700 + 2 * kcw + vcw, lens=[1000, 129, 1])
+    for num_ctas in (0, 5):
+        res = run_gpu(pb, mode=0, num_ctas=num_ctas, flags=kvq.FLAG_E2M1_V)
+        assert res["status"] == 0
+        assert_attention_close(pb, res, 0)
+
+
 @pytest.mark.parametrize("gq", [1, 2, 8])
 @pytest.mark.parametrize("kcw,vcw", [(0, 0), (0, 1), (1, 0), (1, 1)])
 def test_query_heads_per_kv_head(gq, kcw, vcw):

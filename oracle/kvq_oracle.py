@@ -31,11 +31,14 @@ lost in the [NEWS] extraction):
     q = clamp(rint_half_even(fp32(fp32(x - z) / s)), 0, 2^b - 1), every step
     an IEEE fp32 operation (no fused multiply-add); a group whose max equals z
     gets s = 0 and q = 0 (x_hat = z);
-  * groups: token-wise = the 128 channels of one token of one KV head;
-    channel-wise = 128 consecutive tokens (one 128-token block, aligned to
-    token 0) of one channel of one KV head; a block's tokens at or past the
-    sequence length are excluded from min/max and get code 0 (token-wise:
-    s = z = 0 as well);
+  * groups of G elements (G = 128 by default; [SUM] 使える条件 names 128,
+    [SUM] 限界と未検証の範囲 says results depend on the group size):
+    token-wise = G consecutive channels of one token of one KV head (G divides
+    the head dim D); channel-wise = G consecutive tokens of one channel of one
+    KV head, aligned to token 0 (G divides the 128-token block); a block's
+    tokens at or past the sequence length are excluded from min/max and get
+    code 0 (token-wise: s = z = 0 as well; a channel-wise group with no valid
+    token: s = z = 0);
   * GQA: query head h reads KV head h // (Hq / Hkv);
   * scores S_l = sm_scale * q . x_hat_K[l], sm_scale = 1/sqrt(D) by default;
     lse = natural-log sum of exp(S_l); an empty sequence gives out = 0,
@@ -49,8 +52,8 @@ import math
 import numpy as np
 
 BLOCK_TOKENS = 128  # tokens per block (= page); also the channel-wise group
-HEAD_DIM = 128
-GROUP = 128
+HEAD_DIM = 128  # default head dim; 64 and 256 are also covered
+GROUP = 128     # default group size; 32 and 64 are also covered
 TOKENWISE = 0
 CHANNELWISE = 1
 K_CACHE = 0
@@ -144,36 +147,54 @@ def num_blocks(n_tokens):
     return (int(n_tokens) + BLOCK_TOKENS - 1) // BLOCK_TOKENS
 
 
-def quantize_sequence(x_seq, bits, scheme):
+def check_geometry(head_dim, group):
+    if head_dim not in (64, 128, 256) or group not in (32, 64, 128) or group > head_dim:
+        raise OracleError("head_dim must be 64, 128 or 256 and the group 32, 64 or 128 (at most head_dim)")
+
+
+def sz_per_block(head_dim, group):
+    """s (or z) values per 128-token block of one KV head: 128 * D / G."""
+    return BLOCK_TOKENS * head_dim // group
+
+
+def quantize_sequence(x_seq, bits, scheme, group=GROUP):
     """Quantize the valid tokens of one (sequence, KV head).
 
     x_seq: fp32 [n, D] holding exactly the valid tokens.
     Returns codes uint8 [nblk, 128 tokens, D channels] and s, z fp16
-    [nblk, 128]: indexed by token within the block (token-wise) or by channel
-    (channel-wise).
+    [nblk, 128 * D / G]: token-wise, entry t * (D / G) + g belongs to channels
+    [g G, (g + 1) G) of block token t; channel-wise, entry k * D + c belongs
+    to channel c over block tokens [k G, (k + 1) G).  (G = D = 128: one entry
+    per token, resp. per channel.)
     """
     x_seq = np.asarray(x_seq, dtype=np.float32)
     n, d = x_seq.shape
-    if d != HEAD_DIM:
-        raise OracleError("head_dim must be 128")
+    check_geometry(d, group)
     nblk = num_blocks(n)
-    codes = np.zeros((nblk, BLOCK_TOKENS, HEAD_DIM), np.uint8)
-    s = np.zeros((nblk, BLOCK_TOKENS), np.float16)
-    z = np.zeros((nblk, BLOCK_TOKENS), np.float16)
-    if scheme == TOKENWISE:  # one group = the 128 channels of one token
-        ct, st, zt = quantize_groups(x_seq, bits)
+    codes = np.zeros((nblk, BLOCK_TOKENS, d), np.uint8)
+    if scheme == TOKENWISE:  # one group = G consecutive channels of one token
+        gpt = d // group
+        ct, st, zt = quantize_groups(x_seq.reshape(n * gpt, group), bits)
         pad = nblk * BLOCK_TOKENS - n
-        codes[:] = np.concatenate([ct, np.zeros((pad, d), np.uint8)]).reshape(nblk, BLOCK_TOKENS, d)
-        s[:] = np.concatenate([st, np.zeros(pad, np.float16)]).reshape(nblk, BLOCK_TOKENS)
-        z[:] = np.concatenate([zt, np.zeros(pad, np.float16)]).reshape(nblk, BLOCK_TOKENS)
-    elif scheme == CHANNELWISE:  # one group = one channel over a block's valid tokens
+        codes[:] = np.concatenate([ct.reshape(n, d), np.zeros((pad, d), np.uint8)]).reshape(nblk, BLOCK_TOKENS, d)
+        s = np.concatenate([st.reshape(n, gpt), np.zeros((pad, gpt), np.float16)]).reshape(nblk, -1)
+        z = np.concatenate([zt.reshape(n, gpt), np.zeros((pad, gpt), np.float16)]).reshape(nblk, -1)
+    elif scheme == CHANNELWISE:  # one group = one channel over G consecutive valid tokens
+        gpb = BLOCK_TOKENS // group
+        s = np.zeros((nblk, gpb, d), np.float16)
+        z = np.zeros((nblk, gpb, d), np.float16)
         for j in range(nblk):
-            t0 = j * BLOCK_TOKENS
-            nv = min(BLOCK_TOKENS, n - t0)
-            cc, sc, zc = quantize_groups(x_seq[t0:t0 + nv].T, bits)
-            codes[j, :nv] = cc.T
-            s[j] = sc
-            z[j] = zc
+            for k in range(gpb):
+                t0 = j * BLOCK_TOKENS + k * group
+                nv = min(group, n - t0)
+                if nv <= 0:
+                    continue
+                cc, sc, zc = quantize_groups(x_seq[t0:t0 + nv].T, bits)
+                codes[j, k * group:k * group + nv] = cc.T
+                s[j, k] = sc
+                z[j, k] = zc
+        s = s.reshape(nblk, -1)
+        z = z.reshape(nblk, -1)
     else:
         raise OracleError("unknown scheme")
     return codes, s, z
@@ -183,9 +204,9 @@ def quantize_sequence(x_seq, bits, scheme):
 # Packed block layout
 # ---------------------------------------------------------------------------
 
-def block_bytes(bits):
-    """Bytes of one packed 128 x 128 code block."""
-    return BLOCK_TOKENS * HEAD_DIM * bits // 8
+def block_bytes(bits, head_dim=HEAD_DIM):
+    """Bytes of one packed block: 128 tokens x D channels of b-bit codes."""
+    return BLOCK_TOKENS * head_dim * bits // 8
 
 
 def block_rows(codes_tc, which):
@@ -239,25 +260,26 @@ def page_of(b, j, max_blocks, page_table):
 # Whole cache
 # ---------------------------------------------------------------------------
 
-def pack_cache(x, seq_lens, bits, scheme, which, page_table=None, num_pages=None):
+def pack_cache(x, seq_lens, bits, scheme, which, page_table=None, num_pages=None, group=GROUP):
     """Quantize and pack K or V for a batch.
 
     x: fp32 [B, Hkv, Lcap, D]; only tokens < seq_lens[b] are read.
     Cache arrays: codes uint8 [num_pages, Hkv, block_bytes], s and z fp16
-    [num_pages, Hkv, 128].  Pages not covered by a sequence stay zero.
+    [num_pages, Hkv, 128 * D / G].  Pages not covered by a sequence stay zero.
     """
     x = np.asarray(x, dtype=np.float32)
     B, Hkv, Lcap, D = x.shape
     max_blocks = num_blocks(Lcap) if page_table is None else page_table.shape[1]
     if num_pages is None:
         num_pages = B * max_blocks if page_table is None else int(np.max(page_table)) + 1
-    codes = np.zeros((num_pages, Hkv, block_bytes(bits)), np.uint8)
-    s = np.zeros((num_pages, Hkv, BLOCK_TOKENS), np.float16)
-    z = np.zeros((num_pages, Hkv, BLOCK_TOKENS), np.float16)
+    check_geometry(D, group)
+    codes = np.zeros((num_pages, Hkv, block_bytes(bits, D)), np.uint8)
+    s = np.zeros((num_pages, Hkv, sz_per_block(D, group)), np.float16)
+    z = np.zeros((num_pages, Hkv, sz_per_block(D, group)), np.float16)
     for b in range(B):
         n = int(seq_lens[b])
         for h in range(Hkv):
-            c, sb, zb = quantize_sequence(x[b, h, :n], bits, scheme)
+            c, sb, zb = quantize_sequence(x[b, h, :n], bits, scheme, group)
             for j in range(c.shape[0]):
                 p = page_of(b, j, max_blocks, page_table)
                 codes[p, h] = pack_rows(block_rows(c[j], which), bits)
@@ -270,25 +292,41 @@ def unpack_cache(codes, s, z, seq_lens, bits, which, Lcap, page_table=None):
     """Logical view of a packed cache.
 
     Returns codes uint8 [B, Hkv, Lcap, D] (token, channel) and s, z fp16
-    [B, Hkv, nblk, 128] per block (token- or channel-indexed as stored).
+    [B, Hkv, nblk, 128 * D / G] per block, laid out as stored (see
+    quantize_sequence).  D follows from the block size, G from the s arrays.
     """
     B = len(seq_lens)
     Hkv = codes.shape[1]
+    D = codes.shape[2] * 8 // (BLOCK_TOKENS * bits)
     max_blocks = num_blocks(Lcap) if page_table is None else page_table.shape[1]
     nblk = num_blocks(Lcap)
-    out_c = np.zeros((B, Hkv, nblk * BLOCK_TOKENS, HEAD_DIM), np.uint8)
-    out_s = np.zeros((B, Hkv, nblk, BLOCK_TOKENS), np.float16)
-    out_z = np.zeros((B, Hkv, nblk, BLOCK_TOKENS), np.float16)
+    out_c = np.zeros((B, Hkv, nblk * BLOCK_TOKENS, D), np.uint8)
+    out_s = np.zeros((B, Hkv, nblk, s.shape[2]), np.float16)
+    out_z = np.zeros((B, Hkv, nblk, s.shape[2]), np.float16)
     for b in range(B):
         for j in range(num_blocks(seq_lens[b])):
             p = page_of(b, j, max_blocks, page_table)
             for h in range(Hkv):
-                rows = unpack_rows(codes[p, h], bits)
+                rows = unpack_rows(codes[p, h], bits, BLOCK_TOKENS if which == K_CACHE else D,
+                                   D if which == K_CACHE else BLOCK_TOKENS)
                 tc = rows if which == K_CACHE else rows.T
                 out_c[b, h, j * BLOCK_TOKENS:(j + 1) * BLOCK_TOKENS] = tc
                 out_s[b, h, j] = s[p, h]
                 out_z[b, h, j] = z[p, h]
     return out_c[:, :, :Lcap], out_s, out_z
+
+
+def expand_sz(s_blk, scheme, head_dim, nv):
+    """Per-element view [Hkv, nv, D] of one block's s (or z) values
+    [Hkv, 128 * D / G] for its first nv tokens."""
+    s_blk = np.asarray(s_blk, np.float64)
+    Hkv, m = s_blk.shape
+    group = BLOCK_TOKENS * head_dim // m
+    if scheme == TOKENWISE:   # [token][channel group]
+        per = s_blk.reshape(Hkv, BLOCK_TOKENS, head_dim // group)
+        return np.repeat(per, group, axis=2)[:, :nv]
+    per = s_blk.reshape(Hkv, BLOCK_TOKENS // group, head_dim)  # [token group][channel]
+    return np.repeat(per, group, axis=1)[:, :nv]
 
 
 def dequantize(codes_tc, s, z, seq_lens, scheme):
@@ -301,12 +339,8 @@ def dequantize(codes_tc, s, z, seq_lens, scheme):
         for j in range(num_blocks(n)):
             l0, l1 = j * BLOCK_TOKENS, min(n, (j + 1) * BLOCK_TOKENS)
             c = codes_tc[b, :, l0:l1].astype(np.float64)           # [Hkv, nv, D]
-            if scheme == TOKENWISE:   # s, z indexed by token
-                sv = s[b, :, j, :l1 - l0].astype(np.float64)[:, :, None]
-                zv = z[b, :, j, :l1 - l0].astype(np.float64)[:, :, None]
-            else:                     # s, z indexed by channel
-                sv = s[b, :, j].astype(np.float64)[:, None, :]
-                zv = z[b, :, j].astype(np.float64)[:, None, :]
+            sv = expand_sz(s[b, :, j], scheme, D, l1 - l0)
+            zv = expand_sz(z[b, :, j], scheme, D, l1 - l0)
             xh[b, :, l0:l1] = sv * c + zv
     return xh
 
@@ -352,21 +386,26 @@ def attend_folded(q, kc, ks, kz, vc, vs, vz, seq_lens, k_scheme, v_scheme, sm_sc
     """The folded formulation on integer codes, fp64.
 
     QK^T contracts over channels ([SUM] 解説): token-wise K folds on the
-    accumulator (scale the partial q.code by s_l, add z_l * sum(q)); channel-
-    wise K folds on the operand (q * s_g, then add q . z_g).  PV contracts over
-    tokens: token-wise V folds on the operand P (p_l * s_l, plus the scalar
-    sum_l p_l z_l); channel-wise V folds on the accumulator, one quantization
-    group at a time (s_g * (p_g @ code_g) + z_g * sum(p_g)) because partial
-    products across group boundaries cannot be accumulated unscaled
-    ([SUM] 限界と未検証の範囲).  [ABS] states the result equals the dequantized
-    attention in exact arithmetic.
+    accumulator (scale the partial q.code of each channel group by its s,
+    add z * sum(q) over the group); channel-wise K folds on the operand
+    (q * s_g, then add q . z_g, for the tokens of group g).  PV contracts over
+    tokens: token-wise V folds on the operand P (p_l * s_l, plus sum_l p_l z_l,
+    for the channels of each group); channel-wise V folds on the accumulator,
+    one token group at a time (s_g * (p_g @ code_g) + z_g * sum(p_g)) because
+    partial products across group boundaries cannot be accumulated unscaled
+    ([SUM] 限界と未検証の範囲: accumulator folds are applied per quantization
+    group).  [ABS] states the result equals the dequantized attention in
+    exact arithmetic.
 
-    kc, vc: logical codes [B, Hkv, Lcap, D]; ks/kz/vs/vz: [B, Hkv, nblk, 128].
+    kc, vc: logical codes [B, Hkv, Lcap, D]; ks/kz/vs/vz: [B, Hkv, nblk,
+    128 * D / G] as stored (see quantize_sequence); G follows from their size.
     """
     q = np.asarray(q, np.float64)
     B, Hq, D = q.shape
     Hkv = kc.shape[1]
     G = Hq // Hkv
+    gk = BLOCK_TOKENS * D // ks.shape[3]   # group size of K
+    gv = BLOCK_TOKENS * D // vs.shape[3]   # group size of V
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     out = np.zeros((B, Hq, D), np.float64)
@@ -382,16 +421,25 @@ def attend_folded(q, kc, ks, kz, vc, vs, vz, seq_lens, k_scheme, v_scheme, sm_sc
             S = np.zeros(n, np.float64)
             for j in range(nblk):
                 l0, l1 = j * BLOCK_TOKENS, min(n, (j + 1) * BLOCK_TOKENS)
-                codes = kc[b, kv, l0:l1].astype(np.float64)
-                if k_scheme == TOKENWISE:
-                    s_l = ks[b, kv, j, :l1 - l0].astype(np.float64)
-                    z_l = kz[b, kv, j, :l1 - l0].astype(np.float64)
-                    acc = codes @ qh                      # partial q . code
-                    S[l0:l1] = s_l * acc + z_l * qh.sum()  # accumulator fold
-                else:
-                    q_fold = qh * ks[b, kv, j].astype(np.float64)  # operand fold
-                    c_g = qh @ kz[b, kv, j].astype(np.float64)
-                    S[l0:l1] = codes @ q_fold + c_g
+                codes = kc[b, kv, l0:l1].astype(np.float64)          # [nv, D]
+                sb = ks[b, kv, j].astype(np.float64)
+                zb = kz[b, kv, j].astype(np.float64)
+                if k_scheme == TOKENWISE:   # channel groups: [token][group]
+                    s_tg = sb.reshape(BLOCK_TOKENS, D // gk)[:l1 - l0]
+                    z_tg = zb.reshape(BLOCK_TOKENS, D // gk)[:l1 - l0]
+                    for g in range(D // gk):
+                        ch = slice(g * gk, (g + 1) * gk)
+                        acc = codes[:, ch] @ qh[ch]                   # partial q . code of group g
+                        S[l0:l1] += s_tg[:, g] * acc + z_tg[:, g] * qh[ch].sum()  # accumulator fold
+                else:                       # token groups: [group][channel]
+                    s_gc = sb.reshape(BLOCK_TOKENS // gk, D)
+                    z_gc = zb.reshape(BLOCK_TOKENS // gk, D)
+                    for g in range(BLOCK_TOKENS // gk):
+                        t0, t1 = g * gk, min(l1 - l0, (g + 1) * gk)
+                        if t0 >= t1:
+                            continue
+                        q_fold = qh * s_gc[g]                          # operand fold
+                        S[l0 + t0:l0 + t1] = codes[t0:t1] @ q_fold + qh @ z_gc[g]
             S *= sm_scale
             m = S.max()
             p = np.exp(S - m)
@@ -401,14 +449,23 @@ def attend_folded(q, kc, ks, kz, vc, vs, vz, seq_lens, k_scheme, v_scheme, sm_sc
                 l0, l1 = j * BLOCK_TOKENS, min(n, (j + 1) * BLOCK_TOKENS)
                 codes = vc[b, kv, l0:l1].astype(np.float64)
                 pg = p[l0:l1]
-                if v_scheme == TOKENWISE:
-                    s_l = vs[b, kv, j, :l1 - l0].astype(np.float64)
-                    z_l = vz[b, kv, j, :l1 - l0].astype(np.float64)
-                    acc_o += (pg * s_l) @ codes + pg @ z_l  # operand fold on P
-                else:
-                    s_g = vs[b, kv, j].astype(np.float64)
-                    z_g = vz[b, kv, j].astype(np.float64)
-                    acc_o += s_g * (pg @ codes) + z_g * pg.sum()  # per-group accumulator fold
+                sb = vs[b, kv, j].astype(np.float64)
+                zb = vz[b, kv, j].astype(np.float64)
+                if v_scheme == TOKENWISE:   # channel groups: [token][group]
+                    s_tg = sb.reshape(BLOCK_TOKENS, D // gv)[:l1 - l0]
+                    z_tg = zb.reshape(BLOCK_TOKENS, D // gv)[:l1 - l0]
+                    for g in range(D // gv):
+                        ch = slice(g * gv, (g + 1) * gv)
+                        acc_o[ch] += (pg * s_tg[:, g]) @ codes[:, ch] + pg @ z_tg[:, g]  # operand fold on P
+                else:                       # token groups: [group][channel]
+                    s_gc = sb.reshape(BLOCK_TOKENS // gv, D)
+                    z_gc = zb.reshape(BLOCK_TOKENS // gv, D)
+                    for g in range(BLOCK_TOKENS // gv):
+                        t0, t1 = g * gv, min(l1 - l0, (g + 1) * gv)
+                        if t0 >= t1:
+                            continue
+                        pk = pg[t0:t1]
+                        acc_o += s_gc[g] * (pk @ codes[t0:t1]) + z_gc[g] * pk.sum()  # per-group accumulator fold
             out[b, h] = acc_o / den
             lse[b, h] = m + math.log(den)
     return out, lse
@@ -446,13 +503,13 @@ def merge(o_parts, lse_parts):
 # ---------------------------------------------------------------------------
 
 def reference_decode(q_bits, k, v, seq_lens, bits, k_scheme, v_scheme,
-                     page_table=None, num_pages=None, sm_scale=None):
-    """End to end on the CPU: pack K and V, read the packed cache back, and
-    attend over the dequantized cache.  Returns a dict with the packed arrays
-    and out/lse."""
+                     page_table=None, num_pages=None, sm_scale=None, group=GROUP):
+    """End to end on the CPU: pack K and V (groups of G elements), read the
+    packed cache back, and attend over the dequantized cache.  Returns a dict
+    with the packed arrays and out/lse."""
     B, Hkv, Lcap, D = k.shape
-    kcodes, ks, kz = pack_cache(k, seq_lens, bits, k_scheme, K_CACHE, page_table, num_pages)
-    vcodes, vs, vz = pack_cache(v, seq_lens, bits, v_scheme, V_CACHE, page_table, num_pages)
+    kcodes, ks, kz = pack_cache(k, seq_lens, bits, k_scheme, K_CACHE, page_table, num_pages, group)
+    vcodes, vs, vz = pack_cache(v, seq_lens, bits, v_scheme, V_CACHE, page_table, num_pages, group)
     kc, kss, kzz = unpack_cache(kcodes, ks, kz, seq_lens, bits, K_CACHE, Lcap, page_table)
     vc, vss, vzz = unpack_cache(vcodes, vs, vz, seq_lens, bits, V_CACHE, Lcap, page_table)
     khat = dequantize(kc, kss, kzz, seq_lens, k_scheme)

@@ -22,7 +22,7 @@ GROUP_Q = 4
 
 __all__ = ["CacheDesc", "AttnDesc", "KvqError", "TOKENWISE", "CHANNELWISE", "OPERANDS_FP8", "OPERANDS_BF16",
            "DEV_BAD_SEQ_LEN", "DEV_BAD_PAGE", "DEV_NONFINITE", "DEV_TIMEOUT", "FLAG_TEST_STALL", "FLAG_E2M1_V", "cache_desc",
-           "attn_desc", "cache_bytes", "block_bytes", "alloc_cache", "pack", "append", "dequant", "workspace_size",
+           "attn_desc", "cache_bytes", "block_bytes", "sz_per_block", "alloc_cache", "pack", "append", "dequant", "workspace_size",
            "decode_attn", "decode_attn_static", "merge", "library"]
 
 
@@ -50,8 +50,8 @@ def _need(t: torch.Tensor, name: str, dtype=None, numel=None):
 
 
 def cache_desc(bits: int, k_scheme: int, v_scheme: int, num_kv_heads: int, num_pages: int,
-               head_dim: int = HEAD_DIM) -> CacheDesc:
-    return CacheDesc(bits, k_scheme, v_scheme, head_dim, num_kv_heads, num_pages)
+               head_dim: int = HEAD_DIM, group: int = 128) -> CacheDesc:
+    return CacheDesc(bits, k_scheme, v_scheme, head_dim, num_kv_heads, num_pages, group)
 
 
 def attn_desc(cache: CacheDesc, batch: int, max_blocks: int, mode: int = OPERANDS_FP8, sm_scale: float = 0.0,
@@ -60,8 +60,13 @@ def attn_desc(cache: CacheDesc, batch: int, max_blocks: int, mode: int = OPERAND
     return AttnDesc(cache, batch, hq, max_blocks, mode, sm_scale, num_ctas, flags)
 
 
-def block_bytes(bits: int) -> int:
-    return BLOCK_TOKENS * HEAD_DIM * bits // 8
+def block_bytes(bits: int, head_dim: int = HEAD_DIM) -> int:
+    return BLOCK_TOKENS * head_dim * bits // 8
+
+
+def sz_per_block(desc: CacheDesc) -> int:
+    """s (or z) values per page and KV head: 128 * head_dim / group."""
+    return BLOCK_TOKENS * desc.head_dim // (desc.group_size or 128)
 
 
 def cache_bytes(desc: CacheDesc) -> Tuple[int, int]:
@@ -73,9 +78,9 @@ def cache_bytes(desc: CacheDesc) -> Tuple[int, int]:
 def alloc_cache(desc: CacheDesc, device="cuda"):
     """Zeroed (codes, scale, zero) arrays for one K or V cache."""
     P, H = desc.num_pages, desc.num_kv_heads
-    codes = torch.zeros(P, H, block_bytes(desc.bits), dtype=torch.uint8, device=device)
-    scale = torch.zeros(P, H, BLOCK_TOKENS, dtype=torch.float16, device=device)
-    zero = torch.zeros(P, H, BLOCK_TOKENS, dtype=torch.float16, device=device)
+    codes = torch.zeros(P, H, block_bytes(desc.bits, desc.head_dim), dtype=torch.uint8, device=device)
+    scale = torch.zeros(P, H, sz_per_block(desc), dtype=torch.float16, device=device)
+    zero = torch.zeros(P, H, sz_per_block(desc), dtype=torch.float16, device=device)
     return codes, scale, zero
 
 
@@ -96,11 +101,11 @@ def _geometry(batch, max_seq_len, seq_lens, page_table, max_blocks):
 def pack(desc: CacheDesc, which: int, x: torch.Tensor, seq_lens: Optional[torch.Tensor] = None,
          page_table: Optional[torch.Tensor] = None, max_blocks: Optional[int] = None, cache=None,
          dev_status: Optional[torch.Tensor] = None):
-    """Quantize + pack fp32 x [B, Hkv, L, 128] into a K (which=0) or V (which=1)
-    cache; returns (codes, scale, zero)."""
+    """Quantize + pack fp32 x [B, Hkv, L, head_dim] into a K (which=0) or V
+    (which=1) cache; returns (codes, scale, zero)."""
     _need(x, "x", torch.float32)
-    if x.dim() != 4 or x.shape[1] != desc.num_kv_heads or x.shape[3] != HEAD_DIM:
-        raise ValueError("x must be fp32 [batch, num_kv_heads, max_seq_len, 128]")
+    if x.dim() != 4 or x.shape[1] != desc.num_kv_heads or x.shape[3] != desc.head_dim:
+        raise ValueError("x must be fp32 [batch, num_kv_heads, max_seq_len, head_dim]")
     B, _, L, _ = x.shape
     mb = _geometry(B, L, seq_lens, page_table, max_blocks)
     codes, scale, zero = cache if cache is not None else alloc_cache(desc, x.device)
@@ -125,11 +130,11 @@ def append(desc: CacheDesc, which: int, x_new: torch.Tensor, seq_lens: torch.Ten
     _need(x_new, "x_new", torch.float32)
     _need(window, "window", torch.float32)
     _need(seq_lens, "seq_lens", torch.int32)
-    if x_new.dim() != 3 or x_new.shape[1] != desc.num_kv_heads or x_new.shape[2] != HEAD_DIM:
-        raise ValueError("x_new must be fp32 [batch, num_kv_heads, 128]")
+    if x_new.dim() != 3 or x_new.shape[1] != desc.num_kv_heads or x_new.shape[2] != desc.head_dim:
+        raise ValueError("x_new must be fp32 [batch, num_kv_heads, head_dim]")
     B = x_new.shape[0]
-    if tuple(window.shape) != (B, desc.num_kv_heads, BLOCK_TOKENS, HEAD_DIM):
-        raise ValueError("window must be fp32 [batch, num_kv_heads, 128, 128]")
+    if tuple(window.shape) != (B, desc.num_kv_heads, BLOCK_TOKENS, desc.head_dim):
+        raise ValueError("window must be fp32 [batch, num_kv_heads, 128, head_dim]")
     if seq_lens.numel() != B:
         raise ValueError("seq_lens must hold one int32 per sequence")
     if page_table is not None:
@@ -154,7 +159,7 @@ def dequant(desc: CacheDesc, which: int, cache, batch: int, max_seq_len: int,
     """x_hat fp32 [B, Hkv, L, 128] read back from a packed cache."""
     codes, scale, zero = cache
     mb = _geometry(batch, max_seq_len, seq_lens, page_table, max_blocks)
-    out = torch.empty(batch, desc.num_kv_heads, max_seq_len, HEAD_DIM, dtype=torch.float32, device=codes.device)
+    out = torch.empty(batch, desc.num_kv_heads, max_seq_len, desc.head_dim, dtype=torch.float32, device=codes.device)
     st = library().kvq_dequant(ctypes.byref(desc), which, _p(codes), _p(scale), _p(zero), batch, max_seq_len,
                                _p(seq_lens), _p(page_table), mb, _p(out), _p(dev_status), _stream())
     _lib.check(st, "kvq_dequant")
@@ -175,8 +180,8 @@ def decode_attn(desc: CacheDesc, q: torch.Tensor, k_cache, v_cache, seq_lens: to
                 flags: int = 0):
     """out fp32 [B, Hq, 128] and lse fp32 [B, Hq] for bf16 q [B, Hq, 128]."""
     _need(q, "q", torch.bfloat16)
-    if q.dim() != 3 or q.shape[2] != HEAD_DIM:
-        raise ValueError("q must be bf16 [batch, num_q_heads, 128]")
+    if q.dim() != 3 or q.shape[2] != desc.head_dim:
+        raise ValueError("q must be bf16 [batch, num_q_heads, head_dim]")
     B, Hq, _ = q.shape
     if page_table is not None:
         mb = _geometry(B, 1, seq_lens, page_table, None)
@@ -187,10 +192,10 @@ def decode_attn(desc: CacheDesc, q: torch.Tensor, k_cache, v_cache, seq_lens: to
         _need(seq_lens, "seq_lens", torch.int32, B)
     ad = AttnDesc(desc, B, Hq, mb, mode, sm_scale, num_ctas, flags)
     if out is None:
-        out = torch.empty(B, Hq, HEAD_DIM, dtype=torch.float32, device=q.device)
+        out = torch.empty(B, Hq, desc.head_dim, dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
-    _need(out, "out", torch.float32, B * Hq * HEAD_DIM)
+    _need(out, "out", torch.float32, B * Hq * desc.head_dim)
     _need(lse, "lse", torch.float32, B * Hq)
     if workspace is None:
         workspace = torch.empty(workspace_size(ad), dtype=torch.uint8, device=q.device)
@@ -213,8 +218,8 @@ def decode_attn_static(desc: CacheDesc, q: torch.Tensor, k_cache, v_cache, seq_l
     kvq_decode_attn_static in include/kvq.h).  `out` and `lse` are still
     caller buffers; pass them preallocated to avoid any allocation here."""
     _need(q, "q", torch.bfloat16)
-    if q.dim() != 3 or q.shape[2] != HEAD_DIM:
-        raise ValueError("q must be bf16 [batch, num_q_heads, 128]")
+    if q.dim() != 3 or q.shape[2] != desc.head_dim:
+        raise ValueError("q must be bf16 [batch, num_q_heads, head_dim]")
     B, Hq, _ = q.shape
     if page_table is not None:
         mb = _geometry(B, 1, seq_lens, page_table, None)
@@ -225,10 +230,10 @@ def decode_attn_static(desc: CacheDesc, q: torch.Tensor, k_cache, v_cache, seq_l
         _need(seq_lens, "seq_lens", torch.int32, B)
     ad = AttnDesc(desc, B, Hq, mb, mode, sm_scale, num_ctas, 0)
     if out is None:
-        out = torch.empty(B, Hq, HEAD_DIM, dtype=torch.float32, device=q.device)
+        out = torch.empty(B, Hq, desc.head_dim, dtype=torch.float32, device=q.device)
     if lse is None:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
-    _need(out, "out", torch.float32, B * Hq * HEAD_DIM)
+    _need(out, "out", torch.float32, B * Hq * desc.head_dim)
     _need(lse, "lse", torch.float32, B * Hq)
     kc, ks, kz = k_cache
     vc, vs, vz = v_cache

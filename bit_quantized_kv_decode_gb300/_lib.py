@@ -29,7 +29,8 @@ EXPORTS = ("kvq_status_string", "kvq_version", "kvq_cache_bytes", "kvq_pack", "k
 
 class CacheDesc(ctypes.Structure):
     _fields_ = [("bits", ctypes.c_int32), ("k_scheme", ctypes.c_int32), ("v_scheme", ctypes.c_int32),
-                ("head_dim", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
+                ("head_dim", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+                ("group_size", ctypes.c_int32)]
 
 
 class AttnDesc(ctypes.Structure):

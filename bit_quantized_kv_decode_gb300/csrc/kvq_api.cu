@@ -14,7 +14,9 @@ constexpr int kMaxBatchDecode = 1024;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int block_bytes(int bits) { return kBlockTokens * kHeadDim * bits / 8; }
+int group_of(const kvq_cache_desc* c) { return c->group_size == 0 ? 128 : c->group_size; }
+int block_bytes(const kvq_cache_desc* c) { return kBlockTokens * c->head_dim * c->bits / 8; }
+int sz_per_block(const kvq_cache_desc* c) { return kBlockTokens * c->head_dim / group_of(c); }
 
 kvq_status check_cache(const kvq_cache_desc* c) {
   if (c == nullptr) return KVQ_ERR_INVALID_ARG;
@@ -22,10 +24,15 @@ kvq_status check_cache(const kvq_cache_desc* c) {
   if ((c->k_scheme != KVQ_TOKENWISE && c->k_scheme != KVQ_CHANNELWISE) ||
       (c->v_scheme != KVQ_TOKENWISE && c->v_scheme != KVQ_CHANNELWISE))
     return KVQ_ERR_INVALID_ARG;
-  if (c->head_dim != kHeadDim) return KVQ_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  const int g = group_of(c);
+  if ((g != 32 && g != 64 && g != 128) || g > c->head_dim) return KVQ_ERR_UNSUPPORTED;
   if (c->num_kv_heads < 1 || c->num_pages < 1) return KVQ_ERR_INVALID_ARG;
   return KVQ_OK;
 }
+
+// The specialised decode kernel's geometry; others take the general kernel.
+bool default_geometry(const kvq_cache_desc* c) { return c->head_dim == kHeadDim && group_of(c) == 128; }
 
 }  // namespace
 
@@ -134,8 +141,8 @@ KVQ_API kvq_status kvq_cache_bytes(const kvq_cache_desc* cache, size_t* codes_by
   if (s != KVQ_OK) return s;
   if (codes_bytes == nullptr || scale_bytes == nullptr) return KVQ_ERR_INVALID_ARG;
   const size_t blocks = (size_t)cache->num_pages * cache->num_kv_heads;
-  *codes_bytes = blocks * block_bytes(cache->bits);
-  *scale_bytes = blocks * kBlockTokens * sizeof(uint16_t);
+  *codes_bytes = blocks * block_bytes(cache);
+  *scale_bytes = blocks * sz_per_block(cache) * sizeof(uint16_t);
   return KVQ_OK;
 }
 
@@ -160,6 +167,7 @@ KVQ_API kvq_status kvq_pack(const kvq_cache_desc* cache, int32_t which, const fl
   p.x = x; p.seq_lens = seq_lens; p.page_table = page_table;
   p.codes = codes; p.scale = scale; p.zero = zero; p.dev_status = dev_status;
   p.bits = cache->bits; p.k_scheme = cache->k_scheme; p.v_scheme = cache->v_scheme; p.which = which;
+  p.head_dim = cache->head_dim; p.group = group_of(cache);
   p.num_kv_heads = cache->num_kv_heads; p.num_pages = cache->num_pages;
   p.batch = batch; p.max_seq_len = max_seq_len; p.max_blocks = max_blocks; p.max_blocks_needed = need_blocks;
   return launch_pack(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
@@ -185,6 +193,7 @@ KVQ_API kvq_status kvq_append(const kvq_cache_desc* cache, int32_t which, const 
   p.x = x_new; p.window = window; p.seq_lens = seq_lens; p.page_table = page_table;
   p.codes = codes; p.scale = scale; p.zero = zero; p.dev_status = dev_status;
   p.bits = cache->bits; p.k_scheme = cache->k_scheme; p.v_scheme = cache->v_scheme; p.which = which;
+  p.head_dim = cache->head_dim; p.group = group_of(cache);
   p.num_kv_heads = cache->num_kv_heads; p.num_pages = cache->num_pages;
   p.batch = batch; p.max_seq_len = max_blocks * kBlockTokens; p.max_blocks = max_blocks; p.max_blocks_needed = 1;
   return launch_append(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
@@ -208,6 +217,7 @@ KVQ_API kvq_status kvq_dequant(const kvq_cache_desc* cache, int32_t which, const
   p.codes = codes; p.scale = scale; p.zero = zero; p.seq_lens = seq_lens; p.page_table = page_table;
   p.x_hat = x_hat; p.dev_status = dev_status;
   p.bits = cache->bits; p.k_scheme = cache->k_scheme; p.v_scheme = cache->v_scheme; p.which = which;
+  p.head_dim = cache->head_dim; p.group = group_of(cache);
   p.num_kv_heads = cache->num_kv_heads; p.num_pages = cache->num_pages;
   p.batch = batch; p.max_seq_len = max_seq_len; p.max_blocks = max_blocks;
   return launch_dequant(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
@@ -216,6 +226,7 @@ KVQ_API kvq_status kvq_dequant(const kvq_cache_desc* cache, int32_t which, const
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* bytes) {
   kvq_status s = check_attn(desc);
   if (s != KVQ_OK) return s;
+  if (!default_geometry(&desc->cache)) return KVQ_ERR_UNSUPPORTED;
   if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
   int sm = 0;
   if (desc->num_ctas == 0) {
@@ -234,6 +245,7 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
                                    size_t workspace_bytes, uint32_t* dev_status, void* stream) {
   kvq_status s = check_attn(desc);
   if (s != KVQ_OK) return s;
+  if (!default_geometry(&desc->cache)) return KVQ_ERR_UNSUPPORTED;
   // cache arrays are read with 16-byte bulk copies; the rest with scalar accesses
   const void* bulk[] = {k_codes, k_scale, k_zero, v_codes, v_scale, v_zero};
   for (const void* ptr : bulk)

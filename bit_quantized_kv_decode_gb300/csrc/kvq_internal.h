@@ -9,8 +9,8 @@
 
 namespace kvq {
 
-constexpr int kBlockTokens = 128;  // tokens per block / page; channel-wise group
-constexpr int kHeadDim = 128;
+constexpr int kBlockTokens = 128;  // tokens per block / page
+constexpr int kHeadDim = 128;      // head dim of the specialised decode kernel (64 and 256: the general one)
 constexpr int kGroupQ = 4;  // query heads per KV head
 constexpr int kCounterGroups = 1;  // split-merge arrival counters per (sequence, kv head)
 
@@ -28,6 +28,7 @@ struct PackParams {
   uint16_t* zero;
   uint32_t* dev_status;
   int bits, k_scheme, v_scheme, which;
+  int head_dim, group;  // D (64, 128, 256); group size G (32, 64, 128; <= D)
   int num_kv_heads, num_pages;
   int batch, max_seq_len, max_blocks, max_blocks_needed;
 };
@@ -41,6 +42,7 @@ struct DequantParams {
   float* x_hat;
   uint32_t* dev_status;
   int bits, k_scheme, v_scheme, which;
+  int head_dim, group;
   int num_kv_heads, num_pages;
   int batch, max_seq_len, max_blocks;
 };
@@ -84,7 +86,7 @@ struct DecodeParams {
 // *sm_count when non-null), else KVQ_ERR_DEVICE; launches nothing.
 kvq_status check_device(int* sm_count);
 
-size_t pack_smem_bytes();
+size_t pack_smem_bytes(int head_dim, int group);
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream);
 cudaError_t launch_append(const PackParams& p, cudaStream_t stream);
 cudaError_t launch_dequant(const DequantParams& p, cudaStream_t stream);

@@ -1,7 +1,9 @@
 // Quantize + pack (and the inverse, dequantize) of one K or V cache.
 //
-// One CTA per (block j, KV head h, sequence b).  The block's 128 x 128 fp32
-// tile is staged in shared memory, each group's min/max gives its scale s and
+// One CTA per (block j, KV head h, sequence b).  The block's 128 x D fp32
+// tile (D = head dim: 64, 128 or 256) is staged in shared memory; groups are
+// G consecutive channels of a token (token-wise) or G consecutive tokens of
+// a channel (channel-wise), G = 32, 64 or 128.  Each group's min/max gives its scale s and
 // offset z (asymmetric quantization, rag-lover.com summary of arXiv
 // 2611.09722, section "使える条件"), codes are computed with IEEE fp32
 // subtract/divide and round-half-even, and the block is written in the packed
@@ -20,7 +22,6 @@ namespace kvq {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kPitch = 129;  // fp32 tile row pitch (bank-conflict-free columns)
 
 struct GroupQ {
   float s, z;
@@ -82,95 +83,110 @@ __device__ __forceinline__ bool block_geometry(const PackParams& p, int b, int j
 }
 
 // Quantize and pack one block of KV head h: the nv valid token rows at src
-// (fp32, 128 channels each) into page `page`.
+// (fp32, D channels each) into page `page`.  s / z of a block: token-wise,
+// entry t * (D / G) + g for channels [gG, gG + G) of token t; channel-wise,
+// entry k * D + c for channel c over block tokens [kG, kG + G).
 __device__ void pack_block(const PackParams& p, const float* src, int page, int nv, int h, unsigned char* smem_raw) {
-  float* xs = reinterpret_cast<float*>(smem_raw);                                    // [128][kPitch]
-  uint8_t* cs = reinterpret_cast<uint8_t*>(xs + kBlockTokens * kPitch);             // [128 tok][128 ch]
-  uint16_t* s_out = reinterpret_cast<uint16_t*>(cs + kBlockTokens * kHeadDim);     // [128]
-  uint16_t* z_out = s_out + kBlockTokens;                                          // [128]
+  const int D = p.head_dim, G = p.group, pitch = D + 1;
+  float* xs = reinterpret_cast<float*>(smem_raw);                                    // [128][D + 1]
+  uint8_t* cs = reinterpret_cast<uint8_t*>(xs + kBlockTokens * pitch);              // [128 tok][D ch]
+  uint16_t* s_out = reinterpret_cast<uint16_t*>(cs + kBlockTokens * D);             // [128 * D / G]
+  uint16_t* z_out = s_out + kBlockTokens * D / G;                                   // [128 * D / G]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int qmax = (1 << p.bits) - 1;
+  const int nsz = kBlockTokens * D / G;
 
   // Stage the valid tokens of the tile (rows t < nv).
-  for (int i = tid; i < nv * (kHeadDim / 4); i += kThreads) {
-    int t = i / (kHeadDim / 4), c4 = (i % (kHeadDim / 4)) * 4;
-    float4 v = *reinterpret_cast<const float4*>(src + (size_t)t * kHeadDim + c4);
-    float* row = xs + t * kPitch + c4;
+  for (int i = tid; i < nv * (D / 4); i += kThreads) {
+    int t = i / (D / 4), c4 = (i % (D / 4)) * 4;
+    float4 v = *reinterpret_cast<const float4*>(src + (size_t)t * D + c4);
+    float* row = xs + t * pitch + c4;
     row[0] = v.x; row[1] = v.y; row[2] = v.z; row[3] = v.w;
   }
-  for (int i = tid; i < kBlockTokens * kHeadDim / 4; i += kThreads) reinterpret_cast<uint32_t*>(cs)[i] = 0u;
+  for (int i = tid; i < kBlockTokens * D / 4; i += kThreads) reinterpret_cast<uint32_t*>(cs)[i] = 0u;
+  for (int i = tid; i < nsz; i += kThreads) { s_out[i] = 0; z_out[i] = 0; }  // groups without valid values
   __syncthreads();
 
   const bool tokenwise = (p.which == 0 ? p.k_scheme : p.v_scheme) == KVQ_TOKENWISE;
   if (tokenwise) {
-    // group = the 128 channels of token t; one warp per token
-    for (int t = warp; t < kBlockTokens; t += kThreads / 32) {
-      if (t >= nv) {  // padding token: s = z = 0, codes 0
-        if (lane == 0) { s_out[t] = 0; z_out[t] = 0; }
-        continue;
+    // groups of G channels of token t; one warp per token, lane holds channels lane + 32 k
+    const int gpt = D / G, kpg = G / 32;  // groups per token, 32-channel slices per group
+    for (int t = warp; t < nv; t += kThreads / 32) {
+      for (int g = 0; g < gpt; ++g) {
+        float v[4];
+        bool fin = true;
+        float mn = INFINITY, mx = -INFINITY;
+        for (int k = 0; k < kpg; ++k) {
+          v[k] = xs[t * pitch + g * G + lane + 32 * k];
+          fin &= isfinite(v[k]);
+          mn = fminf(mn, v[k]);
+          mx = fmaxf(mx, v[k]);
+        }
+        fin = __all_sync(0xffffffffu, fin);
+        mn = warp_min(mn);
+        mx = warp_max(mx);
+        GroupQ q = fin ? group_params(mn, mx, qmax) : GroupQ{0.f, 0.f, 0, 0, false};
+        if (!q.ok) {
+          if (lane == 0) report(p.dev_status, KVQ_DEV_NONFINITE);  // group left as zeros
+          continue;
+        }
+        for (int k = 0; k < kpg; ++k) cs[t * D + g * G + lane + 32 * k] = (uint8_t)quantize_one(v[k], q, qmax);
+        if (lane == 0) { s_out[t * gpt + g] = q.s_bits; z_out[t * gpt + g] = q.z_bits; }
       }
-      float v[4];
-      bool fin = true;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) { v[k] = xs[t * kPitch + lane + 32 * k]; fin &= isfinite(v[k]); }
-      fin = __all_sync(0xffffffffu, fin);
-      float mn = warp_min(fminf(fminf(v[0], v[1]), fminf(v[2], v[3])));
-      float mx = warp_max(fmaxf(fmaxf(v[0], v[1]), fmaxf(v[2], v[3])));
-      GroupQ g = fin ? group_params(mn, mx, qmax) : GroupQ{0.f, 0.f, 0, 0, false};
-      if (!g.ok) {
-        if (lane == 0) { report(p.dev_status, KVQ_DEV_NONFINITE); s_out[t] = 0; z_out[t] = 0; }
-        continue;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) cs[t * kHeadDim + lane + 32 * k] = (uint8_t)quantize_one(v[k], g, qmax);
-      if (lane == 0) { s_out[t] = g.s_bits; z_out[t] = g.z_bits; }
     }
   } else {
-    // group = channel c over the block's valid tokens; one warp per channel
-    for (int c = warp; c < kHeadDim; c += kThreads / 32) {
-      float mn = INFINITY, mx = -INFINITY;
-      bool fin = true;
-      for (int t = lane; t < nv; t += 32) {
-        float v = xs[t * kPitch + c];
-        fin &= isfinite(v);
-        mn = fminf(mn, v);
-        mx = fmaxf(mx, v);
+    // groups of G tokens of channel c (aligned to the block); one warp per channel
+    const int gpb = kBlockTokens / G;
+    for (int c = warp; c < D; c += kThreads / 32) {
+      for (int g = 0; g < gpb; ++g) {
+        const int t0 = g * G, t1 = min(nv, t0 + G);
+        if (t1 <= t0) break;  // no valid token in this group or the later ones: s = z = 0
+        float mn = INFINITY, mx = -INFINITY;
+        bool fin = true;
+        for (int t = t0 + lane; t < t1; t += 32) {
+          float v = xs[t * pitch + c];
+          fin &= isfinite(v);
+          mn = fminf(mn, v);
+          mx = fmaxf(mx, v);
+        }
+        fin = __all_sync(0xffffffffu, fin);
+        mn = warp_min(mn);
+        mx = warp_max(mx);
+        GroupQ q = fin ? group_params(mn, mx, qmax) : GroupQ{0.f, 0.f, 0, 0, false};
+        if (!q.ok) {
+          if (lane == 0) report(p.dev_status, KVQ_DEV_NONFINITE);
+          continue;
+        }
+        for (int t = t0 + lane; t < t1; t += 32) cs[t * D + c] = (uint8_t)quantize_one(xs[t * pitch + c], q, qmax);
+        if (lane == 0) { s_out[g * D + c] = q.s_bits; z_out[g * D + c] = q.z_bits; }
       }
-      fin = __all_sync(0xffffffffu, fin);
-      mn = warp_min(mn);
-      mx = warp_max(mx);
-      GroupQ g = fin ? group_params(mn, mx, qmax) : GroupQ{0.f, 0.f, 0, 0, false};
-      if (!g.ok) {
-        if (lane == 0) { report(p.dev_status, KVQ_DEV_NONFINITE); s_out[c] = 0; z_out[c] = 0; }
-        continue;
-      }
-      for (int t = lane; t < nv; t += 32) cs[t * kHeadDim + c] = (uint8_t)quantize_one(xs[t * kPitch + c], g, qmax);
-      if (lane == 0) { s_out[c] = g.s_bits; z_out[c] = g.z_bits; }
     }
   }
   __syncthreads();
 
-  // Pack: row r, chunk k holds columns [k*per_chunk, (k+1)*per_chunk).
+  // Pack: K rows are tokens (D columns), V rows are channels (128 columns);
+  // row r, chunk k holds columns [k*per_chunk, (k+1)*per_chunk).
   const int bits = p.bits;
-  const int per_chunk = 128 / bits;         // columns per 16-byte chunk: 32 (INT4) or 64 (INT2)
-  const int nchunk = kHeadDim / per_chunk;  // 4 or 2
+  const int per_chunk = 128 / bits;  // columns per 16-byte chunk: 32 (INT4) or 64 (INT2)
+  const int nrows = p.which == 0 ? kBlockTokens : D, ncols = p.which == 0 ? D : kBlockTokens;
+  const int nchunk = ncols / per_chunk;
   const size_t blk = (size_t)page * p.num_kv_heads + h;
-  uint8_t* dst = p.codes + blk * (size_t)(kBlockTokens * kHeadDim * bits / 8);
-  for (int i = tid; i < nchunk * kBlockTokens; i += kThreads) {
-    int k = i / kBlockTokens, r = i % kBlockTokens;
+  uint8_t* dst = p.codes + blk * (size_t)(kBlockTokens * D * bits / 8);
+  for (int i = tid; i < nchunk * nrows; i += kThreads) {
+    int k = i / nrows, r = i % nrows;
     uint32_t w[4] = {0u, 0u, 0u, 0u};
     for (int e = 0; e < per_chunk; ++e) {
       int col = k * per_chunk + e;
       // K: row = token, column = channel.  V: row = channel, column = token.
-      uint32_t code = (p.which == 0) ? cs[r * kHeadDim + col] : cs[col * kHeadDim + r];
+      uint32_t code = (p.which == 0) ? cs[r * D + col] : cs[col * D + r];
       int bitpos = e * bits;
       w[bitpos >> 5] |= code << (bitpos & 31);
     }
     *reinterpret_cast<uint4*>(dst + (size_t)i * 16) = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  if (tid < kBlockTokens) {
-    p.scale[blk * kBlockTokens + tid] = s_out[tid];
-    p.zero[blk * kBlockTokens + tid] = z_out[tid];
+  for (int i = tid; i < nsz; i += kThreads) {
+    p.scale[blk * nsz + i] = s_out[i];
+    p.zero[blk * nsz + i] = z_out[i];
   }
 }
 
@@ -179,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(PackParams p) {
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   int page, nv;
   if (!block_geometry(p, b, j, &page, &nv)) return;
-  const float* src = p.x + (((size_t)b * p.num_kv_heads + h) * p.max_seq_len + (size_t)j * kBlockTokens) * kHeadDim;
+  const float* src = p.x + (((size_t)b * p.num_kv_heads + h) * p.max_seq_len + (size_t)j * kBlockTokens) * p.head_dim;
   pack_block(p, src, page, nv, h, smem_raw);
 }
 
@@ -202,9 +218,10 @@ __global__ void __launch_bounds__(kThreads) append_kernel(PackParams p) {
     if (h == 0 && threadIdx.x == 0) report(p.dev_status, KVQ_DEV_BAD_PAGE);
     return;
   }
-  float* win = p.window + ((size_t)b * p.num_kv_heads + h) * kBlockTokens * kHeadDim;
-  const float* xn = p.x + ((size_t)b * p.num_kv_heads + h) * kHeadDim;
-  if (threadIdx.x < kHeadDim) win[(size_t)r * kHeadDim + threadIdx.x] = xn[threadIdx.x];
+  const int D = p.head_dim;
+  float* win = p.window + ((size_t)b * p.num_kv_heads + h) * kBlockTokens * D;
+  const float* xn = p.x + ((size_t)b * p.num_kv_heads + h) * D;
+  for (int c = threadIdx.x; c < D; c += kThreads) win[(size_t)r * D + c] = xn[c];
   __syncthreads();  // the new row is visible to the whole CTA
   pack_block(p, win, page, r + 1, h, smem_raw);
 }
@@ -212,7 +229,8 @@ __global__ void __launch_bounds__(kThreads) append_kernel(PackParams p) {
 __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantParams p) {
   const int j = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x;
-  float* dst = p.x_hat + (((size_t)b * p.num_kv_heads + h) * p.max_seq_len + (size_t)j * kBlockTokens) * kHeadDim;
+  const int D = p.head_dim, G = p.group, nsz = kBlockTokens * D / G;
+  float* dst = p.x_hat + (((size_t)b * p.num_kv_heads + h) * p.max_seq_len + (size_t)j * kBlockTokens) * D;
   const int ntok = min(kBlockTokens, p.max_seq_len - j * kBlockTokens);
   int len = p.seq_lens ? p.seq_lens[b] : p.max_seq_len;
   bool bad_len = len < 0 || len > p.max_seq_len;
@@ -229,37 +247,39 @@ __global__ void __launch_bounds__(kThreads) dequant_kernel(DequantParams p) {
   const bool tokenwise = (p.which == 0 ? p.k_scheme : p.v_scheme) == KVQ_TOKENWISE;
   const size_t blk = (size_t)page * p.num_kv_heads + h;
   const int bits = p.bits;
-  const uint8_t* src = p.codes + blk * (size_t)(kBlockTokens * kHeadDim * bits / 8);
-  const uint16_t* sp = p.scale + blk * kBlockTokens;
-  const uint16_t* zp = p.zero + blk * kBlockTokens;
+  const uint8_t* src = p.codes + blk * (size_t)(kBlockTokens * D * bits / 8);
+  const uint16_t* sp = p.scale + blk * nsz;
+  const uint16_t* zp = p.zero + blk * nsz;
   const int per_chunk = 128 / bits;
-  for (int i = tid; i < ntok * kHeadDim; i += kThreads) {
-    int t = i / kHeadDim, c = i % kHeadDim;
+  const int nrows = p.which == 0 ? kBlockTokens : D;
+  for (int i = tid; i < ntok * D; i += kThreads) {
+    int t = i / D, c = i % D;
     float v = 0.0f;
     if (t < nv) {
       int r = (p.which == 0) ? t : c;    // row in the block
       int col = (p.which == 0) ? c : t;  // column in the row
       int k = col / per_chunk, e = col % per_chunk;
-      const uint32_t* chunk = reinterpret_cast<const uint32_t*>(src + ((size_t)k * kBlockTokens + r) * 16);
+      const uint32_t* chunk = reinterpret_cast<const uint32_t*>(src + ((size_t)k * nrows + r) * 16);
       int bitpos = e * bits;
       uint32_t code = (chunk[bitpos >> 5] >> (bitpos & 31)) & ((1u << bits) - 1u);
-      int g = tokenwise ? t : c;
+      int g = tokenwise ? t * (D / G) + c / G : (t / G) * D + c;
       float s = __half2float(__ushort_as_half(sp[g]));
       float z = __half2float(__ushort_as_half(zp[g]));
       v = fmaf(s, (float)code, z);
     }
-    dst[(size_t)t * kHeadDim + c] = v;
+    dst[(size_t)t * D + c] = v;
   }
 }
 
 }  // namespace
 
-size_t pack_smem_bytes() {
-  return (size_t)kBlockTokens * kPitch * sizeof(float) + kBlockTokens * kHeadDim + 2 * kBlockTokens * sizeof(uint16_t);
+size_t pack_smem_bytes(int head_dim, int group) {
+  return (size_t)kBlockTokens * (head_dim + 1) * sizeof(float) + (size_t)kBlockTokens * head_dim +
+         2 * (size_t)kBlockTokens * head_dim / group * sizeof(uint16_t);
 }
 
 cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
-  const size_t smem = pack_smem_bytes();
+  const size_t smem = pack_smem_bytes(p.head_dim, p.group);
   cudaError_t e = cudaFuncSetAttribute(pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.max_blocks_needed, p.num_kv_heads, p.batch);
@@ -268,7 +288,7 @@ cudaError_t launch_pack(const PackParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_append(const PackParams& p, cudaStream_t stream) {
-  const size_t smem = pack_smem_bytes();
+  const size_t smem = pack_smem_bytes(p.head_dim, p.group);
   cudaError_t e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.num_kv_heads, p.batch);

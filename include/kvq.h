@@ -15,23 +15,28 @@
  *   - same page, section "解説" (commentary): which side each scheme folds on,
  *     and code bits placed in the low bits of a tensor-core element.
  *
- * out[b, h, :] = softmax(S) V_hat[b, h/4],  S_l = sm_scale * q[b,h] . K_hat[b, h/4, l],
+ * out[b, h, :] = softmax(S) V_hat[b, h/G_q],  S_l = sm_scale * q[b,h] . K_hat[b, h/G_q, l],
  * lse[b, h] = ln sum_l exp(S_l), with x_hat = s * code + z and code unsigned.
  *
  * Cache format (this library's; the pages leave it open)
  * -------------------------------------------------------
- * head_dim D = 128; a block (= page) holds 128 consecutive tokens of one KV
- * head.  Codes of one block form a 128 x 128 matrix: K rows are tokens
- * (channels along the row), V rows are channels (tokens along the row).  A
- * row is packed little-endian (column i at bits [b*(i mod 8/b), +b) of row
- * byte i*b/8), cut into 16-byte chunks, and the block is stored chunk-major:
- * byte offset (chunk*128 + row)*16 + byte.  Block bytes: 8192 (INT4), 4096
- * (INT2).  codes array: [num_pages][num_kv_heads][block bytes].
- * scale / zero arrays (fp16 bit patterns): [num_pages][num_kv_heads][128],
- * indexed by token within the block (token-wise) or by channel
- * (channel-wise).  Token-wise groups are the 128 channels of a token;
- * channel-wise groups are one channel over the block's tokens.  Tokens at or
- * past a sequence's length have code 0 (token-wise: s = z = 0).
+ * head_dim D (64, 128 or 256); a block (= page) holds 128 consecutive tokens
+ * of one KV head.  Codes of one block form a matrix: K rows are the 128
+ * tokens (D channels along the row), V rows are the D channels (128 tokens
+ * along the row).  A row is packed little-endian (column i at bits
+ * [b*(i mod 8/b), +b) of row byte i*b/8), cut into 16-byte chunks, and the
+ * block is stored chunk-major: byte offset (chunk*nrows + row)*16 + byte,
+ * nrows = 128 (K) or D (V).  Block bytes: 128 * D * b / 8 (8192 for INT4,
+ * 4096 for INT2 at D = 128).  codes array: [num_pages][num_kv_heads][block
+ * bytes].  Quantization groups of G elements: token-wise, G consecutive
+ * channels of a token; channel-wise, G consecutive tokens of a channel
+ * (aligned to the block).  scale / zero arrays (fp16 bit patterns):
+ * [num_pages][num_kv_heads][128 * D / G]; token-wise, entry t * (D / G) + g
+ * is channel group g of block token t; channel-wise, entry k * D + c is
+ * channel c over block tokens [k G, (k + 1) G).  (D = G = 128: one entry per
+ * token, resp. per channel.)  Tokens at or past a sequence's length have code
+ * 0 (token-wise: s = z = 0; a channel-wise group without valid tokens:
+ * s = z = 0).
  * Sequence b's block j lives in page page_table[b*max_blocks + j], or in page
  * b*max_blocks + j when page_table is NULL ("contiguous" cache).
  *
@@ -65,7 +70,7 @@ extern "C" {
 typedef enum kvq_status {
   KVQ_OK = 0,
   KVQ_ERR_INVALID_ARG = 1, /* NULL/misaligned pointer, bad size or enum value */
-  KVQ_ERR_UNSUPPORTED = 2, /* well-formed but not built (e.g. head_dim != 128) */
+  KVQ_ERR_UNSUPPORTED = 2, /* well-formed but not built (e.g. head_dim 96) */
   KVQ_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required */
   KVQ_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
   KVQ_ERR_DEVICE = 5       /* current device is not an sm_103 GPU */
@@ -90,9 +95,11 @@ typedef struct kvq_cache_desc {
   int32_t bits;         /* 2 or 4 */
   int32_t k_scheme;     /* kvq_scheme used by K */
   int32_t v_scheme;     /* kvq_scheme used by V */
-  int32_t head_dim;     /* must be 128 */
+  int32_t head_dim;     /* D: 64, 128 or 256 */
   int32_t num_kv_heads; /* >= 1 */
   int32_t num_pages;    /* 128-token pages the cache arrays hold */
+  int32_t group_size;   /* G: 32, 64 or 128 elements per quantization group
+                           (0 = 128), at most head_dim; the same for K and V */
 } kvq_cache_desc;
 
 typedef struct kvq_attn_desc {
@@ -137,7 +144,7 @@ KVQ_API kvq_status kvq_cache_bytes(const kvq_cache_desc* cache, size_t* codes_by
  * s = fp16 round-up of fp32((max - z) / (2^bits - 1)),
  * code = clamp(rint(fp32(fp32(x - z) / s)), 0, 2^bits - 1), all IEEE fp32;
  * max == z gives s = 0, code = 0.
- *   x          fp32 [batch][num_kv_heads][max_seq_len][128]
+ *   x          fp32 [batch][num_kv_heads][max_seq_len][head_dim]
  *   seq_lens   int32 [batch] in [0, max_seq_len], or NULL (all max_seq_len)
  *   page_table int32 [batch][max_blocks], or NULL (contiguous; then
  *              batch*max_blocks <= num_pages)
@@ -165,11 +172,11 @@ KVQ_API kvq_status kvq_pack(const kvq_cache_desc* cache, int32_t which, const fl
  * block's rows overwrite the window from row 0 (no reset needed).  A cache
  * that starts from kvq_pack of a prefix needs the prefix's partial last block
  * copied into the window first.
- *   x_new      fp32 [batch][num_kv_heads][128], 16-byte aligned
+ *   x_new      fp32 [batch][num_kv_heads][head_dim], 16-byte aligned
  *   seq_lens   int32 [batch], each in [0, max_blocks * 128)
  *   page_table int32 [batch][max_blocks] or NULL (contiguous; then
  *              batch * max_blocks <= num_pages)
- *   window     fp32 [batch][num_kv_heads][128][128], caller-owned (one for
+ *   window     fp32 [batch][num_kv_heads][128][head_dim], caller-owned (one for
  *              K, one for V), 16-byte aligned
  *   codes, scale, zero: the cache arrays (only the current block's page is
  *              written)
@@ -183,7 +190,7 @@ KVQ_API kvq_status kvq_append(const kvq_cache_desc* cache, int32_t which, const 
 
 /*
  * Read a packed K or V cache back as fp32 x_hat = s * code + z (exact, one
- * rounding).  x_hat: fp32 [batch][num_kv_heads][max_seq_len][128]; positions
+ * rounding).  x_hat: fp32 [batch][num_kv_heads][max_seq_len][head_dim]; positions
  * at or past seq_lens[b] are written as 0.  Other arguments as kvq_pack.
  */
 KVQ_API kvq_status kvq_dequant(const kvq_cache_desc* cache, int32_t which, const uint8_t* codes,
@@ -206,11 +213,11 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* 
  * CTAs is merged on the device by log-sum-exp.  Query heads per KV head:
  * 1, 2, 4 or 8 (a work unit takes up to 4 query heads of one KV head, so
  * with 8 each KV block is read twice).
- *   q        bf16 [batch][num_q_heads][128]
+ *   q        bf16 [batch][num_q_heads][head_dim]
  *   k_codes, v_codes, k_scale, k_zero, v_scale, v_zero: cache arrays
  *   seq_lens int32 [batch], each in [0, max_blocks*128]
  *   page_table int32 [batch][max_blocks] or NULL (contiguous)
- *   out      fp32 [batch][num_q_heads][128];  lse fp32 [batch][num_q_heads]
+ *   out      fp32 [batch][num_q_heads][head_dim];  lse fp32 [batch][num_q_heads]
  *            (natural log; empty sequence: out = 0, lse = -inf)
  *   workspace >= kvq_decode_workspace_size bytes, 256-byte aligned; its
  *            contents need no initialisation; concurrent calls need separate

@@ -177,8 +177,8 @@ def quantize_sequence(x_seq, bits, scheme, group=GROUP):
         ct, st, zt = quantize_groups(x_seq.reshape(n * gpt, group), bits)
         pad = nblk * BLOCK_TOKENS - n
         codes[:] = np.concatenate([ct.reshape(n, d), np.zeros((pad, d), np.uint8)]).reshape(nblk, BLOCK_TOKENS, d)
-        s = np.concatenate([st.reshape(n, gpt), np.zeros((pad, gpt), np.float16)]).reshape(nblk, -1)
-        z = np.concatenate([zt.reshape(n, gpt), np.zeros((pad, gpt), np.float16)]).reshape(nblk, -1)
+        s = np.concatenate([st.reshape(n, gpt), np.zeros((pad, gpt), np.float16)]).reshape(nblk, BLOCK_TOKENS * gpt)
+        z = np.concatenate([zt.reshape(n, gpt), np.zeros((pad, gpt), np.float16)]).reshape(nblk, BLOCK_TOKENS * gpt)
     elif scheme == CHANNELWISE:  # one group = one channel over G consecutive valid tokens
         gpb = BLOCK_TOKENS // group
         s = np.zeros((nblk, gpb, d), np.float16)
@@ -193,8 +193,8 @@ def quantize_sequence(x_seq, bits, scheme, group=GROUP):
                 codes[j, k * group:k * group + nv] = cc.T
                 s[j, k] = sc
                 z[j, k] = zc
-        s = s.reshape(nblk, -1)
-        z = z.reshape(nblk, -1)
+        s = s.reshape(nblk, gpb * d)
+        z = z.reshape(nblk, gpb * d)
     else:
         raise OracleError("unknown scheme")
     return codes, s, z

@@ -46,8 +46,8 @@ def test_status_strings_and_version(lib):
     assert lib.kvq_version() >= 100
 
 
-def _cache(bits=4, k=0, v=1, heads=8, pages=1024, hd=128):
-    return _lib.CacheDesc(bits, k, v, hd, heads, pages)
+def _cache(bits=4, k=0, v=1, heads=8, pages=1024, hd=128, group=0):
+    return _lib.CacheDesc(bits, k, v, hd, heads, pages, group)
 
 
 def test_cache_bytes(lib):
@@ -57,7 +57,14 @@ def test_cache_bytes(lib):
     assert lib.kvq_cache_bytes(ctypes.byref(_cache(2)), ctypes.byref(cb), ctypes.byref(sb)) == 0
     assert cb.value == 1024 * 8 * 4096
     assert lib.kvq_cache_bytes(ctypes.byref(_cache(3)), ctypes.byref(cb), ctypes.byref(sb)) == 2
-    assert lib.kvq_cache_bytes(ctypes.byref(_cache(4, hd=64)), ctypes.byref(cb), ctypes.byref(sb)) == 2
+    # head dims 64 / 256 and groups of 32 / 64: codes 128 * D * b / 8, s / z 128 * D / G per page and head
+    assert lib.kvq_cache_bytes(ctypes.byref(_cache(4, hd=256, group=64)), ctypes.byref(cb), ctypes.byref(sb)) == 0
+    assert cb.value == 1024 * 8 * 128 * 256 * 4 // 8 and sb.value == 1024 * 8 * (128 * 256 // 64) * 2
+    assert lib.kvq_cache_bytes(ctypes.byref(_cache(2, hd=64, group=32)), ctypes.byref(cb), ctypes.byref(sb)) == 0
+    assert cb.value == 1024 * 8 * 128 * 64 * 2 // 8 and sb.value == 1024 * 8 * (128 * 64 // 32) * 2
+    for hd, group in ((64, 0), (64, 128), (96, 32), (128, 16), (128, 96), (512, 128)):
+        assert lib.kvq_cache_bytes(ctypes.byref(_cache(4, hd=hd, group=group)), ctypes.byref(cb),
+                                   ctypes.byref(sb)) == 2, (hd, group)
     assert lib.kvq_cache_bytes(None, ctypes.byref(cb), ctypes.byref(sb)) == 1
 
 

@@ -79,6 +79,16 @@ def test_mutation_group_size_caught():
         check_constant_groups(wrong, o.TOKENWISE, 128, 32)
 
 
+@pytest.mark.parametrize("D,G", GEOMETRIES + [(128, 128)])
+@pytest.mark.parametrize("scheme", [o.TOKENWISE, o.CHANNELWISE])
+def test_empty_sequence_shapes(D, G, scheme):
+    codes, s, z = o.quantize_sequence(np.zeros((0, D), np.float32), 2, scheme, G)
+    assert codes.shape == (0, 128, D) and s.shape == (0, 128 * D // G) and z.shape == s.shape
+    c, s, z = o.pack_cache(np.zeros((2, 1, 128, D), np.float32), [0, 5], 4, scheme, o.V_CACHE, group=G)
+    assert c.shape == (2, 1, o.block_bytes(4, D)) and s.shape == (2, 1, 128 * D // G)
+    assert not c[0].any() and not s[0].any()
+
+
 def _sequence(seed, D, n=260):
     r = _rng(seed)
     return (r.standard_normal((n, D)) * (1 + 4 * np.abs(r.standard_normal(D)))).astype(np.float32)

@@ -43,8 +43,13 @@ SCHEME_NAMES = {0: "token", 1: "channel"}
 def algorithmic_bytes(w, lens) -> int:
     """Packed K+V codes and their fp16 scale/offset arrays touched by a step."""
     blocks = sum((int(n) + 127) // 128 for n in lens) * w.num_kv_heads
-    per_block = 2 * (128 * 128 * w.bits // 8) + 2 * 2 * 128 * 2
-    return blocks * per_block
+    return blocks * block_bytes_kv(w)
+
+
+def block_bytes_kv(w) -> int:
+    """K and V codes of one 128-token block of one KV head, plus their fp16
+    s and z (128 * D / G values each)."""
+    return 2 * (128 * w.head_dim * w.bits // 8) + 2 * 2 * (128 * w.head_dim // w.group) * 2
 
 
 def build_cache(w, seed, dev, k_scheme=None, v_scheme=None, chunk=16):
@@ -59,7 +64,7 @@ def build_cache(w, seed, dev, k_scheme=None, v_scheme=None, chunk=16):
         pt = pt_cpu.to(dev)
     else:
         pt, num_pages = None, w.batch * max_blocks
-    desc = kvq.cache_desc(w.bits, ks, vs, w.num_kv_heads, num_pages)
+    desc = kvq.cache_desc(w.bits, ks, vs, w.num_kv_heads, num_pages, head_dim=w.head_dim, group=w.group)
     kc, vc = kvq.alloc_cache(desc, dev), kvq.alloc_cache(desc, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     cs = synth.outlier_channels(w, seed, dev)
@@ -179,7 +184,7 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
     desc = c["desc"]
     ad = kvq.attn_desc(desc, w.batch, c["max_blocks"], num_q_heads=w.num_q_heads)
     ws = torch.empty(kvq.workspace_size(ad), dtype=torch.uint8, device=dev)
-    out = torch.empty(w.batch, w.num_q_heads, 128, dtype=torch.float32, device=dev)
+    out = torch.empty(w.batch, w.num_q_heads, w.head_dim, dtype=torch.float32, device=dev)
     lse = torch.empty(w.batch, w.num_q_heads, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream()
@@ -196,8 +201,9 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
     t_wall1 = time.time()
     if int(status.item()) != 0:
         raise RuntimeError(f"decode reported device status {int(status.item()):#x}")
+    general = w.head_dim != 128 or w.group != 128  # block-range kernel + log-sum-exp merge kernel
     res = dict(ms=ms, per=per, bytes=algorithmic_bytes(w, c["lens_cpu"].tolist()), t0=t_wall0, t1=t_wall1,
-               launches=steps, sets=sets, lens=c["lens_cpu"].tolist())
+               launches=steps * (2 if general else 1), sets=sets, lens=c["lens_cpu"].tolist())
     if e2e:
         # end to end through the public API with host buffers: H2D of this step's
         # query and lengths from pinned memory, decode, D2H of out and lse
@@ -263,8 +269,8 @@ def oracle_pack_unit(args):
     n = int(lens[b])
     k = synth.kv_unit(w, seed, 0, b, h, n, "cpu", cs[h]).numpy()[None, None]
     v = synth.kv_unit(w, seed, 1, b, h, n, "cpu").numpy()[None, None]
-    kcodes, ks, kz = orc.pack_cache(k, [n], w.bits, w.k_scheme, 0)
-    vcodes, vs, vz = orc.pack_cache(v, [n], w.bits, w.v_scheme, 1)
+    kcodes, ks, kz = orc.pack_cache(k, [n], w.bits, w.k_scheme, 0, group=w.group)
+    vcodes, vs, vz = orc.pack_cache(v, [n], w.bits, w.v_scheme, 1, group=w.group)
     qb = q[b:b + 1, 4 * h:4 * h + 4].contiguous().view(torch.int16).numpy().view(np.uint16)
     return (qb, kcodes, ks, kz, vcodes, vs, vz, n, w.bits, w.k_scheme, w.v_scheme)
 
@@ -285,7 +291,7 @@ class OracleTimer:
         self.cores = max(1, min(host_cores(), self.units))
         lens = synth.seq_lens_for(w, seed)
         self.sample_lens = [int(lens[divmod(u, w.num_kv_heads)[0] % w.batch]) for u in range(self.units)]
-        self.bytes = sum(((n + 127) // 128) * (2 * (128 * 128 * w.bits // 8) + 2 * 2 * 128 * 2)
+        self.bytes = sum(((n + 127) // 128) * block_bytes_kv(w)
                          for n in self.sample_lens)
         self.sample = (f"{self.units} of {w.batch * w.num_kv_heads} (sequence, kv head) units "
                        f"({sum(self.sample_lens)} tokens), oracle unpack+dequantize+attend in fp64")
@@ -379,7 +385,7 @@ def config_of(w):
     return {"workload": w.name, "batch": w.batch, "kv_heads": w.num_kv_heads, "q_heads": w.num_q_heads,
             "head_dim": w.head_dim, "seq_len": w.max_seq_len if w.ragged is None else f"log-uniform {w.ragged}",
             "bits": w.bits, "k_scheme": SCHEME_NAMES[w.k_scheme], "v_scheme": SCHEME_NAMES[w.v_scheme],
-            "paged": w.paged, "group": 128, "operands": "fp8 (E4M3 codes, 3-part E4M3 Q'/P')"}
+            "paged": w.paged, "group": w.group, "operands": "fp8 (E4M3 codes, 3-part E4M3 Q'/P')"}
 
 
 def run_reference(args, w):
@@ -481,6 +487,17 @@ def main():
                                          f"{len(lens3)} x {lens3[0]} tokens"),
                             "paged": w3.paged, "split_kv": "persistent CTAs cut the tile order into equal "
                                                           "ranges; cut units are merged in the kernel"})
+    geometry = []  # head dims 64 / 256 and groups of 32 / 64: the general-geometry kernel
+    if not args.no_extra and w.name == DEFAULT_WORKLOAD and mode == 0:
+        for name in ("b32_l32k_d256_g64_int4", "b32_l32k_d128_g32_int2", "b32_l32k_d64_g32_int2"):
+            w4 = synth.WORKLOADS[name]
+            r4 = measure_kvq(w4, args.seed + rank, 20, args.warmup, dev, e2e=False)
+            ms4 = max_over_ranks(r4["ms"], world, dev)
+            geometry.append({"workload": name, "head_dim": w4.head_dim, "group": w4.group, "bits": w4.bits,
+                             "k_scheme": SCHEME_NAMES[w4.k_scheme], "v_scheme": SCHEME_NAMES[w4.v_scheme],
+                             "ms_per_step": ms4, "GB/s": r4["bytes"] / (ms4 / 1e3) / 1e9, "latency_us": ms4 * 1e3,
+                             "algorithmic_bytes": r4["bytes"], "l2": l2_note(r4),
+                             "kernel": "kvq::decode_general_kernel + kvq::merge_kernel"})
     clk = clocks.summary(res["t0"], res["t1"])
     clocks.stop()
     if rank != 0:
@@ -489,7 +506,7 @@ def main():
     total_bytes = res["bytes"] * world
     value = total_bytes / (ms / 1e3) / 1e9
     achieved = res["bytes"] / (ms / 1e3) / 1e9
-    for e in extra + configs + e2m1:
+    for e in extra + configs + e2m1 + geometry:
         e["frac_of_peak"] = e["GB/s"] / peak
     line = {
         "metric": "effective KV-access HBM GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
@@ -501,7 +518,9 @@ def main():
         "config": dict(config_of(w), l2=l2_note(res),
                        **({"operands": "bf16 (exact BF16 codes, 2-part BF16 Q'/P')"} if mode else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "kvq::decode_kernel",
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": ("kvq::decode_kernel" if w.head_dim == 128 and w.group == 128 else
+                                "kvq::decode_general_kernel + kvq::merge_kernel"),
                      "traffic": None if mode else profile_traffic(w.name),
                      "algorithmic_bytes_per_launch": res["bytes"],
                      "duration_source": "CUDA events around each kvq_decode_attn call (counter memset + kernel)"},
@@ -512,6 +531,7 @@ def main():
         "int2_sweep": extra,
         "int2_sweep_e2m1_v": e2m1,
         "other_configs": configs,
+        "geometry_configs": geometry,
     }
     if not args.no_cpu_baseline and world == 1:
         timer = OracleTimer(w, args.seed, args.oracle_units)

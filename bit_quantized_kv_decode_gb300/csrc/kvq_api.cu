@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "decode_general.h"
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -98,8 +99,46 @@ kvq_status check_attn(const kvq_attn_desc* d) {
   if ((d->flags & KVQ_FLAG_E2M1_V) &&
       (d->cache.bits != 2 || d->operand_mode != KVQ_OPERANDS_FP8 || heads_per_kv(d) != kGroupQ))
     return KVQ_ERR_UNSUPPORTED;  // the E2M1 placement is built for these only
+  if (!default_geometry(&d->cache) && (d->operand_mode != KVQ_OPERANDS_FP8 || (d->flags & KVQ_FLAG_E2M1_V)))
+    return KVQ_ERR_UNSUPPORTED;  // the general-geometry kernel has FP8 operands only
   if (!(std::isfinite(d->sm_scale))) return KVQ_ERR_INVALID_ARG;
   if ((long long)d->batch * units_per_seq(d) * d->max_blocks > (1LL << 30)) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+// General geometry: block ranges per (sequence, unit) and the launch shape.
+// The grid aims at two waves of resident CTAs (or num_ctas CTAs when given).
+struct GeneralPlan {
+  GenLaunch launch;
+  int splits;
+  size_t part_lse, part_o, total;  // workspace offsets and size
+};
+
+kvq_status general_plan(const kvq_attn_desc* d, GeneralPlan* plan) {
+  int sm = 0, smem_sm = 228 * 1024, reserved = 1024;
+  if (d->num_ctas == 0) {
+    kvq_status s = check_device(&sm);
+    if (s != KVQ_OK) return s;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return KVQ_ERR_DEVICE;
+    }
+  }
+  plan->launch = general_launch_shape(d->cache.bits, d->cache.k_scheme, d->cache.v_scheme, d->cache.head_dim,
+                                      group_of(&d->cache), smem_sm, reserved);
+  const long long units = (long long)d->batch * units_per_seq(d);
+  const long long target = d->num_ctas > 0 ? d->num_ctas : 2LL * plan->launch.ctas_per_sm * sm;
+  long long splits = (target + units - 1) / units;
+  if (splits > d->max_blocks) splits = d->max_blocks;
+  if (splits < 1) splits = 1;
+  plan->splits = (int)splits;
+  const size_t rows = (size_t)d->batch * d->num_q_heads;
+  plan->part_lse = 0;
+  plan->part_o = round_up(rows * splits * sizeof(float), 256);
+  plan->total = plan->part_o + round_up(rows * splits * d->cache.head_dim * sizeof(float), 256);
   return KVQ_OK;
 }
 
@@ -108,6 +147,47 @@ int resolve_ctas(const kvq_attn_desc* d, int sm_count) {
   long long tiles_bound = (long long)d->batch * units_per_seq(d) * d->max_blocks;
   if (want > tiles_bound) want = tiles_bound;
   return (int)(want < 1 ? 1 : want);
+}
+
+// The general-geometry path of kvq_decode_attn (arguments already checked):
+// the block-range kernel, then the log-sum-exp merge of the ranges.
+kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const uint8_t* k_codes,
+                          const uint16_t* k_scale, const uint16_t* k_zero, const uint8_t* v_codes,
+                          const uint16_t* v_scale, const uint16_t* v_zero, const int32_t* seq_lens,
+                          const int32_t* page_table, float* out, float* lse, void* workspace, size_t workspace_bytes,
+                          uint32_t* dev_status, float sm_scale, cudaStream_t st) {
+  GeneralPlan plan;
+  kvq_status s = general_plan(desc, &plan);
+  if (s != KVQ_OK) return s;
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVQ_ERR_WORKSPACE;
+  if (workspace_bytes < plan.total) return KVQ_ERR_WORKSPACE;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  GenParams p{};
+  p.q = q; p.k_codes = k_codes; p.k_scale = k_scale; p.k_zero = k_zero;
+  p.v_codes = v_codes; p.v_scale = v_scale; p.v_zero = v_zero;
+  p.seq_lens = seq_lens; p.page_table = page_table; p.dev_status = dev_status;
+  p.part_lse = reinterpret_cast<float*>(ws + plan.part_lse);
+  p.part_o = reinterpret_cast<float*>(ws + plan.part_o);
+  p.batch = desc->batch; p.num_kv_heads = desc->cache.num_kv_heads; p.num_q_heads = desc->num_q_heads;
+  p.max_blocks = desc->max_blocks; p.num_pages = desc->cache.num_pages;
+  const int g = heads_per_kv(desc);
+  p.gq = g < kGroupQ ? g : kGroupQ;
+  p.units_per_seq = units_per_seq(desc);
+  p.kv_shift = g > kGroupQ ? 1 : 0;
+  p.group = group_of(&desc->cache);
+  p.splits = plan.splits;
+  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.flags = desc->flags;
+  p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
+  p.nibble_mul = 1u << 28;
+  p.minus_one = 0xffffffffu;
+  const int grid = desc->batch * p.units_per_seq * plan.splits;
+  cudaError_t e = launch_decode_general(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme,
+                                        desc->cache.head_dim, p, grid, plan.launch.smem, st);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  e = launch_merge(p.part_o, p.part_lse, desc->batch * desc->num_q_heads, plan.splits, desc->cache.head_dim, out, lse,
+                   st);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 }  // namespace
@@ -226,8 +306,14 @@ KVQ_API kvq_status kvq_dequant(const kvq_cache_desc* cache, int32_t which, const
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* bytes) {
   kvq_status s = check_attn(desc);
   if (s != KVQ_OK) return s;
-  if (!default_geometry(&desc->cache)) return KVQ_ERR_UNSUPPORTED;
   if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (!default_geometry(&desc->cache)) {
+    GeneralPlan plan;
+    s = general_plan(desc, &plan);
+    if (s != KVQ_OK) return s;
+    *bytes = plan.total;
+    return KVQ_OK;
+  }
   int sm = 0;
   if (desc->num_ctas == 0) {
     s = check_device(&sm);
@@ -245,7 +331,6 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
                                    size_t workspace_bytes, uint32_t* dev_status, void* stream) {
   kvq_status s = check_attn(desc);
   if (s != KVQ_OK) return s;
-  if (!default_geometry(&desc->cache)) return KVQ_ERR_UNSUPPORTED;
   // cache arrays are read with 16-byte bulk copies; the rest with scalar accesses
   const void* bulk[] = {k_codes, k_scale, k_zero, v_codes, v_scale, v_zero};
   for (const void* ptr : bulk)
@@ -260,11 +345,15 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
   int sm = 0;
   s = check_device(&sm);
   if (s != KVQ_OK) return s;
+  const float sm_scale = desc->sm_scale > 0.0f ? desc->sm_scale : 1.0f / std::sqrt((float)desc->cache.head_dim);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!default_geometry(&desc->cache)) return decode_general(desc, q, k_codes, k_scale, k_zero, v_codes, v_scale,
+                                                             v_zero, seq_lens, page_table, out, lse, workspace,
+                                                             workspace_bytes, dev_status, sm_scale, st);
   const int ctas = resolve_ctas(desc, sm);
   const WorkspaceLayout w = workspace_layout(desc->batch, units_per_seq(desc), ctas);
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVQ_ERR_WORKSPACE;
   if (workspace_bytes < w.total) return KVQ_ERR_WORKSPACE;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   if (cudaMemsetAsync(ws + w.counters, 0, (size_t)desc->batch * units_per_seq(desc) * kCounterGroups * sizeof(int),
                       st) !=
@@ -285,7 +374,6 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
     p.units_per_seq = units_per_seq(desc);
     p.kv_shift = g > kGroupQ ? 1 : 0;
   }
-  const float sm_scale = desc->sm_scale > 0.0f ? desc->sm_scale : 1.0f / std::sqrt((float)kHeadDim);
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.flags = desc->flags;
   p.nibble_mul = 1u << 28;

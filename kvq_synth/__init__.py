@@ -44,6 +44,7 @@ class Workload:
     paged: bool = False
     ragged: Optional[tuple] = None  # (lo, hi) log-uniform lengths
     description: str = ""
+    group: int = 128  # elements per quantization group (channels of a token, or tokens of a channel)
 
 
 WORKLOADS = {
@@ -63,6 +64,20 @@ WORKLOADS = {
                                   description="64 sequences, lengths log-uniform in [1K, 128K], "
                                               "128-token pages in a shuffled page table; INT2 "
                                               "K channel-wise, V token-wise"),
+    # cache geometries beyond head dim 128 / groups of 128
+    "b32_l32k_d256_g64_int4": Workload("b32_l32k_d256_g64_int4", 32, 8, 32, 256, 32768, 4, CHANNELWISE,
+                                       TOKENWISE, group=64,
+                                       description="B=32, Hkv=8, Hq=32, D=256, L=32768; INT4 K channel-wise, "
+                                                   "V token-wise; groups of 64 (channels of a token, tokens of "
+                                                   "a channel)"),
+    "b32_l32k_d64_g32_int2": Workload("b32_l32k_d64_g32_int2", 32, 8, 32, 64, 32768, 2, CHANNELWISE,
+                                      TOKENWISE, group=32,
+                                      description="B=32, Hkv=8, Hq=32, D=64, L=32768; INT2 K channel-wise, "
+                                                  "V token-wise; groups of 32"),
+    "b32_l32k_d128_g32_int2": Workload("b32_l32k_d128_g32_int2", 32, 8, 32, 128, 32768, 2, CHANNELWISE,
+                                       TOKENWISE, group=32,
+                                       description="B=32, Hkv=8, Hq=32, D=128, L=32768; INT2 K channel-wise, "
+                                                   "V token-wise; groups of 32"),
 }
 
 

@@ -1,0 +1,110 @@
+"""Decode attention on the general cache geometry (head dims 64 / 256, groups
+of 32 / 64 elements, and groups of 32 / 64 with head dim 128) against the
+oracle: every bit width and K/V scheme pair, query heads per KV head 1 / 2 /
+4 / 8, ragged and empty sequences, paged caches, block ranges split one way
+and many ways, an explicit softmax scale and the stall hook (the static
+entry point on this geometry: tests/test_zz_no_alloc.py).  Accumulator folds per quantization group follow the
+rag-lover.com summary of arXiv 2611.09722, section "限界と未検証の範囲"."""
+import numpy as np
+import pytest
+import kvq_synth as synth
+from kvq_testlib import assert_attention_close, make_problem, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+GEOMETRIES = [(64, 32), (64, 64), (128, 32), (128, 64), (256, 32), (256, 64), (256, 128)]
+PAIRS = [(0, 0), (0, 1), (1, 0), (1, 1)]
+
+
+def _w(D, G, bits, ks, vs, B=3, Hkv=2, Hq=8, L=300, paged=False):
+    return synth.Workload(f"geom_d{D}_g{G}", B, Hkv, Hq, D, L, bits, ks, vs, paged=paged, group=G)
+
+
+@pytest.mark.parametrize("D,G", GEOMETRIES)
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("ks,vs", PAIRS)
+def test_decode_geometry_parity(D, G, bits, ks, vs):
+    w = _w(D, G, bits, ks, vs, paged=(D + G + bits) % 2 == 0)
+    pb = make_problem(w, 300 + D + G + bits + 2 * ks + vs, lens=[300, 129, 1])
+    res = run_gpu(pb)
+    assert res["status"] == 0
+    assert_attention_close(pb, res, 0)
+
+
+@pytest.mark.parametrize("D,G", [(64, 32), (256, 64)])
+@pytest.mark.parametrize("heads", [1, 2, 8])
+def test_decode_geometry_gqa(D, G, heads):
+    w = _w(D, G, 4, 1, 0, B=2, Hkv=2, Hq=2 * heads)
+    pb = make_problem(w, 40 + heads, lens=[257, 90])
+    res = run_gpu(pb)
+    assert res["status"] == 0
+    assert_attention_close(pb, res, 0)
+
+
+@pytest.mark.parametrize("D,G,ks,vs", [(256, 32, 0, 0), (64, 64, 1, 1), (128, 32, 1, 0)])
+def test_decode_geometry_splits(D, G, ks, vs):
+    """One range per unit, the default split and one block per range give the
+    oracle's result.  The merge is exact up to rounding, but each range
+    prescales P' from its own running maximum, so the E4M3 roundings -- not
+    the results -- differ between splits: they agree to the operand error."""
+    w = _w(D, G, 2, ks, vs, B=2, Hkv=1, Hq=4, L=5000, paged=True)
+    pb = make_problem(w, 77, lens=[5000, 1700])
+    outs = []
+    for n in (1, 0, 100000):
+        res = run_gpu(pb, num_ctas=n)
+        assert res["status"] == 0
+        assert_attention_close(pb, res, 0)
+        outs.append(res["out"])
+    rms = float(np.sqrt((outs[0] ** 2).mean()))
+    assert np.abs(outs[0] - outs[2]).max() <= 3e-3 * rms
+
+
+@pytest.mark.parametrize("lens", [[0, 0], [0, 5], [128, 0, 256]])
+def test_decode_geometry_empty_and_exact_blocks(lens):
+    w = _w(64, 32, 4, 0, 1, B=len(lens), Hkv=1, Hq=4, L=max(lens) or 1)
+    pb = make_problem(w, 5, lens=lens)
+    res = run_gpu(pb)
+    assert res["status"] == 0
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert np.all(res["out"][b] == 0) and np.all(np.isneginf(res["lse"][b]))
+    assert_attention_close(pb, res, 0)
+
+
+@pytest.mark.parametrize("D,G", [(256, 64), (64, 32)])
+@pytest.mark.parametrize("mult", [0.57, 3.4])
+def test_decode_geometry_sm_scale(D, G, mult):
+    """An explicit softmax scale: the same multiples of the default 1/sqrt(D)
+    as the head-dim-128 cases (0.05 and 0.3 there); score and lse errors grow
+    in proportion to the scale."""
+    w = _w(D, G, 2, 1, 0, B=2, Hkv=1, Hq=4)
+    pb = make_problem(w, 11, lens=[300, 40], sm_scale=mult / D ** 0.5)
+    res = run_gpu(pb)
+    assert res["status"] == 0
+    assert_attention_close(pb, res, 0)
+
+
+def test_decode_geometry_stall_reports_timeout():
+    """The stall hook withholds one block from one CTA: its wait runs out, the
+    call returns, and the timeout bit is set (nothing hangs)."""
+    import bit_quantized_kv_decode_gb300 as kvq
+    w = _w(64, 32, 4, 0, 0, B=1, Hkv=1, Hq=4)
+    pb = make_problem(w, 3, lens=[300])
+    res = run_gpu(pb, flags=kvq.FLAG_TEST_STALL)
+    assert res["status"] & kvq.DEV_TIMEOUT
+    res = run_gpu(pb)  # the context is still usable
+    assert res["status"] == 0
+    assert_attention_close(pb, res, 0)
+
+
+def test_decode_geometry_unsupported_modes():
+    import bit_quantized_kv_decode_gb300 as kvq
+    from bit_quantized_kv_decode_gb300 import _lib
+    w = _w(64, 32, 2, 0, 0, B=1, Hkv=1, Hq=4)
+    pb = make_problem(w, 3, lens=[100])
+    with pytest.raises(_lib.KvqError) as e:
+        run_gpu(pb, mode=kvq.OPERANDS_BF16)
+    assert e.value.status == 2
+    with pytest.raises(_lib.KvqError):
+        run_gpu(pb, flags=kvq.FLAG_E2M1_V)
+

@@ -40,7 +40,8 @@ def _oracle_unit(w, c, b, h, ks, vs, dev):
     k = synth.kv_unit(w, SEED, 0, b, h, n, dev, cs[h]).cpu().numpy()[None, None]
     v = synth.kv_unit(w, SEED, 1, b, h, n, dev).cpu().numpy()[None, None]
     qb = c["q"][b:b + 1, 4 * h:4 * h + 4].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
-    ref = orc.reference_decode(qb, k, v, np.array([n], dtype=np.int32), w.bits, ks, vs, None, (n + 127) // 128)
+    ref = orc.reference_decode(qb, k, v, np.array([n], dtype=np.int32), w.bits, ks, vs, None, (n + 127) // 128,
+                               group=w.group)
     return ref["out"][0], ref["lse"][0]
 
 
@@ -51,6 +52,10 @@ def _oracle_unit(w, c, b, h, ks, vs, dev):
     ("b128_l32k_int2", 1, 0),
     ("b128_l32k_int2", 1, 1),
     ("paged_ragged_int2", 1, 0),
+    ("b32_l32k_d256_g64_int4", 1, 0),
+    ("b32_l32k_d128_g32_int2", 1, 0),
+    ("b32_l32k_d64_g32_int2", 1, 0),
+    ("b32_l32k_d64_g32_int2", 0, 1),
 ])
 def test_full_size_sampled_units(wl, ks, vs):
     import bit_quantized_kv_decode_gb300 as kvq

@@ -54,6 +54,29 @@ def test_static_scratch_matches_workspace_entry_point_twice():
         assert_attention_close(pb, {"out": o.numpy(), "lse": l_.numpy()}, 0)
 
 
+def test_static_scratch_general_geometry_twice():
+    """Head dim 256 with groups of 32 (the block-range kernel, whose scratch
+    holds per-range partial results): two calls in a row match the
+    workspace entry point and the oracle."""
+    import bit_quantized_kv_decode_gb300 as kvq
+    w = synth.Workload("geom_d256_g32", 2, 2, 8, 256, 300, 4, 1, 1, group=32)
+    pb = make_problem(w, seed=8, lens=[300, 77])
+    dev = torch.device("cuda")
+    res = run_gpu(pb)
+    assert res["status"] == 0
+    ref_o = torch.tensor(res["out"])
+    rms = float(ref_o.pow(2).mean().sqrt())
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(2):
+        out, lse = kvq.decode_attn_static(res["desc"], pb.q.to(dev), res["k_cache"], res["v_cache"],
+                                          pb.lens.to(dev), None, pb.max_blocks, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        o = out.cpu().double()
+        assert float((o - ref_o).abs().max()) <= 1e-5 * rms
+        assert_attention_close(pb, {"out": o.numpy(), "lse": lse.cpu().double().numpy()}, 0)
+
+
 def test_static_scratch_rejects_oversized_calls():
     import bit_quantized_kv_decode_gb300 as kvq
     from bit_quantized_kv_decode_gb300 import _lib

@@ -1,0 +1,623 @@
+// Decode attention for the cache geometries the specialised kernel does not
+// take: head dims 64 and 256, groups of 32 or 64 elements (with any head
+// dim).  One warpgroup per CTA runs every step of a 128-token block in turn
+// -- bulk copies into a ring of stages, codes to E4M3 operands in tensor
+// memory, Q' and P' operands in shared memory, tcgen05 MMAs with the
+// accumulators in tensor memory, the affine folds and an online softmax --
+// over a contiguous range of one (sequence, unit)'s blocks; the ranges'
+// partial results are merged by log-sum-exp afterwards.  Tensor memory is
+// kept small (operand and accumulator regions reused within a block) so that
+// several CTAs share an SM and hide one another's latencies.
+//
+// Folds per quantization group (rag-lover.com summary of arXiv 2611.09722,
+// "限界と未検証の範囲": accumulator folds are applied one group at a time;
+// "解説": which side each scheme folds on):
+//   * token-wise K (groups of G channels): the K-steps of each channel group
+//     accumulate into their own 16-column score block, and the softmax adds
+//     s_(l,g) * partial_g + z_(l,g) * sum_(c in g) q_c;
+//   * channel-wise K (groups of G tokens): Q'_g = q * s_g for each token
+//     group g, stacked along N; token l reads the block of its group, plus
+//     q . z_g;
+//   * token-wise V: P'_g = p * s_(l,g) for each channel group, stacked along
+//     N; channel c reads the block of its group, plus sum_l p_l z_(l,g);
+//   * channel-wise V: the K-steps of each token group accumulate into their
+//     own output block: O += s_g * partial_g + z_g * sum_(l in g) p_l.
+#pragma once
+#include "decode.cuh"
+#include "decode_general.h"
+
+namespace kvq {
+namespace gen {
+
+constexpr int kThreads = 128;
+
+// Byte offset of row p, 16-column block nb of a B operand with nb16 blocks
+// (MN-major, no swizzle: core matrices of 8 rows x 16 bytes; K-direction
+// stride nb16 * 128, N-direction stride 128).
+__device__ __forceinline__ uint32_t b_off(int p, int nb, int nb16) {
+  return (uint32_t)((p >> 3) * (nb16 * 128) + nb * 128 + (p & 7) * 16);
+}
+
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
+// The 12 used columns of a 16-column block (4 heads x 3 parts).
+__device__ __forceinline__ void ld_block(uint32_t taddr, uint32_t (&v)[12]) {
+  tmem_ld_32x32b_x8(taddr, v);
+  tmem_ld_32x32b_x4(taddr + 8, v + 8);
+}
+// Sum of the three parts of head h.
+__device__ __forceinline__ float parts3(const uint32_t (&v)[12], int h) {
+  return (__uint_as_float(v[h]) + __uint_as_float(v[4 + h])) + __uint_as_float(v[8 + h]);
+}
+
+// Warp reduction of N values per lane at once (sum or max), halving the
+// values held at each exchange: afterwards lane l holds the warp's result for
+// value l >> (5 - log2 N).  N - 1 + (5 - log2 N) shuffles instead of 5 N.
+template <int N, bool MAX>
+__device__ __forceinline__ float warp_reduce_t(float (&v)[N]) {
+  static_assert(N == 1 || N == 2 || N == 4 || N == 8 || N == 16 || N == 32, "N");
+  const int lane = threadIdx.x & 31;
+  int o = 16;
+#pragma unroll
+  for (int n = N; n > 1; n >>= 1, o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      const float got = __shfl_xor_sync(FULL, send, o);
+      v[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (; o > 0; o >>= 1) {
+    const float got = __shfl_xor_sync(FULL, r, o);
+    r = MAX ? fmaxf(r, got) : r + got;
+  }
+  return r;
+}
+// ... and the per-warp results into buf[warp][N] (one lane per value).
+template <int N, bool MAX>
+__device__ __forceinline__ void warp_reduce_store(float (&v)[N], float* buf) {
+  constexpr int kLog = N == 1 ? 0 : N == 2 ? 1 : N == 4 ? 2 : N == 8 ? 3 : N == 16 ? 4 : 5;
+  const float r = warp_reduce_t<N, MAX>(v);
+  const int lane = threadIdx.x & 31;
+  if ((lane & ((32 >> kLog) - 1)) == 0) buf[(threadIdx.x >> 5) * N + (lane >> (5 - kLog))] = r;
+}
+// Block-wide result i from buf[4][N] (after a barrier).
+template <int N>
+__device__ __forceinline__ float sum4(const float* buf, int i) {
+  return (buf[i] + buf[N + i]) + (buf[2 * N + i] + buf[3 * N + i]);
+}
+template <int N>
+__device__ __forceinline__ float max4(const float* buf, int i) {
+  return fmaxf(fmaxf(buf[i], buf[N + i]), fmaxf(buf[2 * N + i], buf[3 * N + i]));
+}
+
+// Thread 0 waits (bounded) for the phase; the whole CTA learns the outcome,
+// so that a wait that runs out leaves every thread on the same path.
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* ok_flag, uint64_t limit) {
+  if (threadIdx.x == 0) *ok_flag = mbar_wait_bounded(bar, parity, nullptr, limit) ? 1 : 0;
+  __syncthreads();
+  const bool ok = *ok_flag != 0;
+  if (ok && threadIdx.x != 0) (void)mbar_try_wait(bar, parity);  // completed: observe it in every thread
+  return ok;
+}
+
+// Codes of `chunks` 16-byte chunks of row `row` (chunk-major block layout
+// with `nrows` rows) -> E4M3 operand words in tensor memory from column col.
+template <int BITS, int CHUNKS>
+__device__ __forceinline__ void convert_row(const unsigned char* blk, int nrows, int row, uint32_t taddr, uint32_t mul,
+                                            uint32_t m1) {
+  using Cv = Convert<BITS, false>;
+#pragma unroll
+  for (int c = 0; c < CHUNKS; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(blk + ((size_t)c * nrows + row) * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) Cv::run(w[i], &o[i * Cv::kOut], mul, m1);
+#pragma unroll
+    for (int q8 = 0; q8 < Cv::kOut / 2; ++q8)  // a chunk gives 32 / BITS columns
+      tmem_st_x8(taddr + c * (32 / BITS) + 8 * q8, &o[8 * q8]);
+  }
+}
+
+template <int BITS, bool KCW, bool VCW, int D, int G>
+__global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenParams p, int stages) {
+  constexpr int kKBytes = kBlockTokens * D * BITS / 8;  // K (and V) codes of a block
+  constexpr int kHalves = D > 128 ? 2 : 1;              // M = 128 halves of the channels
+  constexpr int kQv = (D + 127) / 128;                  // channels per thread
+  constexpr int NGC = D / G;                            // channel groups (token-wise)
+  constexpr int NGT = kBlockTokens / G;                 // token groups (channel-wise)
+  constexpr int NBQ = KCW ? NGT : 1;                    // 16-column blocks of Q' / of S with channel-wise K
+  constexpr int NBP = VCW ? 1 : NGC;                    // of P'
+  constexpr int NBO = VCW ? NGT : NGC;                  // of O per channel half
+  constexpr int NSZ = kBlockTokens * D / G;
+  constexpr int NM = VCW ? 4 : 8;                       // values of the block-max reduction (+ largest V scale)
+  constexpr int NZ = VCW ? 4 : 4 * NGC;                 // values of the per-group p sums
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const GenLayout L = gen_layout(BITS, D, G, KCW, VCW, stages);  // shared-memory offsets (depend on stages)
+  constexpr GenLayout LT = gen_layout(BITS, D, G, KCW, VCW, 2);  // tensor-memory columns (do not)
+  constexpr bool kSeq = LT.seq_halves;
+
+  unsigned char* qop = smem + L.q_off;  // [D rows][NBQ blocks]
+  unsigned char* pop = smem + L.p_off;  // [128 rows][NBP blocks]
+  float* red_c = reinterpret_cast<float*>(smem + L.scratch_off);  // [4][16] q . z_g (channel-wise K)
+  float* red_m = red_c + 64;                                      // [4][8] block maxima
+  float* red_z = red_m + 32;                                      // [4][32] per-group p (z) sums
+  uint32_t* eg_w = reinterpret_cast<uint32_t*>(red_z + 128);      // [4][4] per-warp largest K scale of group g
+  uint64_t* bars = reinterpret_cast<uint64_t*>(eg_w + 16);        // stages [4], mma, drain
+  uint32_t* tbase = reinterpret_cast<uint32_t*>(bars + 6);
+  int* ok_flag = reinterpret_cast<int*>(tbase + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  const int unit = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
+  const int b = unit / p.units_per_seq, uh = unit % p.units_per_seq, kvh = uh >> p.kv_shift;
+  int len = p.seq_lens[b];
+  if (len < 0 || len > p.max_blocks * kBlockTokens) {
+    if (split == 0 && uh == 0 && tid == 0) report(p.dev_status, KVQ_DEV_BAD_SEQ_LEN);
+    len = 0;
+  }
+  const int nblk = (len + kBlockTokens - 1) / kBlockTokens;
+  const int j0 = (int)((long long)split * nblk / p.splits), j1 = (int)((long long)(split + 1) * nblk / p.splits);
+  const size_t row0 = (size_t)b * p.num_q_heads + (size_t)uh * p.gq;  // first query head of the unit
+
+  if (j1 <= j0) {  // no block in this range: an empty part (weight 0 in the merge)
+    for (int k = 0; k < p.gq; ++k) {
+      for (int c = tid; c < D; c += kThreads) p.part_o[((row0 + k) * p.splits + split) * D + c] = 0.f;
+      if (tid == 0) p.part_lse[(row0 + k) * p.splits + split] = -INFINITY;
+    }
+    return;
+  }
+
+  if (tid == 0) {
+    for (int i = 0; i < stages + 2; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  for (int i = tid; i < (L.scratch_off - L.q_off) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(qop)[i] = make_uint4(0u, 0u, 0u, 0u);  // unused operand columns stay zero
+  if (warp == 0) {
+    tmem_alloc(tbase, (uint32_t)LT.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tbase;
+  const uint32_t t_a = tmem + lane_off + LT.col_a;    // this warp's lanes of the operand region
+  const uint32_t t_so = tmem + lane_off + LT.col_so;  // ... of the S / O region
+  uint64_t* mma_bar = &bars[stages];
+  uint64_t* drain_bar = &bars[stages + 1];
+
+  const uint64_t limit = p.wait_limit_ns;
+  int pend[4] = {-1, -1, -1, -1};  // thread 0: block whose copy into stage s is in flight
+  auto load = [&](int j, int s) {  // thread 0: block j of the unit into stage s
+    int page = p.page_table ? p.page_table[(size_t)b * p.max_blocks + j] : b * p.max_blocks + j;
+    if (page < 0 || page >= p.num_pages) {
+      report(p.dev_status, KVQ_DEV_BAD_PAGE);
+      page = 0;
+    }
+    const size_t blk = (size_t)page * p.num_kv_heads + kvh;
+    unsigned char* st = smem + s * L.stage_bytes;
+    constexpr uint32_t szb = (uint32_t)NSZ * 2;
+    mbar_arrive_expect_tx(&bars[s], (uint32_t)L.stage_bytes);
+    bulk_g2s(st, p.k_codes + blk * kKBytes, kKBytes, &bars[s]);
+    bulk_g2s(st + kKBytes, p.v_codes + blk * kKBytes, kKBytes, &bars[s]);
+    unsigned char* sz = st + 2 * kKBytes;
+    bulk_g2s(sz, p.k_scale + blk * NSZ, szb, &bars[s]);
+    bulk_g2s(sz + szb, p.k_zero + blk * NSZ, szb, &bars[s]);
+    bulk_g2s(sz + 2 * szb, p.v_scale + blk * NSZ, szb, &bars[s]);
+    bulk_g2s(sz + 3 * szb, p.v_zero + blk * NSZ, szb, &bars[s]);
+    pend[s] = j;
+  };
+  if (tid == 0) {
+    for (int i = 0; i < stages && j0 + i < j1; ++i) {
+      if (i == 0 && (p.flags & KVQ_FLAG_TEST_STALL) && blockIdx.x == 0) continue;  // test hook: withhold one block
+      load(j0 + i, i);
+    }
+  }
+
+  // ---- per-unit query statistics (all 4 head slots; empty slots are 0)
+  const uint16_t* qb = p.q + row0 * D;
+  float qv[4][kQv];  // q of this thread's channels c = tid + 128 i
+  float qmax[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < kQv; ++i) {
+      const int c = tid + 128 * i;
+      qv[h][i] = (h < p.gq && c < D) ? bf2f(qb[h * D + c]) : 0.f;
+      m = fmaxf(m, fabsf(qv[h][i]));
+    }
+    qmax[h] = m;
+  }
+  {
+    float t[4] = {qmax[0], qmax[1], qmax[2], qmax[3]};
+    warp_reduce_store<4, true>(t, red_m);
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < 4; ++h) qmax[h] = max4<4>(red_m, h);
+  }
+  float mult[4];  // partial-score multiplier (log2 units)
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+    mult[h] = 512.0f * (KCW ? pow2_head_inv(qmax[h]) : pow2_prescale_inv(qmax[h])) * p.sm_scale_log2;
+  float qsz[NGC][4];  // token-wise K: sum of q over channel group g, times the log2 softmax scale
+  if (!KCW) {
+    // Q' = q * 2^k (k per head) in three E4M3 parts at row a_pos(c); and the
+    // per-channel-group sums of q for the offset term
+#pragma unroll
+    for (int i = 0; i < kQv; ++i) {
+      const int c = tid + 128 * i;
+      if (c < D) {
+        const float f = odd_quarter<BITS, false>(c);
+        const float4 v = make_float4(qv[0][i] * pow2_prescale(qmax[0]) * f, qv[1][i] * pow2_prescale(qmax[1]) * f,
+                                     qv[2][i] * pow2_prescale(qmax[2]) * f, qv[3][i] * pow2_prescale(qmax[3]) * f);
+        *reinterpret_cast<uint4*>(qop + b_off(a_pos<BITS, false>(c), 0, 1)) = split3_e4m3(v);
+      }
+    }
+    float t[4 * NGC];
+#pragma unroll
+    for (int g = 0; g < NGC; ++g)
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < kQv; ++i)
+          if ((tid + 128 * i) / G == g && tid + 128 * i < D) s += qv[h][i];
+        t[g * 4 + h] = s;
+      }
+    warp_reduce_store<4 * NGC, false>(t, red_z);
+    fence_proxy_async_smem();
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < NGC; ++g)
+#pragma unroll
+      for (int h = 0; h < 4; ++h) qsz[g][h] = sum4<4 * NGC>(red_z, g * 4 + h) * p.sm_scale_log2;
+  }
+  float qk[4][kQv];  // channel-wise K: q * 2^(6 - E_q)
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+#pragma unroll
+    for (int i = 0; i < kQv; ++i) qk[h][i] = qv[h][i] * pow2_head(qmax[h]);
+
+  float m_run[4], l_thr[4], oacc[kHalves][4], zacc[kHalves][4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    m_run[h] = -INFINITY;
+    l_thr[h] = 0.f;
+#pragma unroll
+    for (int hf = 0; hf < kHalves; ++hf) oacc[hf][h] = zacc[hf][h] = 0.f;
+  }
+
+  bool ok = true;
+  uint32_t mma_phase = 0u;
+  for (int j = j0; j < j1; ++j) {
+    const int s = (j - j0) % stages;
+    if (!cta_wait(&bars[s], (uint32_t)((j - j0) / stages) & 1u, ok_flag, limit)) { ok = false; break; }
+    const unsigned char* st = smem + s * L.stage_bytes;
+    const uint16_t* ksz = reinterpret_cast<const uint16_t*>(st + 2 * kKBytes);
+    const uint16_t* kzz = ksz + NSZ;
+    const uint16_t* vsz = kzz + NSZ;
+    const uint16_t* vzz = vsz + NSZ;
+    const int nv = min(kBlockTokens, len - j * kBlockTokens);  // valid tokens of the block
+    const int l = tid;
+    const bool valid = l < nv;
+
+    // ---- K codes -> E4M3 operand (rows = tokens)
+    convert_row<BITS, D * BITS / 128>(st, kBlockTokens, tid, t_a, p.nibble_mul, p.minus_one);
+    tc_wait_st();
+
+    // ---- channel-wise K: Q'_g = q * s_g per token group g, and q . z_g
+    if (KCW) {
+      {
+        uint32_t mx[NGT];
+#pragma unroll
+        for (int g = 0; g < NGT; ++g) {
+          uint32_t m = 0u;  // fp16 bits of non-negative values order as integers
+#pragma unroll
+          for (int i = 0; i < kQv; ++i)
+            if (tid + 128 * i < D) m = max(m, (uint32_t)ksz[g * D + tid + 128 * i]);
+          mx[g] = __reduce_max_sync(FULL, m);
+        }
+        if ((tid & 31) == 0)
+#pragma unroll
+          for (int g = 0; g < NGT; ++g) eg_w[warp * 4 + g] = mx[g];
+      }
+      float t[4 * NGT];
+#pragma unroll
+      for (int k = 0; k < 4 * NGT; ++k) t[k] = 0.f;
+      __syncthreads();
+#pragma unroll
+      for (int g = 0; g < NGT; ++g) {
+        const uint32_t e16 = f16_exp_field(max(max(eg_w[g], eg_w[4 + g]), max(eg_w[8 + g], eg_w[12 + g])));
+        const float fg = pow2_group(e16);
+#pragma unroll
+        for (int i = 0; i < kQv; ++i) {
+          const int c = tid + 128 * i;
+          if (c < D) {
+            const float f = h2f(ksz[g * D + c]) * fg * odd_quarter<BITS, false>(c);
+            const float4 v = make_float4(qk[0][i] * f, qk[1][i] * f, qk[2][i] * f, qk[3][i] * f);
+            *reinterpret_cast<uint4*>(qop + b_off(a_pos<BITS, false>(c), g, NGT)) = split3_e4m3(v);
+            const float zgc = h2f(kzz[g * D + c]);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) t[g * 4 + h] = fmaf(qv[h][i], zgc, t[g * 4 + h]);
+          }
+        }
+      }
+      warp_reduce_store<4 * NGT, false>(t, red_c);
+      fence_proxy_async_smem();
+    }
+
+    // ---- QK^T: S[token][column block] (swap-AB: tokens are the M = 128 rows)
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      constexpr uint32_t idesc_q = make_idesc(0, 0, 0, 1, 128, 16 * NBQ);
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) {
+        const uint64_t bd = make_smem_desc(smem_u32(qop) + k * 4 * NBQ * 128, NBQ * 128, 128);
+        const uint32_t a = tmem + LT.col_a + 8 * k;
+        if (KCW) {
+          mma_f8f6f4_ts(tmem + LT.col_so, a, bd, idesc_q, k > 0);
+        } else {  // the K-steps of channel group g accumulate into S block g
+          mma_f8f6f4_ts(tmem + LT.col_so + 16 * ((32 * k) / G), a, bd, idesc_q, (32 * k) % G != 0);
+        }
+      }
+      tc_commit(mma_bar);
+    }
+    // while QK^T runs: the largest V scale of this token (token-wise V)
+    float vmax = 0.f;
+    if (!VCW && valid) {
+#pragma unroll
+      for (int g = 0; g < NGC; ++g) vmax = fmaxf(vmax, h2f(vsz[l * NGC + g]));
+    }
+    if (!cta_wait(mma_bar, mma_phase, ok_flag, limit)) { ok = false; break; }
+    mma_phase ^= 1u;
+    tc_fence_after();
+
+    // ---- scores of token l (log2 units), folded per group
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (KCW) {
+      const int g = l / G;  // warp-uniform (G >= 32)
+      uint32_t v[12];
+      ld_block(t_so + 16 * g, v);
+      const uint32_t e16 = f16_exp_field(max(max(eg_w[g], eg_w[4 + g]), max(eg_w[8 + g], eg_w[12 + g])));
+      const float fs = pow2_group_inv(e16);
+      float cz[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) cz[h] = sum4<4 * NGT>(red_c, g * 4 + h) * p.sm_scale_log2;
+      tc_wait_ld();
+#pragma unroll
+      for (int h = 0; h < 4; ++h) sc[h] = fmaf(parts3(v, h), mult[h] * fs, cz[h]);
+    } else {
+#pragma unroll
+      for (int g = 0; g < NGC; ++g) {
+        uint32_t v[12];
+        ld_block(t_so + 16 * g, v);
+        const float s_lg = h2f(ksz[l * NGC + g]), z_lg = h2f(kzz[l * NGC + g]);
+        tc_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 4; ++h) sc[h] += fmaf(parts3(v, h) * mult[h], s_lg, z_lg * qsz[g][h]);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 4; ++h) sc[h] = valid ? sc[h] : -INFINITY;
+
+    // ---- V codes -> E4M3 operand (rows = channels), replacing the K codes
+    //      (QK^T is complete).  A 64-dim head leaves rows 64..127 as they are:
+    //      output row m depends on operand row m alone, and rows >= D are
+    //      never read.
+#pragma unroll
+    for (int hf = 0; hf < kHalves; ++hf)
+      if (hf * 128 + tid < D)  // warp-uniform
+        convert_row<BITS, BITS>(st + kKBytes, D, hf * 128 + tid, t_a + 32 * hf, p.nibble_mul, p.minus_one);
+
+    // ---- online softmax over the block: block maxima (and the largest V scale)
+    {
+      float t[NM];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) t[h] = sc[h];
+#pragma unroll
+      for (int k = 4; k < NM; ++k) t[k] = vmax;
+      warp_reduce_store<NM, true>(t, red_m);
+    }
+    tc_wait_st();
+    __syncthreads();
+    float bmax[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) bmax[h] = max4<NM>(red_m, h);
+    const int e_v = VCW ? 0 : (int)((__float_as_uint(max4<NM>(red_m, 4)) >> 23) & 0xffu) - 127;
+    float alpha[4], pr[4];
+    int pe[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float mn = fmaxf(m_run[h], bmax[h]);
+      alpha[h] = ex2(m_run[h] - mn);
+      m_run[h] = mn;
+      pr[h] = valid ? ex2(sc[h] - mn) : 0.f;
+      pe[h] = p_exponent(bmax[h] - mn, e_v);  // P' prescale 2^(6 - E)
+      l_thr[h] = fmaf(l_thr[h], alpha[h], pr[h]);
+    }
+
+    // per-group sums: token-wise V: sum_l p_l z_(l,g) per channel group;
+    // channel-wise V: sum_(l in g) p_l per token group (a warp's tokens lie in one group)
+    {
+      float t[NZ];
+      if (!VCW) {
+#pragma unroll
+        for (int g = 0; g < NGC; ++g) {
+          const float z_lg = valid ? h2f(vzz[l * NGC + g]) : 0.f;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) t[g * 4 + h] = pr[h] * z_lg;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) t[h] = pr[h];
+      }
+      warp_reduce_store<NZ, false>(t, red_z);
+    }
+
+    // ---- P' operand: row a_pos(l), one 16-column block per channel group (token-wise V)
+    {
+      const float oq = odd_quarter<BITS, false>(l);
+      float ps[4];
+#pragma unroll
+      for (int h = 0; h < 4; ++h) ps[h] = pr[h] * oq * __uint_as_float((uint32_t)(133 - pe[h]) << 23);
+#pragma unroll
+      for (int g = 0; g < NBP; ++g) {
+        const float sv = VCW ? 1.0f : (valid ? h2f(vsz[l * NGC + g]) : 0.f);
+        const float4 v = make_float4(ps[0] * sv, ps[1] * sv, ps[2] * sv, ps[3] * sv);
+        *reinterpret_cast<uint4*>(pop + b_off(a_pos<BITS, false>(l), g, NBP)) = split3_e4m3_via_f16(v);
+      }
+    }
+    fence_proxy_async_smem();
+
+    float pinv[4];  // 2^(E - 6) * 2^9 (the codes' E4M3 scale)
+#pragma unroll
+    for (int h = 0; h < 4; ++h) pinv[h] = __uint_as_float((uint32_t)(130 + pe[h]) << 23);
+
+    // ---- PV: O[channel][column block] per M = 128 half of the channels, then
+    //      the epilogue: channel c = 128 hf + tid; undo the P' prescale, fold V
+#pragma unroll
+    for (int pass = 0; pass < (kSeq ? kHalves : 1); ++pass) {
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (tid == 0) {
+#pragma unroll
+        for (int hf = 0; hf < kHalves; ++hf) {
+          if (kSeq && hf != pass) continue;
+          const uint32_t o = tmem + LT.col_so + (kSeq ? 0 : hf * 16 * NBO);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint32_t a = tmem + LT.col_a + 32 * hf + 8 * k;
+            if (VCW) {  // the K-steps of token group g accumulate into O block g
+              const uint64_t bd = make_smem_desc(smem_u32(pop) + k * 4 * 128, 128, 128);
+              mma_f8f6f4_ts(o + 16 * ((32 * k) / G), a, bd, make_idesc(0, 0, 0, 1, 128, 16), (32 * k) % G != 0);
+            } else {
+              const uint64_t bd = make_smem_desc(smem_u32(pop) + k * 4 * NGC * 128, NGC * 128, 128);
+              mma_f8f6f4_ts(o, a, bd, make_idesc(0, 0, 0, 1, 128, 16 * NGC), k > 0);
+            }
+          }
+        }
+        tc_commit(mma_bar);
+      }
+      if (!cta_wait(mma_bar, mma_phase, ok_flag, limit)) { ok = false; break; }
+      mma_phase ^= 1u;
+      tc_fence_after();
+#pragma unroll
+      for (int hf = 0; hf < kHalves; ++hf) {
+        if (kSeq && hf != pass) continue;
+        const int c = hf * 128 + tid;
+        const uint32_t o = t_so + (kSeq ? 0 : hf * 16 * NBO);
+        float add[4] = {0.f, 0.f, 0.f, 0.f};
+        if (VCW) {
+#pragma unroll
+          for (int g = 0; g < NGT; ++g) {
+            uint32_t v[12];
+            ld_block(o + 16 * g, v);
+            tc_wait_ld();
+            if (g * G >= nv || c >= D) continue;  // no valid token in this group / no such channel
+            const float s_gc = h2f(vsz[g * D + c]), z_gc = h2f(vzz[g * D + c]);
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              float psum = 0.f;  // sum of p over the group's tokens (the warps covering them)
+#pragma unroll
+              for (int w = 0; w < 4; ++w)
+                if ((32 * w) / G == g) psum += red_z[w * 4 + h];
+              add[h] = fmaf(s_gc, parts3(v, h) * pinv[h], fmaf(z_gc, psum, add[h]));
+            }
+          }
+        } else {
+          const int g = (c < D ? c : 0) / G;  // warp-uniform (G >= 32)
+          uint32_t v[12];
+          ld_block(o + 16 * g, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            add[h] = parts3(v, h) * pinv[h];
+            zacc[hf][h] = fmaf(zacc[hf][h], alpha[h], sum4<NZ>(red_z, g * 4 + h));
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) oacc[hf][h] = fmaf(oacc[hf][h], alpha[h], add[h]);
+      }
+    }
+    if (!ok) break;
+    tc_fence_before();
+    __syncthreads();  // stage s, Q', P', S / O and the reduction buffers are free again
+    if (tid == 0) {
+      pend[s] = -1;
+      if (j + stages < j1) load(j + stages, s);
+    }
+  }
+
+  // ---- this range's part: O / l and lse = m + ln l per head
+  if (ok) {
+    {
+      float t[4] = {l_thr[0], l_thr[1], l_thr[2], l_thr[3]};
+      warp_reduce_store<4, false>(t, red_m);
+    }
+    __syncthreads();
+    float l_run[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) l_run[h] = sum4<4>(red_m, h);
+#pragma unroll
+    for (int hf = 0; hf < kHalves; ++hf) {
+      const int c = hf * 128 + tid;
+      if (c < D) {
+        for (int k = 0; k < p.gq; ++k)
+          p.part_o[((row0 + k) * p.splits + split) * D + c] = (oacc[hf][k] + zacc[hf][k]) / l_run[k];
+      }
+    }
+    if (tid < p.gq)
+      p.part_lse[(row0 + tid) * p.splits + split] = (m_run[tid] + __log2f(l_run[tid])) * 0.69314718055994530942f;
+  } else if (tid == 0) {
+    report(p.dev_status, KVQ_DEV_TIMEOUT);
+  }
+  // leave no copy or MMA in flight: wait (bounded) for both, then release tensor memory
+  if (tid == 0) {
+    for (int s = 0; s < stages; ++s)
+      if (pend[s] >= 0)
+        (void)mbar_wait_bounded(&bars[s], (uint32_t)((pend[s] - j0) / stages) & 1u, nullptr, limit);
+    tc_commit(drain_bar);
+    (void)mbar_wait_bounded(drain_bar, 0u, nullptr, limit);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)LT.tmem_cols);
+  }
+}
+
+template <int BITS, bool KCW, bool VCW, int D, int G>
+cudaError_t launch_instance(const GenParams& p, int grid, const GenLaunch& shape, cudaStream_t stream) {
+  auto kern = decode_general_kernel<BITS, KCW, VCW, D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shape.smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, shape.smem, stream>>>(p, shape.stages);
+  return cudaGetLastError();
+}
+
+template <int BITS, int D, int G>
+cudaError_t launch_schemes(bool kcw, bool vcw, const GenParams& p, int grid, const GenLaunch& shape,
+                           cudaStream_t s) {
+  if (!kcw && !vcw) return launch_instance<BITS, false, false, D, G>(p, grid, shape, s);
+  if (!kcw && vcw) return launch_instance<BITS, false, true, D, G>(p, grid, shape, s);
+  if (kcw && !vcw) return launch_instance<BITS, true, false, D, G>(p, grid, shape, s);
+  return launch_instance<BITS, true, true, D, G>(p, grid, shape, s);
+}
+
+}  // namespace gen
+}  // namespace kvq

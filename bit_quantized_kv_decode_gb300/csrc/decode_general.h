@@ -22,7 +22,7 @@ struct GenParams {
   uint32_t* dev_status;
   int batch, num_kv_heads, num_q_heads, max_blocks, num_pages;
   int gq, units_per_seq, kv_shift;  // units of work, as in DecodeParams
-  int group, splits;                // G; block ranges per unit (grid = units * splits)
+  int splits;                       // block ranges per unit (grid = units * splits)
   float sm_scale_log2;
   uint32_t flags;
   uint64_t wait_limit_ns;
@@ -30,35 +30,44 @@ struct GenParams {
 };
 
 // Byte offsets in shared memory and column offsets in tensor memory.
+//   tensor memory: [A: K codes, then V codes of the block][S and O]
+//   (the V codes replace the K codes once QK^T is done; O replaces S once
+//   the scores are read), with the two M = 128 channel halves of a 256-dim
+//   head run one after the other when both would not fit in 256 columns.
 struct GenLayout {
   int nsz;          // s (and z) values per block: 128 * D / G
   int stage_bytes;  // K codes, V codes, K s, K z, V s, V z of one block
+  int stages;
   int q_off, p_off, scratch_off, total_bytes;
-  int col_ak, col_av, col_s, col_o, tmem_cols;
+  int col_a, col_so, tmem_cols;
+  bool seq_halves;  // PV one channel half at a time
 };
 
-__host__ __device__ inline GenLayout gen_layout(int bits, int D, int G, bool kcw, bool vcw) {
-  GenLayout L;
+constexpr int kGenScratchBytes = 1280;
+
+__host__ __device__ constexpr int gen_pow2_cols(int used) {
+  return used <= 32 ? 32 : used <= 64 ? 64 : used <= 128 ? 128 : used <= 256 ? 256 : 512;
+}
+
+__host__ __device__ constexpr GenLayout gen_layout(int bits, int D, int G, bool kcw, bool vcw, int stages) {
   const int halves = D > 128 ? 2 : 1, ngc = D / G, ngt = kBlockTokens / G;
-  L.nsz = kBlockTokens * D / G;
-  L.stage_bytes = 2 * (kBlockTokens * D * bits / 8) + 4 * L.nsz * 2;
-  L.q_off = 2 * L.stage_bytes;                             // two stages
-  L.p_off = L.q_off + D * 16 * (kcw ? ngt : 1);            // Q': D rows x (16-byte block per token group)
-  L.scratch_off = L.p_off + kBlockTokens * 16 * (vcw ? 1 : ngc);  // P': 128 rows x (block per channel group)
-  L.total_bytes = L.scratch_off + 512;                     // reductions, group sums, barriers
-  L.col_ak = 0;                                            // K operand: D / 4 columns
-  L.col_av = D / 4;                                        // V operand: 32 columns per channel half
-  L.col_s = L.col_av + 32 * halves;                        // S: 16 columns per block
-  L.col_o = L.col_s + 16 * (kcw ? ngt : ngc);              // O: 16 columns per block per half
-  const int used = L.col_o + halves * 16 * (vcw ? ngt : ngc);
-  int cols = 32;
-  while (cols < used) cols *= 2;
-  L.tmem_cols = cols;
-  return L;
+  const int a_cols = (D / 4 > 32 * halves) ? D / 4 : 32 * halves;
+  const int s_cols = 16 * (kcw ? ngt : ngc);
+  const int o_all = halves * 16 * (vcw ? ngt : ngc);
+  const bool seq = a_cols + (s_cols > o_all ? s_cols : o_all) > 256;
+  const int o_cols = seq ? o_all / halves : o_all;
+  const int nsz = kBlockTokens * D / G;
+  const int stage_bytes = 2 * (kBlockTokens * D * bits / 8) + 4 * nsz * 2;
+  const int q_off = stages * stage_bytes;
+  const int p_off = q_off + D * 16 * (kcw ? ngt : 1);  // Q': D rows x (16-byte block per token group)
+  const int scratch_off = p_off + kBlockTokens * 16 * (vcw ? 1 : ngc);  // P': 128 rows x (block per channel group)
+  return GenLayout{nsz, stage_bytes, stages, q_off, p_off, scratch_off, scratch_off + kGenScratchBytes, 0, a_cols,
+                   gen_pow2_cols(a_cols + (s_cols > o_cols ? s_cols : o_cols)), seq};
 }
 
 struct GenLaunch {
   int ctas_per_sm;  // resident CTAs per SM (tensor memory and shared memory)
+  int stages;       // copy-ring stages
   size_t smem;      // dynamic shared memory per CTA
 };
 
@@ -67,7 +76,7 @@ struct GenLaunch {
 GenLaunch general_launch_shape(int bits, int k_scheme, int v_scheme, int head_dim, int group, int smem_per_sm,
                                int smem_reserved_per_cta);
 
-cudaError_t launch_decode_general(int bits, int k_scheme, int v_scheme, int head_dim, const GenParams& p, int grid,
-                                  size_t smem, cudaStream_t stream);
+cudaError_t launch_decode_general(int bits, int k_scheme, int v_scheme, int head_dim, int group, const GenParams& p,
+                                  int grid, const GenLaunch& shape, cudaStream_t stream);
 
 }  // namespace kvq

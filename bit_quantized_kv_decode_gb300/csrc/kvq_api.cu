@@ -107,7 +107,10 @@ kvq_status check_attn(const kvq_attn_desc* d) {
 }
 
 // General geometry: block ranges per (sequence, unit) and the launch shape.
-// The grid aims at two waves of resident CTAs (or num_ctas CTAs when given).
+// With num_ctas = 0 the number of ranges per unit is chosen between one and
+// eight waves of resident CTAs so that the grid fills its last wave best
+// (fewest idle CTA slots), then the fewest ranges; with num_ctas > 0 it is
+// ceil(num_ctas / units).  At most max_blocks ranges per unit.
 struct GeneralPlan {
   GenLaunch launch;
   int splits;
@@ -130,8 +133,20 @@ kvq_status general_plan(const kvq_attn_desc* d, GeneralPlan* plan) {
   plan->launch = general_launch_shape(d->cache.bits, d->cache.k_scheme, d->cache.v_scheme, d->cache.head_dim,
                                       group_of(&d->cache), smem_sm, reserved);
   const long long units = (long long)d->batch * units_per_seq(d);
-  const long long target = d->num_ctas > 0 ? d->num_ctas : 2LL * plan->launch.ctas_per_sm * sm;
-  long long splits = (target + units - 1) / units;
+  long long splits;
+  if (d->num_ctas > 0) {
+    splits = (d->num_ctas + units - 1) / units;
+  } else {
+    const long long resident = (long long)plan->launch.ctas_per_sm * sm;
+    const long long lo = (resident + units - 1) / units, hi = (8 * resident + units - 1) / units;
+    splits = lo;
+    double best = -1.0;
+    for (long long s = lo; s <= hi && s <= d->max_blocks; ++s) {
+      const long long ctas = units * s, waves = (ctas + resident - 1) / resident;
+      const double fill = (double)ctas / (double)(waves * resident);
+      if (fill > best + 1e-9) { best = fill; splits = s; }
+    }
+  }
   if (splits > d->max_blocks) splits = d->max_blocks;
   if (splits < 1) splits = 1;
   plan->splits = (int)splits;
@@ -174,7 +189,6 @@ kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const ui
   p.gq = g < kGroupQ ? g : kGroupQ;
   p.units_per_seq = units_per_seq(desc);
   p.kv_shift = g > kGroupQ ? 1 : 0;
-  p.group = group_of(&desc->cache);
   p.splits = plan.splits;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.flags = desc->flags;
@@ -183,7 +197,7 @@ kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const ui
   p.minus_one = 0xffffffffu;
   const int grid = desc->batch * p.units_per_seq * plan.splits;
   cudaError_t e = launch_decode_general(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme,
-                                        desc->cache.head_dim, p, grid, plan.launch.smem, st);
+                                        desc->cache.head_dim, group_of(&desc->cache), p, grid, plan.launch, st);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   e = launch_merge(p.part_o, p.part_lse, desc->batch * desc->num_q_heads, plan.splits, desc->cache.head_dim, out, lse,
                    st);

@@ -32,10 +32,14 @@ namespace gen {
 constexpr int kThreads = 128;
 
 // Byte offset of row p, 16-column block nb of a B operand with nb16 blocks
-// (MN-major, no swizzle: core matrices of 8 rows x 16 bytes; K-direction
-// stride nb16 * 128, N-direction stride 128).
+// (MN-major, no swizzle: core matrices of 8 rows x 16 bytes, N-direction
+// stride 128).  An E4M3 block is one core matrix wide (K-direction stride
+// nb16 * 128); a BF16 block two (K-direction stride nb16 * 256), of which
+// the parts use the first.
+template <bool BF16>
 __device__ __forceinline__ uint32_t b_off(int p, int nb, int nb16) {
-  return (uint32_t)((p >> 3) * (nb16 * 128) + nb * 128 + (p & 7) * 16);
+  constexpr int kCm = BF16 ? 256 : 128;
+  return (uint32_t)((p >> 3) * (nb16 * kCm) + nb * kCm + (p & 7) * 16);
 }
 
 __device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t* r) {
@@ -44,14 +48,18 @@ __device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t* r) {
                : "memory");
 }
 
-// The 12 used columns of a 16-column block (4 heads x 3 parts).
+// The used columns of a 16-column block (4 heads x 3 E4M3 parts, or x 2
+// BF16 parts).
+template <bool BF16>
 __device__ __forceinline__ void ld_block(uint32_t taddr, uint32_t (&v)[12]) {
   tmem_ld_32x32b_x8(taddr, v);
-  tmem_ld_32x32b_x4(taddr + 8, v + 8);
+  if (!BF16) tmem_ld_32x32b_x4(taddr + 8, v + 8);
 }
-// Sum of the three parts of head h.
-__device__ __forceinline__ float parts3(const uint32_t (&v)[12], int h) {
-  return (__uint_as_float(v[h]) + __uint_as_float(v[4 + h])) + __uint_as_float(v[8 + h]);
+// Sum of the parts of head h.
+template <bool BF16>
+__device__ __forceinline__ float parts(const uint32_t (&v)[12], int h) {
+  return BF16 ? __uint_as_float(v[h]) + __uint_as_float(v[4 + h])
+              : (__uint_as_float(v[h]) + __uint_as_float(v[4 + h])) + __uint_as_float(v[8 + h]);
 }
 
 // Warp reduction of N values per lane at once (sum or max), halving the
@@ -88,6 +96,7 @@ __device__ __forceinline__ void warp_reduce_store(float (&v)[N], float* buf) {
   const float r = warp_reduce_t<N, MAX>(v);
   const int lane = threadIdx.x & 31;
   if ((lane & ((32 >> kLog) - 1)) == 0) buf[(threadIdx.x >> 5) * N + (lane >> (5 - kLog))] = r;
+  __syncwarp();
 }
 // Block-wide result i from buf[4][N] (after a barrier).
 template <int N>
@@ -100,37 +109,44 @@ __device__ __forceinline__ float max4(const float* buf, int i) {
 }
 
 // Thread 0 waits (bounded) for the phase; the whole CTA learns the outcome,
-// so that a wait that runs out leaves every thread on the same path.
+// so that a wait that runs out leaves every thread on the same path.  Ends
+// with the warp converged: the tcgen05.ld / st that follow are .sync.aligned
+// (every lane of the warp must execute them together).
 __device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* ok_flag, uint64_t limit) {
   if (threadIdx.x == 0) *ok_flag = mbar_wait_bounded(bar, parity, nullptr, limit) ? 1 : 0;
   __syncthreads();
   const bool ok = *ok_flag != 0;
-  if (ok && threadIdx.x != 0) (void)mbar_try_wait(bar, parity);  // completed: observe it in every thread
+  if (ok) (void)mbar_try_wait(bar, parity);  // completed: observe it in every thread
+  __syncwarp();
   return ok;
 }
 
-// Codes of `chunks` 16-byte chunks of row `row` (chunk-major block layout
-// with `nrows` rows) -> E4M3 operand words in tensor memory from column col.
-template <int BITS, int CHUNKS>
+// Codes of `CHUNKS` 16-byte chunks of row `row` (chunk-major block layout
+// with `nrows` rows) -> operand words (E4M3 bytes or exact BF16 values) in
+// tensor memory from column taddr: 4 * kOut columns per chunk.
+template <int BITS, bool BF16, int CHUNKS>
 __device__ __forceinline__ void convert_row(const unsigned char* blk, int nrows, int row, uint32_t taddr, uint32_t mul,
                                             uint32_t m1) {
-  using Cv = Convert<BITS, false>;
+  using Cv = Convert<BITS, BF16>;
 #pragma unroll
   for (int c = 0; c < CHUNKS; ++c) {
     const uint4 v = *reinterpret_cast<const uint4*>(blk + ((size_t)c * nrows + row) * 16);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[16];
+    uint32_t o[4 * Cv::kOut];
 #pragma unroll
     for (int i = 0; i < 4; ++i) Cv::run(w[i], &o[i * Cv::kOut], mul, m1);
 #pragma unroll
-    for (int q8 = 0; q8 < Cv::kOut / 2; ++q8)  // a chunk gives 32 / BITS columns
-      tmem_st_x8(taddr + c * (32 / BITS) + 8 * q8, &o[8 * q8]);
+    for (int q8 = 0; q8 < Cv::kOut / 2; ++q8) tmem_st_x8(taddr + c * 4 * Cv::kOut + 8 * q8, &o[8 * q8]);
   }
 }
 
-template <int BITS, bool KCW, bool VCW, int D, int G>
+template <int BITS, bool KCW, bool VCW, int D, int G, bool BF16>
 __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenParams p, int stages) {
   constexpr int kKBytes = kBlockTokens * D * BITS / 8;  // K (and V) codes of a block
+  constexpr int kElems = BF16 ? 16 : 32;                // contraction elements per MMA
+  constexpr int kCm = BF16 ? 256 : 128;                 // bytes of one B block per 8 rows
+  constexpr int kVCols = BF16 ? 64 : 32;                // operand columns of 128 V codes (one row)
+  constexpr uint32_t kFmt = BF16 ? 1u : 0u;             // BF16 (kind::f16) or E4M3 (kind::f8f6f4)
   constexpr int kHalves = D > 128 ? 2 : 1;              // M = 128 halves of the channels
   constexpr int kQv = (D + 127) / 128;                  // channels per thread
   constexpr int NGC = D / G;                            // channel groups (token-wise)
@@ -142,8 +158,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
   constexpr int NM = VCW ? 4 : 8;                       // values of the block-max reduction (+ largest V scale)
   constexpr int NZ = VCW ? 4 : 4 * NGC;                 // values of the per-group p sums
   extern __shared__ __align__(1024) unsigned char smem[];
-  const GenLayout L = gen_layout(BITS, D, G, KCW, VCW, stages);  // shared-memory offsets (depend on stages)
-  constexpr GenLayout LT = gen_layout(BITS, D, G, KCW, VCW, 2);  // tensor-memory columns (do not)
+  const GenLayout L = gen_layout(BITS, D, G, KCW, VCW, BF16, stages);  // shared-memory offsets (depend on stages)
+  constexpr GenLayout LT = gen_layout(BITS, D, G, KCW, VCW, BF16, 2);  // tensor-memory columns (do not)
   constexpr bool kSeq = LT.seq_halves;
 
   unsigned char* qop = smem + L.q_off;  // [D rows][NBQ blocks]
@@ -183,6 +199,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
   }
   for (int i = tid; i < (L.scratch_off - L.q_off) / 16; i += kThreads)
     reinterpret_cast<uint4*>(qop)[i] = make_uint4(0u, 0u, 0u, 0u);  // unused operand columns stay zero
+  __syncwarp();  // converged for the .sync.aligned allocation
   if (warp == 0) {
     tmem_alloc(tbase, (uint32_t)LT.tmem_cols);
     tmem_relinquish();
@@ -249,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
   float mult[4];  // partial-score multiplier (log2 units)
 #pragma unroll
   for (int h = 0; h < 4; ++h)
-    mult[h] = 512.0f * (KCW ? pow2_head_inv(qmax[h]) : pow2_prescale_inv(qmax[h])) * p.sm_scale_log2;
+    mult[h] = BF16 ? p.sm_scale_log2  // exact BF16 codes, no prescale
+                   : 512.0f * (KCW ? pow2_head_inv(qmax[h]) : pow2_prescale_inv(qmax[h])) * p.sm_scale_log2;
   float qsz[NGC][4];  // token-wise K: sum of q over channel group g, times the log2 softmax scale
   if (!KCW) {
     // Q' = q * 2^k (k per head) in three E4M3 parts at row a_pos(c); and the
@@ -258,10 +276,16 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
     for (int i = 0; i < kQv; ++i) {
       const int c = tid + 128 * i;
       if (c < D) {
-        const float f = odd_quarter<BITS, false>(c);
-        const float4 v = make_float4(qv[0][i] * pow2_prescale(qmax[0]) * f, qv[1][i] * pow2_prescale(qmax[1]) * f,
-                                     qv[2][i] * pow2_prescale(qmax[2]) * f, qv[3][i] * pow2_prescale(qmax[3]) * f);
-        *reinterpret_cast<uint4*>(qop + b_off(a_pos<BITS, false>(c), 0, 1)) = split3_e4m3(v);
+        const float f = odd_quarter<BITS, BF16>(c);
+        float4 v;
+        if (BF16) {
+          v = make_float4(qv[0][i] * f, qv[1][i] * f, qv[2][i] * f, qv[3][i] * f);
+        } else {
+          v = make_float4(qv[0][i] * pow2_prescale(qmax[0]) * f, qv[1][i] * pow2_prescale(qmax[1]) * f,
+                          qv[2][i] * pow2_prescale(qmax[2]) * f, qv[3][i] * pow2_prescale(qmax[3]) * f);
+        }
+        *reinterpret_cast<uint4*>(qop + b_off<BF16>(a_pos<BITS, BF16>(c), 0, 1)) = BF16 ? split2_bf16(v)
+                                                                                        : split3_e4m3(v);
       }
     }
     float t[4 * NGC];
@@ -287,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
 #pragma unroll
   for (int h = 0; h < 4; ++h)
 #pragma unroll
-    for (int i = 0; i < kQv; ++i) qk[h][i] = qv[h][i] * pow2_head(qmax[h]);
+    for (int i = 0; i < kQv; ++i) qk[h][i] = BF16 ? qv[h][i] : qv[h][i] * pow2_head(qmax[h]);
 
   float m_run[4], l_thr[4], oacc[kHalves][4], zacc[kHalves][4];
 #pragma unroll
@@ -313,11 +337,12 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
     const bool valid = l < nv;
 
     // ---- K codes -> E4M3 operand (rows = tokens)
-    convert_row<BITS, D * BITS / 128>(st, kBlockTokens, tid, t_a, p.nibble_mul, p.minus_one);
+    __syncwarp();
+    convert_row<BITS, BF16, D * BITS / 128>(st, kBlockTokens, tid, t_a, p.nibble_mul, p.minus_one);
     tc_wait_st();
 
     // ---- channel-wise K: Q'_g = q * s_g per token group g, and q . z_g
-    if (KCW) {
+    if (KCW && !BF16) {  // largest scale of each group: the E4M3 Q' prescale
       {
         uint32_t mx[NGT];
 #pragma unroll
@@ -332,21 +357,24 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
 #pragma unroll
           for (int g = 0; g < NGT; ++g) eg_w[warp * 4 + g] = mx[g];
       }
+      __syncthreads();
+    }
+    if (KCW) {
       float t[4 * NGT];
 #pragma unroll
       for (int k = 0; k < 4 * NGT; ++k) t[k] = 0.f;
-      __syncthreads();
 #pragma unroll
       for (int g = 0; g < NGT; ++g) {
-        const uint32_t e16 = f16_exp_field(max(max(eg_w[g], eg_w[4 + g]), max(eg_w[8 + g], eg_w[12 + g])));
-        const float fg = pow2_group(e16);
+        const float fg =
+            BF16 ? 1.0f : pow2_group(f16_exp_field(max(max(eg_w[g], eg_w[4 + g]), max(eg_w[8 + g], eg_w[12 + g]))));
 #pragma unroll
         for (int i = 0; i < kQv; ++i) {
           const int c = tid + 128 * i;
           if (c < D) {
-            const float f = h2f(ksz[g * D + c]) * fg * odd_quarter<BITS, false>(c);
+            const float f = h2f(ksz[g * D + c]) * fg * odd_quarter<BITS, BF16>(c);
             const float4 v = make_float4(qk[0][i] * f, qk[1][i] * f, qk[2][i] * f, qk[3][i] * f);
-            *reinterpret_cast<uint4*>(qop + b_off(a_pos<BITS, false>(c), g, NGT)) = split3_e4m3(v);
+            *reinterpret_cast<uint4*>(qop + b_off<BF16>(a_pos<BITS, BF16>(c), g, NGT)) = BF16 ? split2_bf16(v)
+                                                                                            : split3_e4m3(v);
             const float zgc = h2f(kzz[g * D + c]);
 #pragma unroll
             for (int h = 0; h < 4; ++h) t[g * 4 + h] = fmaf(qv[h][i], zgc, t[g * 4 + h]);
@@ -362,16 +390,17 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
     __syncthreads();
     tc_fence_after();
     if (tid == 0) {
-      constexpr uint32_t idesc_q = make_idesc(0, 0, 0, 1, 128, 16 * NBQ);
+      constexpr uint32_t idesc_q = make_idesc(kFmt, kFmt, 0, 1, 128, 16 * NBQ);
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) {
-        const uint64_t bd = make_smem_desc(smem_u32(qop) + k * 4 * NBQ * 128, NBQ * 128, 128);
+      for (int k = 0; k < D / kElems; ++k) {
+        const uint64_t bd = make_smem_desc(smem_u32(qop) + k * 4 * NBQ * 128, NBQ * kCm, 128);
         const uint32_t a = tmem + LT.col_a + 8 * k;
-        if (KCW) {
-          mma_f8f6f4_ts(tmem + LT.col_so, a, bd, idesc_q, k > 0);
-        } else {  // the K-steps of channel group g accumulate into S block g
-          mma_f8f6f4_ts(tmem + LT.col_so + 16 * ((32 * k) / G), a, bd, idesc_q, (32 * k) % G != 0);
-        }
+        // channel-wise K: one accumulator; token-wise K: the K-steps of channel
+        // group g accumulate into S block g
+        const uint32_t d = tmem + LT.col_so + (KCW ? 0 : 16 * ((kElems * k) / G));
+        const uint32_t acc = KCW ? (k > 0) : ((kElems * k) % G != 0);
+        if (BF16) mma_f16_ts(d, a, bd, idesc_q, acc);
+        else mma_f8f6f4_ts(d, a, bd, idesc_q, acc);
       }
       tc_commit(mma_bar);
     }
@@ -390,24 +419,24 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
     if (KCW) {
       const int g = l / G;  // warp-uniform (G >= 32)
       uint32_t v[12];
-      ld_block(t_so + 16 * g, v);
-      const uint32_t e16 = f16_exp_field(max(max(eg_w[g], eg_w[4 + g]), max(eg_w[8 + g], eg_w[12 + g])));
-      const float fs = pow2_group_inv(e16);
+      ld_block<BF16>(t_so + 16 * g, v);
+      const float fs =
+          BF16 ? 1.0f : pow2_group_inv(f16_exp_field(max(max(eg_w[g], eg_w[4 + g]), max(eg_w[8 + g], eg_w[12 + g]))));
       float cz[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) cz[h] = sum4<4 * NGT>(red_c, g * 4 + h) * p.sm_scale_log2;
       tc_wait_ld();
 #pragma unroll
-      for (int h = 0; h < 4; ++h) sc[h] = fmaf(parts3(v, h), mult[h] * fs, cz[h]);
+      for (int h = 0; h < 4; ++h) sc[h] = fmaf(parts<BF16>(v, h), mult[h] * fs, cz[h]);
     } else {
 #pragma unroll
       for (int g = 0; g < NGC; ++g) {
         uint32_t v[12];
-        ld_block(t_so + 16 * g, v);
+        ld_block<BF16>(t_so + 16 * g, v);
         const float s_lg = h2f(ksz[l * NGC + g]), z_lg = h2f(kzz[l * NGC + g]);
         tc_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 4; ++h) sc[h] += fmaf(parts3(v, h) * mult[h], s_lg, z_lg * qsz[g][h]);
+        for (int h = 0; h < 4; ++h) sc[h] += fmaf(parts<BF16>(v, h) * mult[h], s_lg, z_lg * qsz[g][h]);
       }
     }
 #pragma unroll
@@ -417,10 +446,12 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
     //      (QK^T is complete).  A 64-dim head leaves rows 64..127 as they are:
     //      output row m depends on operand row m alone, and rows >= D are
     //      never read.
+    __syncwarp();
 #pragma unroll
     for (int hf = 0; hf < kHalves; ++hf)
       if (hf * 128 + tid < D)  // warp-uniform
-        convert_row<BITS, BITS>(st + kKBytes, D, hf * 128 + tid, t_a + 32 * hf, p.nibble_mul, p.minus_one);
+        convert_row<BITS, BF16, BITS>(st + kKBytes, D, hf * 128 + tid, t_a + kVCols * hf, p.nibble_mul,
+                                      p.minus_one);
 
     // ---- online softmax over the block: block maxima (and the largest V scale)
     {
@@ -445,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
       alpha[h] = ex2(m_run[h] - mn);
       m_run[h] = mn;
       pr[h] = valid ? ex2(sc[h] - mn) : 0.f;
-      pe[h] = p_exponent(bmax[h] - mn, e_v);  // P' prescale 2^(6 - E)
+      pe[h] = BF16 ? 6 : p_exponent(bmax[h] - mn, e_v);  // P' prescale 2^(6 - E) (1 for BF16)
       l_thr[h] = fmaf(l_thr[h], alpha[h], pr[h]);
     }
 
@@ -469,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
 
     // ---- P' operand: row a_pos(l), one 16-column block per channel group (token-wise V)
     {
-      const float oq = odd_quarter<BITS, false>(l);
+      const float oq = odd_quarter<BITS, BF16>(l);
       float ps[4];
 #pragma unroll
       for (int h = 0; h < 4; ++h) ps[h] = pr[h] * oq * __uint_as_float((uint32_t)(133 - pe[h]) << 23);
@@ -477,14 +508,15 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
       for (int g = 0; g < NBP; ++g) {
         const float sv = VCW ? 1.0f : (valid ? h2f(vsz[l * NGC + g]) : 0.f);
         const float4 v = make_float4(ps[0] * sv, ps[1] * sv, ps[2] * sv, ps[3] * sv);
-        *reinterpret_cast<uint4*>(pop + b_off(a_pos<BITS, false>(l), g, NBP)) = split3_e4m3_via_f16(v);
+        *reinterpret_cast<uint4*>(pop + b_off<BF16>(a_pos<BITS, BF16>(l), g, NBP)) =
+            BF16 ? split2_bf16(v) : split3_e4m3_via_f16(v);
       }
     }
     fence_proxy_async_smem();
 
-    float pinv[4];  // 2^(E - 6) * 2^9 (the codes' E4M3 scale)
+    float pinv[4];  // 2^(E - 6), times 2^9 for E4M3 codes (code * 2^-9)
 #pragma unroll
-    for (int h = 0; h < 4; ++h) pinv[h] = __uint_as_float((uint32_t)(130 + pe[h]) << 23);
+    for (int h = 0; h < 4; ++h) pinv[h] = __uint_as_float((uint32_t)((BF16 ? 121 : 130) + pe[h]) << 23);
 
     // ---- PV: O[channel][column block] per M = 128 half of the channels, then
     //      the epilogue: channel c = 128 hf + tid; undo the P' prescale, fold V
@@ -499,15 +531,16 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
           if (kSeq && hf != pass) continue;
           const uint32_t o = tmem + LT.col_so + (kSeq ? 0 : hf * 16 * NBO);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint32_t a = tmem + LT.col_a + 32 * hf + 8 * k;
-            if (VCW) {  // the K-steps of token group g accumulate into O block g
-              const uint64_t bd = make_smem_desc(smem_u32(pop) + k * 4 * 128, 128, 128);
-              mma_f8f6f4_ts(o + 16 * ((32 * k) / G), a, bd, make_idesc(0, 0, 0, 1, 128, 16), (32 * k) % G != 0);
-            } else {
-              const uint64_t bd = make_smem_desc(smem_u32(pop) + k * 4 * NGC * 128, NGC * 128, 128);
-              mma_f8f6f4_ts(o, a, bd, make_idesc(0, 0, 0, 1, 128, 16 * NGC), k > 0);
-            }
+          for (int k = 0; k < kBlockTokens / kElems; ++k) {
+            const uint32_t a = tmem + LT.col_a + kVCols * hf + 8 * k;
+            // channel-wise V: the K-steps of token group g accumulate into O block g
+            const uint64_t bd = VCW ? make_smem_desc(smem_u32(pop) + k * 4 * 128, kCm, 128)
+                                    : make_smem_desc(smem_u32(pop) + k * 4 * NGC * 128, NGC * kCm, 128);
+            const uint32_t d = VCW ? o + 16 * ((kElems * k) / G) : o;
+            const uint32_t acc = VCW ? ((kElems * k) % G != 0) : (k > 0);
+            constexpr uint32_t idesc_p = make_idesc(kFmt, kFmt, 0, 1, 128, VCW ? 16 : 16 * NGC);
+            if (BF16) mma_f16_ts(d, a, bd, idesc_p, acc);
+            else mma_f8f6f4_ts(d, a, bd, idesc_p, acc);
           }
         }
         tc_commit(mma_bar);
@@ -525,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
 #pragma unroll
           for (int g = 0; g < NGT; ++g) {
             uint32_t v[12];
-            ld_block(o + 16 * g, v);
+            ld_block<BF16>(o + 16 * g, v);
             tc_wait_ld();
             if (g * G >= nv || c >= D) continue;  // no valid token in this group / no such channel
             const float s_gc = h2f(vsz[g * D + c]), z_gc = h2f(vzz[g * D + c]);
@@ -535,17 +568,17 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
 #pragma unroll
               for (int w = 0; w < 4; ++w)
                 if ((32 * w) / G == g) psum += red_z[w * 4 + h];
-              add[h] = fmaf(s_gc, parts3(v, h) * pinv[h], fmaf(z_gc, psum, add[h]));
+              add[h] = fmaf(s_gc, parts<BF16>(v, h) * pinv[h], fmaf(z_gc, psum, add[h]));
             }
           }
         } else {
           const int g = (c < D ? c : 0) / G;  // warp-uniform (G >= 32)
           uint32_t v[12];
-          ld_block(o + 16 * g, v);
+          ld_block<BF16>(o + 16 * g, v);
           tc_wait_ld();
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
-            add[h] = parts3(v, h) * pinv[h];
+            add[h] = parts<BF16>(v, h) * pinv[h];
             zacc[hf][h] = fmaf(zacc[hf][h], alpha[h], sum4<NZ>(red_z, g * 4 + h));
           }
         }
@@ -595,28 +628,29 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
   }
   tc_fence_before();
   __syncthreads();
+  __syncwarp();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)LT.tmem_cols);
   }
 }
 
-template <int BITS, bool KCW, bool VCW, int D, int G>
+template <int BITS, bool KCW, bool VCW, int D, int G, bool BF16>
 cudaError_t launch_instance(const GenParams& p, int grid, const GenLaunch& shape, cudaStream_t stream) {
-  auto kern = decode_general_kernel<BITS, KCW, VCW, D, G>;
+  auto kern = decode_general_kernel<BITS, KCW, VCW, D, G, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shape.smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, shape.smem, stream>>>(p, shape.stages);
   return cudaGetLastError();
 }
 
-template <int BITS, int D, int G>
+template <int BITS, int D, int G, bool BF16>
 cudaError_t launch_schemes(bool kcw, bool vcw, const GenParams& p, int grid, const GenLaunch& shape,
                            cudaStream_t s) {
-  if (!kcw && !vcw) return launch_instance<BITS, false, false, D, G>(p, grid, shape, s);
-  if (!kcw && vcw) return launch_instance<BITS, false, true, D, G>(p, grid, shape, s);
-  if (kcw && !vcw) return launch_instance<BITS, true, false, D, G>(p, grid, shape, s);
-  return launch_instance<BITS, true, true, D, G>(p, grid, shape, s);
+  if (!kcw && !vcw) return launch_instance<BITS, false, false, D, G, BF16>(p, grid, shape, s);
+  if (!kcw && vcw) return launch_instance<BITS, false, true, D, G, BF16>(p, grid, shape, s);
+  if (kcw && !vcw) return launch_instance<BITS, true, false, D, G, BF16>(p, grid, shape, s);
+  return launch_instance<BITS, true, true, D, G, BF16>(p, grid, shape, s);
 }
 
 }  // namespace gen

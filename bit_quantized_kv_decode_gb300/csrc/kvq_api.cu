@@ -99,8 +99,8 @@ kvq_status check_attn(const kvq_attn_desc* d) {
   if ((d->flags & KVQ_FLAG_E2M1_V) &&
       (d->cache.bits != 2 || d->operand_mode != KVQ_OPERANDS_FP8 || heads_per_kv(d) != kGroupQ))
     return KVQ_ERR_UNSUPPORTED;  // the E2M1 placement is built for these only
-  if (!default_geometry(&d->cache) && (d->operand_mode != KVQ_OPERANDS_FP8 || (d->flags & KVQ_FLAG_E2M1_V)))
-    return KVQ_ERR_UNSUPPORTED;  // the general-geometry kernel has FP8 operands only
+  if (!default_geometry(&d->cache) && (d->flags & KVQ_FLAG_E2M1_V))
+    return KVQ_ERR_UNSUPPORTED;  // the E2M1 placement is built for head dim 128, groups of 128
   if (!(std::isfinite(d->sm_scale))) return KVQ_ERR_INVALID_ARG;
   if ((long long)d->batch * units_per_seq(d) * d->max_blocks > (1LL << 30)) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
@@ -131,7 +131,7 @@ kvq_status general_plan(const kvq_attn_desc* d, GeneralPlan* plan) {
     }
   }
   plan->launch = general_launch_shape(d->cache.bits, d->cache.k_scheme, d->cache.v_scheme, d->cache.head_dim,
-                                      group_of(&d->cache), smem_sm, reserved);
+                                      group_of(&d->cache), d->operand_mode == KVQ_OPERANDS_BF16, smem_sm, reserved);
   const long long units = (long long)d->batch * units_per_seq(d);
   long long splits;
   if (d->num_ctas > 0) {
@@ -197,7 +197,8 @@ kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const ui
   p.minus_one = 0xffffffffu;
   const int grid = desc->batch * p.units_per_seq * plan.splits;
   cudaError_t e = launch_decode_general(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme,
-                                        desc->cache.head_dim, group_of(&desc->cache), p, grid, plan.launch, st);
+                                        desc->cache.head_dim, group_of(&desc->cache),
+                                        desc->operand_mode == KVQ_OPERANDS_BF16, p, grid, plan.launch, st);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   e = launch_merge(p.part_o, p.part_lse, desc->batch * desc->num_q_heads, plan.splits, desc->cache.head_dim, out, lse,
                    st);

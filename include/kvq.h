@@ -207,12 +207,18 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* 
  * token-wise K scales the partial q.code by s and adds z * sum(q); channel-
  * wise K multiplies q by s before the product and adds q . z; token-wise V
  * multiplies the probabilities by s and adds sum(p * z); channel-wise V scales
- * each 128-token group's partial product by s and adds z * sum(p) of that
- * group ([SUM] 限界と未検証の範囲: per-group application).  Work is split
- * over persistent CTAs in equal tile ranges; a sequence/head cut between
- * CTAs is merged on the device by log-sum-exp.  Query heads per KV head:
- * 1, 2, 4 or 8 (a work unit takes up to 4 query heads of one KV head, so
- * with 8 each KV block is read twice).
+ * each G-token group's partial product by s and adds z * sum(p) of that
+ * group ([SUM] 限界と未検証の範囲: per-group application); with groups
+ * smaller than the head dim, token-wise K and V fold per G-channel group.
+ * Head dim 128 with groups of 128: work is split over persistent CTAs in
+ * equal tile ranges; a sequence/head cut between CTAs is merged on the device
+ * by log-sum-exp.  Other geometries (head dim 64 / 256, groups of 32 / 64):
+ * a second kernel walks equal ranges of each (sequence, unit)'s blocks and a
+ * log-sum-exp merge kernel combines the ranges (two launches); only
+ * KVQ_OPERANDS_FP8 is built there (else KVQ_ERR_UNSUPPORTED).  Query heads
+ * per KV head: 1, 2, 4 or 8 (a work unit takes up to 4 query heads of one KV
+ * head, so with 8 each KV block is read twice).  sm_scale <= 0 means
+ * 1 / sqrt(head_dim).
  *   q        bf16 [batch][num_q_heads][head_dim]
  *   k_codes, v_codes, k_scale, k_zero, v_scale, v_zero: cache arrays
  *   seq_lens int32 [batch], each in [0, max_blocks*128]
@@ -239,8 +245,10 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
  * kvq_decode_attn minus the workspace: the split-merge scratch lives in a
  * fixed 4 MiB device array owned by the library, held on every device that
  * loads the library until the process exits.  Returns KVQ_ERR_WORKSPACE when
- * a call needs more scratch than that (batch * num_kv_heads * 4 bytes of
- * counters, twice that with 8 query heads per KV head, plus 4 KiB per CTA);
+ * a call needs more scratch than kvq_decode_workspace_size reports (head dim
+ * 128, groups of 128: batch * num_kv_heads * 4 bytes of counters, twice that
+ * with 8 query heads per KV head, plus 4 KiB per CTA; other geometries: one
+ * head_dim + 1 floats per query head and block range);
  * kvq_decode_attn with a caller workspace then
  * remains available.  Every call on a stream that is not being captured
  * looks up the array's address on the current device (the first such call

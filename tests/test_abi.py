@@ -112,8 +112,8 @@ def test_e2m1_flag_validation(lib):
 def test_general_geometry_workspace_host_only(lib):
     """Head dims 64 / 256 and groups of 32 / 64 take the block-range kernel:
     its workspace holds one partial output and log-sum-exp per query head
-    and range, ranges = ceil(num_ctas / units) capped at max_blocks; FP8
-    operands only."""
+    and range, ranges = ceil(num_ctas / units) capped at max_blocks; both
+    operand modes; not the E2M1 V placement."""
     n = ctypes.c_size_t()
     d = _lib.AttnDesc(_cache(4, 1, 0, hd=256, group=64, pages=16 * 64), 16, 32, 64, 0, 0.0, 304, 0)
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
@@ -122,9 +122,10 @@ def test_general_geometry_workspace_host_only(lib):
     d = _lib.AttnDesc(_cache(2, 0, 1, hd=64, group=32, pages=16 * 64), 2, 16, 2, 0, 0.0, 100000, 0)
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
     assert n.value == 256 + 2 * 16 * 2 * 64 * 4  # two ranges at most (max_blocks = 2)
-    for mode, flags in ((1, 0), (0, _lib.FLAG_E2M1_V)):
-        bad = _lib.AttnDesc(_cache(2, 1, 0, hd=128, group=32), 8, 32, 32, mode, 0.0, 304, flags)
-        assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
+    bf16 = _lib.AttnDesc(_cache(2, 1, 0, hd=128, group=32), 8, 32, 32, 1, 0.0, 304, 0)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(bf16), ctypes.byref(n)) == 0
+    bad = _lib.AttnDesc(_cache(2, 1, 0, hd=128, group=32), 8, 32, 32, 0, 0.0, 304, _lib.FLAG_E2M1_V)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
 
 
 def test_validation_precedes_device(lib):

@@ -1,6 +1,6 @@
 """Decode attention on the general cache geometry (head dims 64 / 256, groups
 of 32 / 64 elements, and groups of 32 / 64 with head dim 128) against the
-oracle: every bit width and K/V scheme pair, query heads per KV head 1 / 2 /
+oracle: every bit width and K/V scheme pair in both operand modes, query heads per KV head 1 / 2 /
 4 / 8, ragged and empty sequences, paged caches, block ranges split one way
 and many ways, an explicit softmax scale and the stall hook (the static
 entry point on this geometry: tests/test_zz_no_alloc.py).  Accumulator folds per quantization group follow the
@@ -29,6 +29,19 @@ def test_decode_geometry_parity(D, G, bits, ks, vs):
     res = run_gpu(pb)
     assert res["status"] == 0
     assert_attention_close(pb, res, 0)
+
+
+@pytest.mark.parametrize("D,G", GEOMETRIES)
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("ks,vs", PAIRS)
+def test_decode_geometry_parity_bf16(D, G, bits, ks, vs):
+    """The BF16-operand mode (exact BF16 codes, two-part BF16 Q' and P'):
+    the tighter tolerance."""
+    w = _w(D, G, bits, ks, vs, paged=(D + G + bits) % 2 == 1)
+    pb = make_problem(w, 700 + D + G + bits + 2 * ks + vs, lens=[300, 129, 1])
+    res = run_gpu(pb, mode=1)
+    assert res["status"] == 0
+    assert_attention_close(pb, res, 1)
 
 
 @pytest.mark.parametrize("D,G", [(64, 32), (256, 64)])
@@ -97,14 +110,13 @@ def test_decode_geometry_stall_reports_timeout():
     assert_attention_close(pb, res, 0)
 
 
-def test_decode_geometry_unsupported_modes():
+def test_decode_geometry_e2m1_unsupported():
+    """The E2M1 V placement is built for head dim 128 with groups of 128 only."""
     import bit_quantized_kv_decode_gb300 as kvq
     from bit_quantized_kv_decode_gb300 import _lib
     w = _w(64, 32, 2, 0, 0, B=1, Hkv=1, Hq=4)
     pb = make_problem(w, 3, lens=[100])
     with pytest.raises(_lib.KvqError) as e:
-        run_gpu(pb, mode=kvq.OPERANDS_BF16)
-    assert e.value.status == 2
-    with pytest.raises(_lib.KvqError):
         run_gpu(pb, flags=kvq.FLAG_E2M1_V)
+    assert e.value.status == 2
 

@@ -488,15 +488,15 @@ def main():
                             "paged": w3.paged, "split_kv": "persistent CTAs cut the tile order into equal "
                                                           "ranges; cut units are merged in the kernel"})
     geometry = []  # head dims 64 / 256 and groups of 32 / 64: the general-geometry kernel
-    if not args.no_extra and w.name == DEFAULT_WORKLOAD and mode == 0:
+    if not args.no_extra and w.name == DEFAULT_WORKLOAD:
         for name in ("b32_l32k_d256_g64_int4", "b32_l32k_d128_g32_int2", "b32_l32k_d64_g32_int2"):
             w4 = synth.WORKLOADS[name]
-            r4 = measure_kvq(w4, args.seed + rank, 20, args.warmup, dev, e2e=False)
+            r4 = measure_kvq(w4, args.seed + rank, 20, args.warmup, dev, e2e=False, mode=mode)
             ms4 = max_over_ranks(r4["ms"], world, dev)
             geometry.append({"workload": name, "head_dim": w4.head_dim, "group": w4.group, "bits": w4.bits,
                              "k_scheme": SCHEME_NAMES[w4.k_scheme], "v_scheme": SCHEME_NAMES[w4.v_scheme],
                              "ms_per_step": ms4, "GB/s": r4["bytes"] / (ms4 / 1e3) / 1e9, "latency_us": ms4 * 1e3,
-                             "algorithmic_bytes": r4["bytes"], "l2": l2_note(r4),
+                             "algorithmic_bytes": r4["bytes"], "l2": l2_note(r4), "operands": args.operands,
                              "kernel": "kvq::decode_general_kernel + kvq::merge_kernel"})
     clk = clocks.summary(res["t0"], res["t1"])
     clocks.stop()

@@ -214,8 +214,8 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* 
  * equal tile ranges; a sequence/head cut between CTAs is merged on the device
  * by log-sum-exp.  Other geometries (head dim 64 / 256, groups of 32 / 64):
  * a second kernel walks equal ranges of each (sequence, unit)'s blocks and a
- * log-sum-exp merge kernel combines the ranges (two launches); only
- * KVQ_OPERANDS_FP8 is built there (else KVQ_ERR_UNSUPPORTED).  Query heads
+ * log-sum-exp merge kernel combines the ranges (two launches); both operand
+ * modes, not KVQ_FLAG_E2M1_V (KVQ_ERR_UNSUPPORTED).  Query heads
  * per KV head: 1, 2, 4 or 8 (a work unit takes up to 4 query heads of one KV
  * head, so with 8 each KV block is read twice).  sm_scale <= 0 means
  * 1 / sqrt(head_dim).

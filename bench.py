@@ -182,7 +182,7 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
     cs = [build_cache(w, seed, dev, k_scheme, v_scheme) for _ in range(sets)]
     c = cs[0]
     desc = c["desc"]
-    ad = kvq.attn_desc(desc, w.batch, c["max_blocks"], num_q_heads=w.num_q_heads)
+    ad = kvq.attn_desc(desc, w.batch, c["max_blocks"], mode=mode, num_q_heads=w.num_q_heads, flags=flags)
     ws = torch.empty(kvq.workspace_size(ad), dtype=torch.uint8, device=dev)
     out = torch.empty(w.batch, w.num_q_heads, w.head_dim, dtype=torch.float32, device=dev)
     lse = torch.empty(w.batch, w.num_q_heads, dtype=torch.float32, device=dev)
@@ -201,7 +201,7 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
     t_wall1 = time.time()
     if int(status.item()) != 0:
         raise RuntimeError(f"decode reported device status {int(status.item()):#x}")
-    general = w.head_dim != 128 or w.group != 128  # block-range kernel + log-sum-exp merge kernel
+    general = w.head_dim != 128 or w.group != 128 or mode == 1  # block-range kernel + log-sum-exp merge kernel
     res = dict(ms=ms, per=per, bytes=algorithmic_bytes(w, c["lens_cpu"].tolist()), t0=t_wall0, t1=t_wall1,
                launches=steps * (2 if general else 1), sets=sets, lens=c["lens_cpu"].tolist())
     if e2e:
@@ -519,7 +519,7 @@ def main():
                        **({"operands": "bf16 (exact BF16 codes, 2-part BF16 Q'/P')"} if mode else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": ("kvq::decode_kernel" if w.head_dim == 128 and w.group == 128 else
+                     "kernel": ("kvq::decode_kernel" if w.head_dim == 128 and w.group == 128 and mode == 0 else
                                 "kvq::decode_general_kernel + kvq::merge_kernel"),
                      "traffic": None if mode else profile_traffic(w.name),
                      "algorithmic_bytes_per_launch": res["bytes"],

@@ -22,8 +22,9 @@
 //    KV bytes staged in shared memory (by cp.async.bulk);
 //  * INT4 and INT2 codes both become E4M3 bytes (code * 2^-9): 3 integer ops
 //    per 8 INT4 codes, 7 per 16 INT2 codes;
-//  * Q' and P' are sums of three E4M3 parts (two BF16 parts in the BF16
-//    correctness mode) stacked along N, so precision costs no extra MMA;
+//  * Q' and P' are sums of three E4M3 parts stacked along N, so precision
+//    costs no extra MMA (the BF16-operand mode runs in the block-range kernel
+//    of decode_general.cuh);
 //  * persistent CTAs take equal ranges of (sequence, kv head, 128-token tile);
 //    a (sequence, kv head) cut by a range boundary is merged by the last CTA
 //    to finish a part (log-sum-exp over the parts, no waiting);
@@ -84,35 +85,35 @@ static_assert(128 * kRegsConvert + 128 * kRegsSoftmax + 128 * kRegsLight == kDec
 
 // E2V: 2-bit V codes as E2M1 values (code / 2) in shared memory (the
 // KVQ_FLAG_E2M1_V placement); otherwise codes are E4M3 bytes in tensor memory.
-template <int BITS, bool BF16, bool E2V = false>
+template <int BITS, bool E2V = false>
 struct DecodeCfg {
   static constexpr int kBlockBytes = kBlockTokens * kHeadDim * BITS / 8;  // 8192 / 4096
   static constexpr int kChunks = kHeadDim * BITS / 8 / 16;                // 16-byte chunks per row
   static constexpr bool kE2V = E2V;
-  static_assert(!E2V || (BITS == 2 && !BF16), "E2M1 placement: 2-bit codes, FP8 operands");
+  static_assert(!E2V || BITS == 2, "E2M1 placement: 2-bit codes");
   // (four stages with the E2M1 tiles: two CTAs per SM must still fit)
   static constexpr int kStages = (BITS == 4) ? 4 : (E2V ? 4 : 6);
   static constexpr int kSzBytes = kBlockTokens * 2;                       // one fp16 [128] array
   static constexpr int kStageBytes = 2 * kBlockBytes + 4 * kSzBytes;
-  static constexpr int kACols = BF16 ? 64 : 32;  // tensor-memory columns of one 128 x 128 A tile
-  static constexpr int kNAK = BF16 ? 1 : 2;      // A tile buffers: K codes
-  static constexpr int kNAV = BF16 ? 1 : 3;      // A tile buffers: V codes (the converters run ahead of PV)
-  static constexpr int kSplits = BF16 ? 2 : 3;   // parts of Q' and P'
-  static constexpr int kBBytes = BF16 ? 4096 : 2048;  // one B operand (128 K-rows x N=16)
-  static constexpr int kKSteps = BF16 ? 8 : 4;
+  static constexpr int kACols = 32;      // tensor-memory columns of one 128 x 128 A tile (E4M3 bytes)
+  static constexpr int kNAK = 2;         // A tile buffers: K codes
+  static constexpr int kNAV = 3;         // A tile buffers: V codes (the converters run ahead of PV)
+  static constexpr int kSplits = 3;      // E4M3 parts of Q' and P'
+  static constexpr int kBBytes = 2048;   // one B operand (128 K-rows x N=16)
+  static constexpr int kKSteps = 4;
   static constexpr uint32_t kKStepBBytes = 512;
-  static constexpr uint32_t kLbo = BF16 ? 256 : 128;  // K-direction core-matrix stride
-  static constexpr uint32_t kSbo = 128;               // N-direction core-matrix stride
-  static constexpr uint32_t kIdesc = BF16 ? make_idesc(1, 1, 0, 1, 128, 16) : make_idesc(0, 0, 0, 1, 128, 16);
-  static constexpr int kSlots = BF16 ? 4 : 3;  // score / probability / output buffers in flight
+  static constexpr uint32_t kLbo = 128;  // K-direction core-matrix stride
+  static constexpr uint32_t kSbo = 128;  // N-direction core-matrix stride
+  static constexpr uint32_t kIdesc = make_idesc(0, 0, 0, 1, 128, 16);
+  static constexpr int kSlots = 3;       // score / probability / output buffers in flight
   static constexpr int kColAK = 0;
   static constexpr int kColAV = kNAK * kACols;
   static constexpr int kColS = kColAV + kNAV * kACols;
   static constexpr int kColO = kColS + 16 * kSlots;
   static constexpr int kTmemCols = 256;
   // code = operand value * code scale (E4M3: code * 2^-9; E2M1: code / 2)
-  static constexpr float kCodeInv = BF16 ? 1.0f : 512.0f;  // K: code = operand value * 2^9
-  static constexpr int kVCodeLog2 = BF16 ? 0 : (E2V ? 1 : 9);
+  static constexpr float kCodeInv = 512.0f;  // K: code = operand value * 2^9
+  static constexpr int kVCodeLog2 = E2V ? 1 : 9;
   static constexpr uint32_t kIdescV = E2V ? make_idesc(5, 0, 0, 1, 128, 16) : kIdesc;  // A = E2M1, B = E4M3
   // E2M1 tiles in shared memory: canonical K-major layout without swizzle;
   // a 16-byte unit holds 16 codes of one row as packed nibbles (8 bytes) and
@@ -138,20 +139,16 @@ __device__ __forceinline__ int a_pos(int e) {
   }
 }
 
-// The used columns of one S / O slot (4 heads x 3 parts; 2 parts for BF16):
-// a single 12- or 8-column load instead of all 16.
-template <bool BF16>
+// The used columns of one S / O slot (4 heads x 3 parts): a single
+// 12-column load instead of all 16.
 __device__ __forceinline__ void tmem_ld_parts(uint32_t taddr, uint32_t (&r)[12]) {
   tmem_ld_32x32b_x8(taddr, r);
-  if (!BF16) tmem_ld_32x32b_x4(taddr + 8, r + 8);
-  else r[8] = r[9] = r[10] = r[11] = 0u;
+  tmem_ld_32x32b_x4(taddr + 8, r + 8);
 }
 
-// Byte offset of B-operand row p (MN-major, no swizzle).
-template <bool BF16>
-__device__ __forceinline__ uint32_t b_row_off(int p) {
-  return BF16 ? (uint32_t)((p >> 3) * 256 + (p & 7) * 16) : (uint32_t)(p * 16);
-}
+// Byte offset of B-operand row p (MN-major, no swizzle, E4M3: one core
+// matrix per 8 rows).
+__device__ __forceinline__ uint32_t b_row_off(int p) { return (uint32_t)(p * 16); }
 
 // B-operand row factor matching Convert: 2-bit codes at odd positions e are
 // stored as 4 * code, so their Q' / P' rows are scaled by 1/4 (exact).
@@ -337,9 +334,9 @@ struct Convert {
 };
 
 // ------------------------------------------------------------ shared state
-template <int BITS, bool BF16, bool E2V>
+template <int BITS, bool E2V>
 struct alignas(16) DecodeBarriers {
-  using C = DecodeCfg<BITS, BF16, E2V>;
+  using C = DecodeCfg<BITS, E2V>;
   uint64_t stg_full[C::kStages], stg_empty[C::kStages];
   // *_empty of the A buffers, Q' slots and P' slots are committed only by
   // kernels that do not wait on the product's own full barrier instead (see
@@ -362,11 +359,11 @@ struct alignas(16) DecodeBarriers {
 #endif
 };
 
-template <int BITS, bool BF16, bool E2V>
+template <int BITS, bool E2V>
 constexpr size_t decode_smem_layout_bytes() {
-  using C = DecodeCfg<BITS, BF16, E2V>;
+  using C = DecodeCfg<BITS, E2V>;
   size_t b = (size_t)C::kStages * C::kStageBytes + (2 + C::kSlots) * (size_t)C::kBBytes +
-             (size_t)C::kASmTiles * C::kASmBytes + sizeof(DecodeBarriers<BITS, BF16, E2V>) +
+             (size_t)C::kASmTiles * C::kASmBytes + sizeof(DecodeBarriers<BITS, E2V>) +
              (2 * kMaxBatch + 1) * sizeof(int) + 1024;
   return b < 80 * 1024 ? 80 * 1024 : b;  // >= 80 KB keeps at most two CTAs per SM
 }
@@ -591,7 +588,7 @@ __device__ __forceinline__ long long range_start(int c, long long T, int C) { re
 // Per-unit set-up, out of line (once per unit).
 // Converter thread r: q[i, r] of the unit's query head i times that head's Q'
 // prescale (0 for the head slots a unit with fewer than 4 heads leaves empty).
-template <bool KCW, bool BF16>
+template <bool KCW>
 static __device__ __noinline__ float4 converter_unit_q(const uint16_t* qb, int rows, int r) {
   float qmax[4], qsum[4];
   unit_q_stats<4>(qb, rows, false, qmax, qsum);
@@ -599,7 +596,7 @@ static __device__ __noinline__ float4 converter_unit_q(const uint16_t* qb, int r
 #pragma unroll
   for (int i = 0; i < 4; ++i)
     qh[i] = bf2f(qb[(i < rows ? i : 0) * kHeadDim + r]) * (i < rows ? 1.0f : 0.0f) *
-            (BF16 ? 1.0f : KCW ? pow2_head(qmax[i]) : pow2_prescale(qmax[i]));
+            (KCW ? pow2_head(qmax[i]) : pow2_prescale(qmax[i]));
   return make_float4(qh[0], qh[1], qh[2], qh[3]);
 }
 // Softmax thread i: per-head score constants of the unit.  Channel-wise K:
@@ -609,7 +606,7 @@ static __device__ __noinline__ float4 converter_unit_q(const uint16_t* qb, int r
 struct SegConsts {
   float qi[4], mult[4], add[4];
 };
-template <bool KCW, bool BF16>
+template <bool KCW>
 static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* qb, int rows, int i,
                                                                float sm_scale_log2, float code_inv) {
   float qmax[4], qsum[4];
@@ -620,10 +617,10 @@ static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* 
     if (KCW) {
       c.qi[k] = bf2f(qb[(k < rows ? k : 0) * kHeadDim + i]) * (k < rows ? 1.0f : 0.0f);
       c.mult[k] = 0.f;
-      c.add[k] = code_inv * (BF16 ? 1.0f : pow2_head_inv(qmax[k])) * sm_scale_log2;
+      c.add[k] = code_inv * pow2_head_inv(qmax[k]) * sm_scale_log2;
     } else {
       c.qi[k] = 0.f;
-      c.mult[k] = code_inv * (BF16 ? 1.0f : pow2_prescale_inv(qmax[k])) * sm_scale_log2;
+      c.mult[k] = code_inv * pow2_prescale_inv(qmax[k]) * sm_scale_log2;
       c.add[k] = qsum[k] * sm_scale_log2;
     }
   }
@@ -633,10 +630,10 @@ static __device__ __forceinline__ SegConsts softmax_unit_consts(const uint16_t* 
 // ================================================================= kernel
 // GQ4: exactly 4 query heads per KV head (one unit per KV head, no empty
 // head slots); the other groupings (1, 2, 8) take the run-time values in p.
-template <int BITS, bool KCW, bool VCW, bool BF16, bool GQ4, bool E2V>
+template <int BITS, bool KCW, bool VCW, bool GQ4, bool E2V>
 __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeParams p) {
-  using C = DecodeCfg<BITS, BF16, E2V>;
-  using Bars = DecodeBarriers<BITS, BF16, E2V>;
+  using C = DecodeCfg<BITS, E2V>;
+  using Bars = DecodeBarriers<BITS, E2V>;
   // Lean commits: each product commits only its full barrier (S or O slot)
   // and the buffers it read are reused on that phase.  Measured faster with
   // token-wise K (INT2: +6% K-tw/V-tw, +2% K-tw/V-cw) and slower with
@@ -692,7 +689,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     }
     lens[b] = len;
   }
-  // operand columns nobody writes (N = 12..15, or 8..15 for BF16) stay zero
+  // operand columns nobody writes (N = 12..15) stay zero
   // (and the padding half of every E2M1 unit, which the converters never write)
   for (int i = tid; i < ((2 + C::kSlots) * C::kBBytes + C::kASmTiles * C::kASmBytes) / 16; i += kDecodeThreads)
     reinterpret_cast<uint4*>(qop)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -810,7 +807,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
                 mma_f8f6f4_ss(d, make_smem_desc(smem_u32(asm_tiles + a * C::kASmBytes) + 2 * k * C::kALbo, C::kALbo,
                                                 C::kASbo),
                               bd, C::kIdescV, k > 0);
-              else if (BF16) mma_f16_ts(d, av, bd, C::kIdesc, k > 0);
               else mma_f8f6f4_ts(d, av, bd, C::kIdesc, k > 0);
             }
             if (!kLeanCommits) {
@@ -834,8 +830,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
             for (int k = 0; k < C::kKSteps; ++k) {
               uint64_t bd = make_smem_desc(b0 + k * C::kKStepBBytes, C::kLbo, C::kSbo);
               uint32_t d = tmem + C::kColS + 16 * sl, ak = tmem + C::kColAK + a * C::kACols + 8 * k;
-              if (BF16) mma_f16_ts(d, ak, bd, C::kIdesc, k > 0);
-              else mma_f8f6f4_ts(d, ak, bd, C::kIdesc, k > 0);
+              mma_f8f6f4_ts(d, ak, bd, C::kIdesc, k > 0);
             }
             if (!kLeanCommits) {
               tc_commit(&sh.ak_empty[a]);
@@ -873,7 +868,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     setmaxnreg_inc<kRegsConvert>();
     const int r = tid;  // tensor-memory lane = A row; also this thread's channel of Q'
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int qrow = a_pos<BITS, BF16>(r);
+    const int qrow = a_pos<BITS, false>(r);
     float qh[4] = {0.f, 0.f, 0.f, 0.f};  // q[b, 4h + i, r] times the head's prescale
     int seg = -1, slot_seg0 = -2, slot_seg1 = -2;  // Q' slot contents (token-wise K: constant per segment)
     TileIter it;
@@ -891,7 +886,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i)
-            Convert<BITS, BF16>::run(w[i], &o[(4 * c + i) * Convert<BITS, BF16>::kOut], p.nibble_mul, p.minus_one);
+            Convert<BITS, false>::run(w[i], &o[(4 * c + i) * Convert<BITS, false>::kOut], p.nibble_mul, p.minus_one);
         }
         tmem_st_32x32b_x32(col + 32 * ps2, o);
       }
@@ -936,7 +931,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       if (t == 0 || it.j == 0) {  // new (sequence, kv head): its four query rows
         ++seg;
         const float4 q4 =
-            converter_unit_q<KCW, BF16>(p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * gq) * kHeadDim, gq, r);
+            converter_unit_q<KCW>(p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * gq) * kHeadDim, gq, r);
         qh[0] = q4.x; qh[1] = q4.y; qh[2] = q4.z; qh[3] = q4.w;
       }
       // Q' operand: token-wise K uses q (written once per segment per slot);
@@ -945,11 +940,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       KVQ_PA(5, c4)
       KVQ_PT(c3)
       if (KCW || (sl ? slot_seg1 : slot_seg0) != seg) {
-        float f = odd_quarter<BITS, BF16>(r);
-        if (KCW) f *= BF16 ? h2f(ks[r]) : h2f(ks[r]) * pow2_group(f16_exp_field(max_f16_bits_128(ks)));
+        float f = odd_quarter<BITS, false>(r);
+        if (KCW) f *= h2f(ks[r]) * pow2_group(f16_exp_field(max_f16_bits_128(ks)));
         const float4 v = make_float4(qh[0] * f, qh[1] * f, qh[2] * f, qh[3] * f);
-        *reinterpret_cast<uint4*>(qop + sl * C::kBBytes + b_row_off<BF16>(qrow)) =
-            BF16 ? split2_bf16(v) : split3_e4m3(v);
+        *reinterpret_cast<uint4*>(qop + sl * C::kBBytes + b_row_off(qrow)) = split3_e4m3(v);
         fence_proxy_async_smem();
         if (sl) slot_seg1 = seg; else slot_seg0 = seg;
       }
@@ -1025,7 +1019,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
     const int i = tid - kWarpSoftmax0 * 32;  // tensor-memory lane: token (scores) / channel (output)
     const int sw = warp - kWarpSoftmax0;     // warp = lane quarter
     const uint32_t lane_off = (uint32_t)(sw * 32) << 16;
-    const int prow = a_pos<BITS, BF16, C::kE2V>(i);
+    const int prow = a_pos<BITS, false, C::kE2V>(i);
     uint32_t grp_phase = 0;
     const float kLn2 = 0.69314718055994530942f;
     const float kFix = 67108864.0f;  // 2^26: fixed-point scale of p for integer warp sums
@@ -1119,8 +1113,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 
       tc_fence_after();
       uint32_t acc[2][12];
-      tmem_ld_parts<BF16>(tmem + lane_off + C::kColO + 16 * oA, acc[0]);
-      tmem_ld_parts<BF16>(tmem + lane_off + C::kColO + 16 * oB, acc[1]);
+      tmem_ld_parts(tmem + lane_off + C::kColO + 16 * oA, acc[0]);
+      tmem_ld_parts(tmem + lane_off + C::kColO + 16 * oB, acc[1]);
       tc_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -1136,7 +1130,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           o[u] = add2(f2u(acc[u][k], acc[u][k + 1]), f2u(acc[u][4 + k], acc[u][5 + k]));
-          if (!BF16) o[u] = add2(o[u], f2u(acc[u][8 + k], acc[u][9 + k]));
+          o[u] = add2(o[u], f2u(acc[u][8 + k], acc[u][9 + k]));
           o[u] = mul2(o[u], pinv);
         }
         if (pend_n < 2) o[1] = f2s(0.f);
@@ -1263,7 +1257,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       }
       if (seg_first) {
         pb = it.b; ph = it.h; pfirst = ustart >= g0; pus = ustart; pue = uend;
-        const SegConsts sc4 = softmax_unit_consts<KCW, BF16>(
+        const SegConsts sc4 = softmax_unit_consts<KCW>(
             p.q + ((size_t)it.b * p.num_q_heads + (size_t)it.h * gq) * kHeadDim, gq, i, p.sm_scale_log2,
             C::kCodeInv);
 #pragma unroll
@@ -1294,8 +1288,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       if (sw == 0) { KVQ_TR(18, t) if (n > 1) KVQ_TR(18, t + 1) }
       tc_fence_after();
       uint32_t acc[2][12];
-      tmem_ld_parts<BF16>(tmem + lane_off + C::kColS + 16 * q0, acc[0]);
-      tmem_ld_parts<BF16>(tmem + lane_off + C::kColS + 16 * q1, acc[1]);
+      tmem_ld_parts(tmem + lane_off + C::kColS + 16 * q0, acc[0]);
+      tmem_ld_parts(tmem + lane_off + C::kColS + 16 * q1, acc[1]);
       float ks_t[2], kz_t[2], fs_t[2] = {1.f, 1.f};
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
@@ -1306,7 +1300,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
         vs_t[u] = h2f(szp[2 * kBlockTokens + i]);
         vz_t[u] = h2f(szp[3 * kBlockTokens + i]);
         // channel-wise K: undo this group's Q' prescale (the converters' factor)
-        if (KCW && !BF16) fs_t[u] = pow2_group_inv(f16_exp_field(max_f16_bits_128(szp)));
+        if (KCW) fs_t[u] = pow2_group_inv(f16_exp_field(max_f16_bits_128(szp)));
       }
       if (n < 2) { kz_t[1] = 0.f; vs_t[1] = 0.f; vz_t[1] = 0.f; }
       // what does not depend on the scores runs while their loads are in flight:
@@ -1335,7 +1329,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
 #pragma unroll
         for (int k = 0; k < 4; k += 2) {  // heads k, k + 1
           float2 a = add2(f2u(acc[u][k], acc[u][k + 1]), f2u(acc[u][4 + k], acc[u][5 + k]));
-          if (!BF16) a = add2(a, f2u(acc[u][8 + k], acc[u][9 + k]));
+          a = add2(a, f2u(acc[u][8 + k], acc[u][9 + k]));
           // channel-wise K adds q . z_g once reduced over channels
           const float2 addk = make_float2(add[k], add[k + 1]);
           const float2 v = KCW ? mul2(a, mul2(addk, fs2))
@@ -1395,7 +1389,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
           const float c0 = h ? cg0.y : cg0.x, c1 = h ? cg1.y : cg1.x;
           const float mt = KCW ? fmaxf(res[kTM + k + h] + c0, res[kTM + 4 + k + h] + c1) : res[kTM + k + h];
           const float mnh = fmaxf(m[k + h], mt);
-          pexp |= ((uint32_t)(BF16 ? 6 : p_exponent(mt - mnh, e_v)) & 0xffu) << (8 * (k + h));
+          pexp |= ((uint32_t)p_exponent(mt - mnh, e_v) & 0xffu) << (8 * (k + h));
           alpha[k + h] = ex2(m[k + h] - mnh);
           m[k + h] = mnh;
           if (h) mn.y = mnh; else mn.x = mnh;
@@ -1429,18 +1423,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
       {
         float psc[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) psc[k] = BF16 ? 1.0f : p_scale(pexp, k);
+        for (int k = 0; k < 4; ++k) psc[k] = p_scale(pexp, k);
         uint4 bytes[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const float2 f = f2s((VCW ? 1.0f : vs_t[u]) * odd_quarter<BITS, BF16, C::kE2V>(i));
+          const float2 f = f2s((VCW ? 1.0f : vs_t[u]) * odd_quarter<BITS, false, C::kE2V>(i));
           const float2 lo = mul2(make_float2(pr[4 * u], pr[4 * u + 1]), mul2(f, make_float2(psc[0], psc[1])));
           const float2 hi = mul2(make_float2(pr[4 * u + 2], pr[4 * u + 3]), mul2(f, make_float2(psc[2], psc[3])));
           const float4 pv = make_float4(lo.x, lo.y, hi.x, hi.y);
-          bytes[u] = BF16 ? split2_bf16(pv) : split3_e4m3_via_f16(pv);
+          bytes[u] = split3_e4m3_via_f16(pv);
         }
-        *reinterpret_cast<uint4*>(pop + q0 * C::kBBytes + b_row_off<BF16>(prow)) = bytes[0];
-        if (n > 1) *reinterpret_cast<uint4*>(pop + q1 * C::kBBytes + b_row_off<BF16>(prow)) = bytes[1];
+        *reinterpret_cast<uint4*>(pop + q0 * C::kBBytes + b_row_off(prow)) = bytes[0];
+        if (n > 1) *reinterpret_cast<uint4*>(pop + q1 * C::kBBytes + b_row_off(prow)) = bytes[1];
       }
       fence_proxy_async_smem();  // both P' rows visible to the tensor core
       __syncwarp();
@@ -1485,11 +1479,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2) decode_kernel(const DecodeP
   }
 }
 
-template <int BITS, bool KCW, bool VCW, bool BF16, bool GQ4, bool E2V = false>
+template <int BITS, bool KCW, bool VCW, bool GQ4, bool E2V = false>
 cudaError_t launch_decode_instance(const DecodeParams& p, cudaStream_t stream) {
-  constexpr size_t smem = decode_smem_layout_bytes<BITS, BF16, E2V>();
+  constexpr size_t smem = decode_smem_layout_bytes<BITS, E2V>();
   static_assert(smem <= 113 * 1024, "two CTAs per SM");
-  auto kern = decode_kernel<BITS, KCW, VCW, BF16, GQ4, E2V>;
+  auto kern = decode_kernel<BITS, KCW, VCW, GQ4, E2V>;
   // The register split inside the kernel assumes exactly kRegsLaunch
   // registers per thread at launch; with fewer, the softmax warpgroup's
   // increase could never be granted.  Refuse to launch such a build.

@@ -8,10 +8,12 @@ cudaError_t launch_general_d128_bf16(int bits, bool kcw, bool vcw, int group, co
   if (bits == 4) {
     if (group == 32) return gen::launch_schemes<4, 128, 32, true>(kcw, vcw, p, grid, shape, s);
     if (group == 64) return gen::launch_schemes<4, 128, 64, true>(kcw, vcw, p, grid, shape, s);
+    if (group == 128) return gen::launch_schemes<4, 128, 128, true>(kcw, vcw, p, grid, shape, s);
   }
   if (bits == 2) {
     if (group == 32) return gen::launch_schemes<2, 128, 32, true>(kcw, vcw, p, grid, shape, s);
     if (group == 64) return gen::launch_schemes<2, 128, 64, true>(kcw, vcw, p, grid, shape, s);
+    if (group == 128) return gen::launch_schemes<2, 128, 128, true>(kcw, vcw, p, grid, shape, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -1,4 +1,4 @@
-// Decode-attention kernel instances for 2-bit caches (all K/V scheme pairs, both operand modes);
+// Decode-attention kernel instances for 2-bit caches (all K/V scheme pairs, E4M3 operands);
 // GQ4 selects 4 query heads per KV head (this file) or the other groupings
 // (decode_i2_g.cu, which defines GQ4 false before including this one).
 #include "decode.cuh"
@@ -12,18 +12,12 @@ namespace kvq {
 
 constexpr bool GQ4 = KVQ_GQ4;
 
-cudaError_t KVQ_FN(int k_scheme, int v_scheme, int mode, const DecodeParams& p, cudaStream_t s) {
-  const bool kcw = k_scheme == KVQ_CHANNELWISE, vcw = v_scheme == KVQ_CHANNELWISE, bf16 = mode == KVQ_OPERANDS_BF16;
-  if (!bf16) {
-    if (!kcw && !vcw) return launch_decode_instance<2, false, false, false, GQ4>(p, s);
-    if (!kcw && vcw) return launch_decode_instance<2, false, true, false, GQ4>(p, s);
-    if (kcw && !vcw) return launch_decode_instance<2, true, false, false, GQ4>(p, s);
-    return launch_decode_instance<2, true, true, false, GQ4>(p, s);
-  }
-  if (!kcw && !vcw) return launch_decode_instance<2, false, false, true, GQ4>(p, s);
-  if (!kcw && vcw) return launch_decode_instance<2, false, true, true, GQ4>(p, s);
-  if (kcw && !vcw) return launch_decode_instance<2, true, false, true, GQ4>(p, s);
-  return launch_decode_instance<2, true, true, true, GQ4>(p, s);
+cudaError_t KVQ_FN(int k_scheme, int v_scheme, const DecodeParams& p, cudaStream_t s) {
+  const bool kcw = k_scheme == KVQ_CHANNELWISE, vcw = v_scheme == KVQ_CHANNELWISE;
+  if (!kcw && !vcw) return launch_decode_instance<2, false, false, GQ4>(p, s);
+  if (!kcw && vcw) return launch_decode_instance<2, false, true, GQ4>(p, s);
+  if (kcw && !vcw) return launch_decode_instance<2, true, false, GQ4>(p, s);
+  return launch_decode_instance<2, true, true, GQ4>(p, s);
 }
 
 }  // namespace kvq

@@ -34,6 +34,13 @@ kvq_status check_cache(const kvq_cache_desc* c) {
 
 // The specialised decode kernel's geometry; others take the general kernel.
 bool default_geometry(const kvq_cache_desc* c) { return c->head_dim == kHeadDim && group_of(c) == 128; }
+// Decode calls the block-range kernel takes: every geometry but the default,
+// and every BF16-operand call (it runs the BF16 mode faster than the
+// specialised kernel, whose tensor memory holds one K and one V tile of
+// BF16 codes).
+bool use_general(const kvq_attn_desc* d) {
+  return !default_geometry(&d->cache) || d->operand_mode == KVQ_OPERANDS_BF16;
+}
 
 }  // namespace
 
@@ -322,7 +329,7 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* 
   kvq_status s = check_attn(desc);
   if (s != KVQ_OK) return s;
   if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
-  if (!default_geometry(&desc->cache)) {
+  if (use_general(desc)) {
     GeneralPlan plan;
     s = general_plan(desc, &plan);
     if (s != KVQ_OK) return s;
@@ -362,7 +369,7 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
   if (s != KVQ_OK) return s;
   const float sm_scale = desc->sm_scale > 0.0f ? desc->sm_scale : 1.0f / std::sqrt((float)desc->cache.head_dim);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (!default_geometry(&desc->cache)) return decode_general(desc, q, k_codes, k_scale, k_zero, v_codes, v_scale,
+  if (use_general(desc)) return decode_general(desc, q, k_codes, k_scale, k_zero, v_codes, v_scale,
                                                              v_zero, seq_lens, page_table, out, lse, workspace,
                                                              workspace_bytes, dev_status, sm_scale, st);
   const int ctas = resolve_ctas(desc, sm);
@@ -397,7 +404,7 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
 #ifdef KVQ_PROFILE
   p.prof = g_prof_counters;
 #endif
-  cudaError_t e = launch_decode(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme, desc->operand_mode, p, st);
+  cudaError_t e = launch_decode(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme, p, st);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

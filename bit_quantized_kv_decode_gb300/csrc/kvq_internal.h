@@ -93,9 +93,9 @@ cudaError_t launch_dequant(const DequantParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const float* o_parts, const float* lse_parts, int rows, int splits, int head_dim, float* out,
                          float* lse, cudaStream_t stream);
 
-// Decode kernel instances: bits in {2, 4}, K/V scheme, operand mode.
-cudaError_t launch_decode(int bits, int k_scheme, int v_scheme, int mode, const DecodeParams& p, cudaStream_t stream);
+// Specialised decode kernel instances (head dim 128, groups of 128, E4M3
+// operands): bits in {2, 4}, K/V scheme.
+cudaError_t launch_decode(int bits, int k_scheme, int v_scheme, const DecodeParams& p, cudaStream_t stream);
 int decode_ctas_per_sm();
-size_t decode_smem_bytes(int bits, int mode);
 
 }  // namespace kvq

@@ -124,6 +124,10 @@ def test_general_geometry_workspace_host_only(lib):
     assert n.value == 256 + 2 * 16 * 2 * 64 * 4  # two ranges at most (max_blocks = 2)
     bf16 = _lib.AttnDesc(_cache(2, 1, 0, hd=128, group=32), 8, 32, 32, 1, 0.0, 304, 0)
     assert lib.kvq_decode_workspace_size(ctypes.byref(bf16), ctypes.byref(n)) == 0
+    # the BF16-operand mode takes the block-range kernel on every geometry
+    bf16 = _lib.AttnDesc(_cache(4, 1, 0, pages=16 * 64), 16, 32, 64, 1, 0.0, 304, 0)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(bf16), ctypes.byref(n)) == 0
+    assert n.value == rows * splits * 4 + rows * splits * 128 * 4
     bad = _lib.AttnDesc(_cache(2, 1, 0, hd=128, group=32), 8, 32, 32, 0, 0.0, 304, _lib.FLAG_E2M1_V)
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
 

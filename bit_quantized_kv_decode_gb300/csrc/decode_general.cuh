@@ -140,8 +140,11 @@ __device__ __forceinline__ void convert_row(const unsigned char* blk, int nrows,
   }
 }
 
-template <int BITS, bool KCW, bool VCW, int D, int G, bool BF16>
-__global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenParams p, int stages) {
+// NH: query heads per unit (4, or 8 with every KV block read once); they
+// come in quads of 4 -- one 16-column block (4 heads x 3 E4M3 or 2 BF16
+// parts) per quad of Q', S, P' and O.
+template <int BITS, bool KCW, bool VCW, int D, int G, bool BF16, int NH>
+__global__ void __launch_bounds__(kThreads, NH > 4 ? 2 : 4) decode_general_kernel(const GenParams p, int stages) {
   constexpr int kKBytes = kBlockTokens * D * BITS / 8;  // K (and V) codes of a block
   constexpr int kElems = BF16 ? 16 : 32;                // contraction elements per MMA
   constexpr int kCm = BF16 ? 256 : 128;                 // bytes of one B block per 8 rows
@@ -149,25 +152,28 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
   constexpr uint32_t kFmt = BF16 ? 1u : 0u;             // BF16 (kind::f16) or E4M3 (kind::f8f6f4)
   constexpr int kHalves = D > 128 ? 2 : 1;              // M = 128 halves of the channels
   constexpr int kQv = (D + 127) / 128;                  // channels per thread
+  constexpr int HH = NH / 4;                            // head quads
   constexpr int NGC = D / G;                            // channel groups (token-wise)
   constexpr int NGT = kBlockTokens / G;                 // token groups (channel-wise)
-  constexpr int NBQ = KCW ? NGT : 1;                    // 16-column blocks of Q' / of S with channel-wise K
-  constexpr int NBP = VCW ? 1 : NGC;                    // of P'
-  constexpr int NBO = VCW ? NGT : NGC;                  // of O per channel half
+  constexpr int NBQ = (KCW ? NGT : 1) * HH;             // 16-column blocks of Q' (and of S with channel-wise K)
+  constexpr int NBP = (VCW ? 1 : NGC) * HH;             // of P'
+  constexpr int NBO = (VCW ? NGT : NGC) * HH;           // of O per channel half
   constexpr int NSZ = kBlockTokens * D / G;
-  constexpr int NM = VCW ? 4 : 8;                       // values of the block-max reduction (+ largest V scale)
-  constexpr int NZ = VCW ? 4 : 4 * NGC;                 // values of the per-group p sums
+  constexpr int NM = VCW ? NH : 2 * NH;                 // block-max reduction: heads (+ largest V scale)
+  constexpr int NZ = VCW ? NH : 4 * NGC;                // per-group p sums (token-wise V: one quad at a time)
+  constexpr bool kQszSmem = NH > 4;                     // token-wise K's q sums in shared memory
   extern __shared__ __align__(1024) unsigned char smem[];
-  const GenLayout L = gen_layout(BITS, D, G, KCW, VCW, BF16, stages);  // shared-memory offsets (depend on stages)
-  constexpr GenLayout LT = gen_layout(BITS, D, G, KCW, VCW, BF16, 2);  // tensor-memory columns (do not)
+  const GenLayout L = gen_layout(BITS, D, G, KCW, VCW, BF16, NH, stages);  // shared-memory offsets
+  constexpr GenLayout LT = gen_layout(BITS, D, G, KCW, VCW, BF16, NH, 2);  // tensor-memory columns
   constexpr bool kSeq = LT.seq_halves;
 
   unsigned char* qop = smem + L.q_off;  // [D rows][NBQ blocks]
   unsigned char* pop = smem + L.p_off;  // [128 rows][NBP blocks]
-  float* red_c = reinterpret_cast<float*>(smem + L.scratch_off);  // [4][16] q . z_g (channel-wise K)
-  float* red_m = red_c + 64;                                      // [4][8] block maxima
-  float* red_z = red_m + 32;                                      // [4][32] per-group p (z) sums
-  uint32_t* eg_w = reinterpret_cast<uint32_t*>(red_z + 128);      // [4][4] per-warp largest K scale of group g
+  float* red_c = reinterpret_cast<float*>(smem + L.scratch_off);  // [4][32] q . z_g (channel-wise K)
+  float* red_m = red_c + 128;                                     // [4][16] block maxima
+  float* red_z = red_m + 64;                                      // [2][4][32] per-group p (z) sums
+  float* qsz_s = red_z + 256;                                     // [8][8] token-wise K q sums (NH = 8)
+  uint32_t* eg_w = reinterpret_cast<uint32_t*>(qsz_s + 64);       // [4][4] per-warp largest K scale of group g
   uint64_t* bars = reinterpret_cast<uint64_t*>(eg_w + 16);        // stages [4], mma, drain
   uint32_t* tbase = reinterpret_cast<uint32_t*>(bars + 6);
   int* ok_flag = reinterpret_cast<int*>(tbase + 1);
@@ -241,85 +247,98 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
     }
   }
 
-  // ---- per-unit query statistics (all 4 head slots; empty slots are 0)
+  // ---- per-unit query statistics (all NH head slots; empty slots are 0)
   const uint16_t* qb = p.q + row0 * D;
-  float qv[4][kQv];  // q of this thread's channels c = tid + 128 i
-  float qmax[4];
+  float qv[NH][kQv];  // q of this thread's channels c = tid + 128 i
+  float qmax[NH];
 #pragma unroll
-  for (int h = 0; h < 4; ++h) {
+  for (int k = 0; k < NH; ++k) {
     float m = 0.f;
 #pragma unroll
     for (int i = 0; i < kQv; ++i) {
       const int c = tid + 128 * i;
-      qv[h][i] = (h < p.gq && c < D) ? bf2f(qb[h * D + c]) : 0.f;
-      m = fmaxf(m, fabsf(qv[h][i]));
+      qv[k][i] = (k < p.gq && c < D) ? bf2f(qb[k * D + c]) : 0.f;
+      m = fmaxf(m, fabsf(qv[k][i]));
     }
-    qmax[h] = m;
+    qmax[k] = m;
   }
   {
-    float t[4] = {qmax[0], qmax[1], qmax[2], qmax[3]};
-    warp_reduce_store<4, true>(t, red_m);
+    float t[NH];
+#pragma unroll
+    for (int k = 0; k < NH; ++k) t[k] = qmax[k];
+    warp_reduce_store<NH, true>(t, red_m);
     __syncthreads();
 #pragma unroll
-    for (int h = 0; h < 4; ++h) qmax[h] = max4<4>(red_m, h);
+    for (int k = 0; k < NH; ++k) qmax[k] = max4<NH>(red_m, k);
   }
-  float mult[4];  // partial-score multiplier (log2 units)
+  float mult[NH];  // partial-score multiplier (log2 units)
 #pragma unroll
-  for (int h = 0; h < 4; ++h)
-    mult[h] = BF16 ? p.sm_scale_log2  // exact BF16 codes, no prescale
-                   : 512.0f * (KCW ? pow2_head_inv(qmax[h]) : pow2_prescale_inv(qmax[h])) * p.sm_scale_log2;
-  float qsz[NGC][4];  // token-wise K: sum of q over channel group g, times the log2 softmax scale
+  for (int k = 0; k < NH; ++k)
+    mult[k] = BF16 ? p.sm_scale_log2  // exact BF16 codes, no prescale
+                   : 512.0f * (KCW ? pow2_head_inv(qmax[k]) : pow2_prescale_inv(qmax[k])) * p.sm_scale_log2;
+  float qsz[kQszSmem ? 1 : NGC][NH];  // token-wise K: sum of q over channel group g, times the log2 scale
   if (!KCW) {
-    // Q' = q * 2^k (k per head) in three E4M3 parts at row a_pos(c); and the
-    // per-channel-group sums of q for the offset term
+    // Q' = q * 2^k (k per head) in three E4M3 parts at row a_pos(c), one
+    // block per head quad; and the per-channel-group sums of q for the offset
 #pragma unroll
     for (int i = 0; i < kQv; ++i) {
       const int c = tid + 128 * i;
       if (c < D) {
         const float f = odd_quarter<BITS, BF16>(c);
-        float4 v;
-        if (BF16) {
-          v = make_float4(qv[0][i] * f, qv[1][i] * f, qv[2][i] * f, qv[3][i] * f);
-        } else {
-          v = make_float4(qv[0][i] * pow2_prescale(qmax[0]) * f, qv[1][i] * pow2_prescale(qmax[1]) * f,
-                          qv[2][i] * pow2_prescale(qmax[2]) * f, qv[3][i] * pow2_prescale(qmax[3]) * f);
+#pragma unroll
+        for (int hq = 0; hq < HH; ++hq) {
+          float x[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) x[h] = qv[4 * hq + h][i] * (BF16 ? 1.0f : pow2_prescale(qmax[4 * hq + h])) * f;
+          const float4 v = make_float4(x[0], x[1], x[2], x[3]);
+          *reinterpret_cast<uint4*>(qop + b_off<BF16>(a_pos<BITS, BF16>(c), hq, HH)) = BF16 ? split2_bf16(v)
+                                                                                           : split3_e4m3(v);
         }
-        *reinterpret_cast<uint4*>(qop + b_off<BF16>(a_pos<BITS, BF16>(c), 0, 1)) = BF16 ? split2_bf16(v)
-                                                                                        : split3_e4m3(v);
       }
     }
-    float t[4 * NGC];
 #pragma unroll
-    for (int g = 0; g < NGC; ++g)
+    for (int hq = 0; hq < HH; ++hq) {
+      float t[4 * NGC];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float s = 0.f;
+      for (int g = 0; g < NGC; ++g)
 #pragma unroll
-        for (int i = 0; i < kQv; ++i)
-          if ((tid + 128 * i) / G == g && tid + 128 * i < D) s += qv[h][i];
-        t[g * 4 + h] = s;
-      }
-    warp_reduce_store<4 * NGC, false>(t, red_z);
+        for (int h = 0; h < 4; ++h) {
+          float s = 0.f;
+#pragma unroll
+          for (int i = 0; i < kQv; ++i)
+            if ((tid + 128 * i) / G == g && tid + 128 * i < D) s += qv[4 * hq + h][i];
+          t[g * 4 + h] = s;
+        }
+      warp_reduce_store<4 * NGC, false>(t, red_z + hq * 128);
+    }
     fence_proxy_async_smem();
     __syncthreads();
 #pragma unroll
     for (int g = 0; g < NGC; ++g)
 #pragma unroll
-      for (int h = 0; h < 4; ++h) qsz[g][h] = sum4<4 * NGC>(red_z, g * 4 + h) * p.sm_scale_log2;
+      for (int k = 0; k < NH; ++k) {
+        const float v = sum4<4 * NGC>(red_z + (k >> 2) * 128, g * 4 + (k & 3)) * p.sm_scale_log2;
+        if (kQszSmem) {
+          if (tid == 0) qsz_s[g * NH + k] = v;
+        } else {
+          qsz[kQszSmem ? 0 : g][k] = v;
+        }
+      }
+    if (kQszSmem) __syncthreads();
   }
-  float qk[4][kQv];  // channel-wise K: q * 2^(6 - E_q)
+  float qk[NH][kQv];  // channel-wise K: q * 2^(6 - E_q)
 #pragma unroll
-  for (int h = 0; h < 4; ++h)
+  for (int k = 0; k < NH; ++k)
 #pragma unroll
-    for (int i = 0; i < kQv; ++i) qk[h][i] = BF16 ? qv[h][i] : qv[h][i] * pow2_head(qmax[h]);
+    for (int i = 0; i < kQv; ++i) qk[k][i] = BF16 ? qv[k][i] : qv[k][i] * pow2_head(qmax[k]);
 
-  float m_run[4], l_thr[4], oacc[kHalves][4], zacc[kHalves][4];
+  float m_run[NH], l_thr[NH], oacc[kHalves][NH], zacc[kHalves][NH];
 #pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    m_run[h] = -INFINITY;
-    l_thr[h] = 0.f;
+  for (int k = 0; k < NH; ++k) {
+    m_run[k] = -INFINITY;
+    l_thr[k] = 0.f;
 #pragma unroll
-    for (int hf = 0; hf < kHalves; ++hf) oacc[hf][h] = zacc[hf][h] = 0.f;
+    for (int hf = 0; hf < kHalves; ++hf) oacc[hf][k] = zacc[hf][k] = 0.f;
   }
 
   bool ok = true;
@@ -360,9 +379,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
       __syncthreads();
     }
     if (KCW) {
-      float t[4 * NGT];
+      float t[NH * NGT];  // q . z_g, value g * NH + k
 #pragma unroll
-      for (int k = 0; k < 4 * NGT; ++k) t[k] = 0.f;
+      for (int k = 0; k < NH * NGT; ++k) t[k] = 0.f;
 #pragma unroll
       for (int g = 0; g < NGT; ++g) {
         const float fg =
@@ -372,16 +391,20 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
           const int c = tid + 128 * i;
           if (c < D) {
             const float f = h2f(ksz[g * D + c]) * fg * odd_quarter<BITS, BF16>(c);
-            const float4 v = make_float4(qk[0][i] * f, qk[1][i] * f, qk[2][i] * f, qk[3][i] * f);
-            *reinterpret_cast<uint4*>(qop + b_off<BF16>(a_pos<BITS, BF16>(c), g, NGT)) = BF16 ? split2_bf16(v)
-                                                                                            : split3_e4m3(v);
+#pragma unroll
+            for (int hq = 0; hq < HH; ++hq) {
+              const float4 v = make_float4(qk[4 * hq][i] * f, qk[4 * hq + 1][i] * f, qk[4 * hq + 2][i] * f,
+                                           qk[4 * hq + 3][i] * f);
+              *reinterpret_cast<uint4*>(qop + b_off<BF16>(a_pos<BITS, BF16>(c), g * HH + hq, NBQ)) =
+                  BF16 ? split2_bf16(v) : split3_e4m3(v);
+            }
             const float zgc = h2f(kzz[g * D + c]);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) t[g * 4 + h] = fmaf(qv[h][i], zgc, t[g * 4 + h]);
+            for (int k = 0; k < NH; ++k) t[g * NH + k] = fmaf(qv[k][i], zgc, t[g * NH + k]);
           }
         }
       }
-      warp_reduce_store<4 * NGT, false>(t, red_c);
+      warp_reduce_store<NH * NGT, false>(t, red_c);
       fence_proxy_async_smem();
     }
 
@@ -396,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
         const uint64_t bd = make_smem_desc(smem_u32(qop) + k * 4 * NBQ * 128, NBQ * kCm, 128);
         const uint32_t a = tmem + LT.col_a + 8 * k;
         // channel-wise K: one accumulator; token-wise K: the K-steps of channel
-        // group g accumulate into S block g
-        const uint32_t d = tmem + LT.col_so + (KCW ? 0 : 16 * ((kElems * k) / G));
+        // group g accumulate into S blocks g * HH ... (both head quads)
+        const uint32_t d = tmem + LT.col_so + (KCW ? 0 : 16 * HH * ((kElems * k) / G));
         const uint32_t acc = KCW ? (k > 0) : ((kElems * k) % G != 0);
         if (BF16) mma_f16_ts(d, a, bd, idesc_q, acc);
         else mma_f8f6f4_ts(d, a, bd, idesc_q, acc);
@@ -415,32 +438,44 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
     tc_fence_after();
 
     // ---- scores of token l (log2 units), folded per group
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    float sc[NH];
+#pragma unroll
+    for (int k = 0; k < NH; ++k) sc[k] = 0.f;
     if (KCW) {
       const int g = l / G;  // warp-uniform (G >= 32)
-      uint32_t v[12];
-      ld_block<BF16>(t_so + 16 * g, v);
       const float fs =
           BF16 ? 1.0f : pow2_group_inv(f16_exp_field(max(max(eg_w[g], eg_w[4 + g]), max(eg_w[8 + g], eg_w[12 + g]))));
-      float cz[4];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) cz[h] = sum4<4 * NGT>(red_c, g * 4 + h) * p.sm_scale_log2;
-      tc_wait_ld();
+      for (int hq = 0; hq < HH; ++hq) {
+        uint32_t v[12];
+        ld_block<BF16>(t_so + 16 * (g * HH + hq), v);
+        float cz[4];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) sc[h] = fmaf(parts<BF16>(v, h), mult[h] * fs, cz[h]);
+        for (int h = 0; h < 4; ++h) cz[h] = sum4<NH * NGT>(red_c, g * NH + 4 * hq + h) * p.sm_scale_log2;
+        tc_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 4; ++h) sc[4 * hq + h] = fmaf(parts<BF16>(v, h), mult[4 * hq + h] * fs, cz[h]);
+      }
     } else {
 #pragma unroll
       for (int g = 0; g < NGC; ++g) {
-        uint32_t v[12];
-        ld_block<BF16>(t_so + 16 * g, v);
         const float s_lg = h2f(ksz[l * NGC + g]), z_lg = h2f(kzz[l * NGC + g]);
-        tc_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 4; ++h) sc[h] += fmaf(parts<BF16>(v, h) * mult[h], s_lg, z_lg * qsz[g][h]);
+        for (int hq = 0; hq < HH; ++hq) {
+          uint32_t v[12];
+          ld_block<BF16>(t_so + 16 * (g * HH + hq), v);
+          tc_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int k = 4 * hq + h;
+            const float qs = kQszSmem ? qsz_s[g * NH + k] : qsz[kQszSmem ? 0 : g][k];
+            sc[k] += fmaf(parts<BF16>(v, h) * mult[k], s_lg, z_lg * qs);
+          }
+        }
       }
     }
 #pragma unroll
-    for (int h = 0; h < 4; ++h) sc[h] = valid ? sc[h] : -INFINITY;
+    for (int k = 0; k < NH; ++k) sc[k] = valid ? sc[k] : -INFINITY;
 
     // ---- V codes -> E4M3 operand (rows = channels), replacing the K codes
     //      (QK^T is complete).  A 64-dim head leaves rows 64..127 as they are:
@@ -457,66 +492,74 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
     {
       float t[NM];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) t[h] = sc[h];
+      for (int k = 0; k < NH; ++k) t[k] = sc[k];
 #pragma unroll
-      for (int k = 4; k < NM; ++k) t[k] = vmax;
+      for (int k = NH; k < NM; ++k) t[k] = vmax;
       warp_reduce_store<NM, true>(t, red_m);
     }
     tc_wait_st();
     __syncthreads();
-    float bmax[4];
+    float bmax[NH];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) bmax[h] = max4<NM>(red_m, h);
-    const int e_v = VCW ? 0 : (int)((__float_as_uint(max4<NM>(red_m, 4)) >> 23) & 0xffu) - 127;
-    float alpha[4], pr[4];
-    int pe[4];
+    for (int k = 0; k < NH; ++k) bmax[k] = max4<NM>(red_m, k);
+    const int e_v = VCW ? 0 : (int)((__float_as_uint(max4<NM>(red_m, NM - 1)) >> 23) & 0xffu) - 127;
+    float alpha[NH], pr[NH];
+    int pe[NH];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const float mn = fmaxf(m_run[h], bmax[h]);
-      alpha[h] = ex2(m_run[h] - mn);
-      m_run[h] = mn;
-      pr[h] = valid ? ex2(sc[h] - mn) : 0.f;
-      pe[h] = BF16 ? 6 : p_exponent(bmax[h] - mn, e_v);  // P' prescale 2^(6 - E) (1 for BF16)
-      l_thr[h] = fmaf(l_thr[h], alpha[h], pr[h]);
+    for (int k = 0; k < NH; ++k) {
+      const float mn = fmaxf(m_run[k], bmax[k]);
+      alpha[k] = ex2(m_run[k] - mn);
+      m_run[k] = mn;
+      pr[k] = valid ? ex2(sc[k] - mn) : 0.f;
+      pe[k] = BF16 ? 6 : p_exponent(bmax[k] - mn, e_v);  // P' prescale 2^(6 - E) (1 for BF16)
+      l_thr[k] = fmaf(l_thr[k], alpha[k], pr[k]);
     }
 
-    // per-group sums: token-wise V: sum_l p_l z_(l,g) per channel group;
-    // channel-wise V: sum_(l in g) p_l per token group (a warp's tokens lie in one group)
-    {
-      float t[NZ];
-      if (!VCW) {
+    // per-group sums: token-wise V: sum_l p_l z_(l,g) per channel group (one
+    // head quad per buffer); channel-wise V: sum_(l in g) p_l per token group
+    // (a warp's tokens lie in one group)
+    if (!VCW) {
+#pragma unroll
+      for (int hq = 0; hq < HH; ++hq) {
+        float t[NZ];
 #pragma unroll
         for (int g = 0; g < NGC; ++g) {
           const float z_lg = valid ? h2f(vzz[l * NGC + g]) : 0.f;
 #pragma unroll
-          for (int h = 0; h < 4; ++h) t[g * 4 + h] = pr[h] * z_lg;
+          for (int h = 0; h < 4; ++h) t[g * 4 + h] = pr[4 * hq + h] * z_lg;
         }
-      } else {
-#pragma unroll
-        for (int h = 0; h < 4; ++h) t[h] = pr[h];
+        warp_reduce_store<NZ, false>(t, red_z + hq * 128);
       }
+    } else {
+      float t[NZ];
+#pragma unroll
+      for (int k = 0; k < NH; ++k) t[k] = pr[k];
       warp_reduce_store<NZ, false>(t, red_z);
     }
 
-    // ---- P' operand: row a_pos(l), one 16-column block per channel group (token-wise V)
+    // ---- P' operand: row a_pos(l), one 16-column block per channel group
+    //      (token-wise V) and head quad
     {
       const float oq = odd_quarter<BITS, BF16>(l);
-      float ps[4];
+      float ps[NH];
 #pragma unroll
-      for (int h = 0; h < 4; ++h) ps[h] = pr[h] * oq * __uint_as_float((uint32_t)(133 - pe[h]) << 23);
+      for (int k = 0; k < NH; ++k) ps[k] = pr[k] * oq * __uint_as_float((uint32_t)(133 - pe[k]) << 23);
 #pragma unroll
-      for (int g = 0; g < NBP; ++g) {
+      for (int g = 0; g < NBP / HH; ++g) {
         const float sv = VCW ? 1.0f : (valid ? h2f(vsz[l * NGC + g]) : 0.f);
-        const float4 v = make_float4(ps[0] * sv, ps[1] * sv, ps[2] * sv, ps[3] * sv);
-        *reinterpret_cast<uint4*>(pop + b_off<BF16>(a_pos<BITS, BF16>(l), g, NBP)) =
-            BF16 ? split2_bf16(v) : split3_e4m3_via_f16(v);
+#pragma unroll
+        for (int hq = 0; hq < HH; ++hq) {
+          const float4 v = make_float4(ps[4 * hq] * sv, ps[4 * hq + 1] * sv, ps[4 * hq + 2] * sv, ps[4 * hq + 3] * sv);
+          *reinterpret_cast<uint4*>(pop + b_off<BF16>(a_pos<BITS, BF16>(l), g * HH + hq, NBP)) =
+              BF16 ? split2_bf16(v) : split3_e4m3_via_f16(v);
+        }
       }
     }
     fence_proxy_async_smem();
 
-    float pinv[4];  // 2^(E - 6), times 2^9 for E4M3 codes (code * 2^-9)
+    float pinv[NH];  // 2^(E - 6), times 2^9 for E4M3 codes (code * 2^-9)
 #pragma unroll
-    for (int h = 0; h < 4; ++h) pinv[h] = __uint_as_float((uint32_t)((BF16 ? 121 : 130) + pe[h]) << 23);
+    for (int k = 0; k < NH; ++k) pinv[k] = __uint_as_float((uint32_t)((BF16 ? 121 : 130) + pe[k]) << 23);
 
     // ---- PV: O[channel][column block] per M = 128 half of the channels, then
     //      the epilogue: channel c = 128 hf + tid; undo the P' prescale, fold V
@@ -533,12 +576,12 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
 #pragma unroll
           for (int k = 0; k < kBlockTokens / kElems; ++k) {
             const uint32_t a = tmem + LT.col_a + kVCols * hf + 8 * k;
-            // channel-wise V: the K-steps of token group g accumulate into O block g
-            const uint64_t bd = VCW ? make_smem_desc(smem_u32(pop) + k * 4 * 128, kCm, 128)
-                                    : make_smem_desc(smem_u32(pop) + k * 4 * NGC * 128, NGC * kCm, 128);
-            const uint32_t d = VCW ? o + 16 * ((kElems * k) / G) : o;
+            // channel-wise V: the K-steps of token group g accumulate into O
+            // blocks g * HH ... (both head quads)
+            const uint64_t bd = make_smem_desc(smem_u32(pop) + k * 4 * NBP * 128, NBP * kCm, 128);
+            const uint32_t d = VCW ? o + 16 * HH * ((kElems * k) / G) : o;
             const uint32_t acc = VCW ? ((kElems * k) % G != 0) : (k > 0);
-            constexpr uint32_t idesc_p = make_idesc(kFmt, kFmt, 0, 1, 128, VCW ? 16 : 16 * NGC);
+            constexpr uint32_t idesc_p = make_idesc(kFmt, kFmt, 0, 1, 128, 16 * NBP);
             if (BF16) mma_f16_ts(d, a, bd, idesc_p, acc);
             else mma_f8f6f4_ts(d, a, bd, idesc_p, acc);
           }
@@ -553,37 +596,47 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
         if (kSeq && hf != pass) continue;
         const int c = hf * 128 + tid;
         const uint32_t o = t_so + (kSeq ? 0 : hf * 16 * NBO);
-        float add[4] = {0.f, 0.f, 0.f, 0.f};
+        float add[NH];
+#pragma unroll
+        for (int k = 0; k < NH; ++k) add[k] = 0.f;
         if (VCW) {
 #pragma unroll
           for (int g = 0; g < NGT; ++g) {
-            uint32_t v[12];
-            ld_block<BF16>(o + 16 * g, v);
-            tc_wait_ld();
-            if (g * G >= nv || c >= D) continue;  // no valid token in this group / no such channel
-            const float s_gc = h2f(vsz[g * D + c]), z_gc = h2f(vzz[g * D + c]);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              float psum = 0.f;  // sum of p over the group's tokens (the warps covering them)
+            for (int hq = 0; hq < HH; ++hq) {
+              uint32_t v[12];
+              ld_block<BF16>(o + 16 * (g * HH + hq), v);
+              tc_wait_ld();
+              if (g * G >= nv || c >= D) continue;  // no valid token in this group / no such channel
+              const float s_gc = h2f(vsz[g * D + c]), z_gc = h2f(vzz[g * D + c]);
 #pragma unroll
-              for (int w = 0; w < 4; ++w)
-                if ((32 * w) / G == g) psum += red_z[w * 4 + h];
-              add[h] = fmaf(s_gc, parts<BF16>(v, h) * pinv[h], fmaf(z_gc, psum, add[h]));
+              for (int h = 0; h < 4; ++h) {
+                const int k = 4 * hq + h;
+                float psum = 0.f;  // sum of p over the group's tokens (the warps covering them)
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                  if ((32 * w) / G == g) psum += red_z[w * NZ + k];
+                add[k] = fmaf(s_gc, parts<BF16>(v, h) * pinv[k], fmaf(z_gc, psum, add[k]));
+              }
             }
           }
         } else {
           const int g = (c < D ? c : 0) / G;  // warp-uniform (G >= 32)
-          uint32_t v[12];
-          ld_block<BF16>(o + 16 * g, v);
-          tc_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            add[h] = parts<BF16>(v, h) * pinv[h];
-            zacc[hf][h] = fmaf(zacc[hf][h], alpha[h], sum4<NZ>(red_z, g * 4 + h));
+          for (int hq = 0; hq < HH; ++hq) {
+            uint32_t v[12];
+            ld_block<BF16>(o + 16 * (g * HH + hq), v);
+            tc_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int k = 4 * hq + h;
+              add[k] = parts<BF16>(v, h) * pinv[k];
+              zacc[hf][k] = fmaf(zacc[hf][k], alpha[k], sum4<NZ>(red_z + hq * 128, g * 4 + h));
+            }
           }
         }
 #pragma unroll
-        for (int h = 0; h < 4; ++h) oacc[hf][h] = fmaf(oacc[hf][h], alpha[h], add[h]);
+        for (int k = 0; k < NH; ++k) oacc[hf][k] = fmaf(oacc[hf][k], alpha[k], add[k]);
       }
     }
     if (!ok) break;
@@ -598,23 +651,28 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
   // ---- this range's part: O / l and lse = m + ln l per head
   if (ok) {
     {
-      float t[4] = {l_thr[0], l_thr[1], l_thr[2], l_thr[3]};
-      warp_reduce_store<4, false>(t, red_m);
+      float t[NH];
+#pragma unroll
+      for (int k = 0; k < NH; ++k) t[k] = l_thr[k];
+      warp_reduce_store<NH, false>(t, red_m);
     }
     __syncthreads();
-    float l_run[4];
+    float l_run[NH];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) l_run[h] = sum4<4>(red_m, h);
+    for (int k = 0; k < NH; ++k) l_run[k] = sum4<NH>(red_m, k);
 #pragma unroll
     for (int hf = 0; hf < kHalves; ++hf) {
       const int c = hf * 128 + tid;
       if (c < D) {
-        for (int k = 0; k < p.gq; ++k)
-          p.part_o[((row0 + k) * p.splits + split) * D + c] = (oacc[hf][k] + zacc[hf][k]) / l_run[k];
+#pragma unroll
+        for (int k = 0; k < NH; ++k)
+          if (k < p.gq) p.part_o[((row0 + k) * p.splits + split) * D + c] = (oacc[hf][k] + zacc[hf][k]) / l_run[k];
       }
     }
-    if (tid < p.gq)
-      p.part_lse[(row0 + tid) * p.splits + split] = (m_run[tid] + __log2f(l_run[tid])) * 0.69314718055994530942f;
+#pragma unroll
+    for (int k = 0; k < NH; ++k)
+      if (tid == k && k < p.gq)
+        p.part_lse[(row0 + k) * p.splits + split] = (m_run[k] + __log2f(l_run[k])) * 0.69314718055994530942f;
   } else if (tid == 0) {
     report(p.dev_status, KVQ_DEV_TIMEOUT);
   }
@@ -635,22 +693,21 @@ __global__ void __launch_bounds__(kThreads, 4) decode_general_kernel(const GenPa
   }
 }
 
-template <int BITS, bool KCW, bool VCW, int D, int G, bool BF16>
+template <int BITS, bool KCW, bool VCW, int D, int G, bool BF16, int NH>
 cudaError_t launch_instance(const GenParams& p, int grid, const GenLaunch& shape, cudaStream_t stream) {
-  auto kern = decode_general_kernel<BITS, KCW, VCW, D, G, BF16>;
+  auto kern = decode_general_kernel<BITS, KCW, VCW, D, G, BF16, NH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shape.smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, shape.smem, stream>>>(p, shape.stages);
   return cudaGetLastError();
 }
 
-template <int BITS, int D, int G, bool BF16>
-cudaError_t launch_schemes(bool kcw, bool vcw, const GenParams& p, int grid, const GenLaunch& shape,
-                           cudaStream_t s) {
-  if (!kcw && !vcw) return launch_instance<BITS, false, false, D, G, BF16>(p, grid, shape, s);
-  if (!kcw && vcw) return launch_instance<BITS, false, true, D, G, BF16>(p, grid, shape, s);
-  if (kcw && !vcw) return launch_instance<BITS, true, false, D, G, BF16>(p, grid, shape, s);
-  return launch_instance<BITS, true, true, D, G, BF16>(p, grid, shape, s);
+template <int BITS, int D, int G, bool BF16, int NH>
+cudaError_t launch_schemes(bool kcw, bool vcw, const GenParams& p, int grid, const GenLaunch& shape, cudaStream_t s) {
+  if (!kcw && !vcw) return launch_instance<BITS, false, false, D, G, BF16, NH>(p, grid, shape, s);
+  if (!kcw && vcw) return launch_instance<BITS, false, true, D, G, BF16, NH>(p, grid, shape, s);
+  if (kcw && !vcw) return launch_instance<BITS, true, false, D, G, BF16, NH>(p, grid, shape, s);
+  return launch_instance<BITS, true, true, D, G, BF16, NH>(p, grid, shape, s);
 }
 
 }  // namespace gen

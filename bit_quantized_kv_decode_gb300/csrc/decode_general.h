@@ -43,7 +43,7 @@ struct GenLayout {
   bool seq_halves;  // PV one channel half at a time
 };
 
-constexpr int kGenScratchBytes = 1280;
+constexpr int kGenScratchBytes = 2304;  // reduction buffers, per-group values, barriers (2,168 used)
 
 __host__ __device__ constexpr int gen_pow2_cols(int used) {
   return used <= 32 ? 32 : used <= 64 ? 64 : used <= 128 ? 128 : used <= 256 ? 256 : 512;
@@ -51,19 +51,20 @@ __host__ __device__ constexpr int gen_pow2_cols(int used) {
 
 // bf16: codes as exact BF16 values (two bytes each: twice the operand
 // columns) and Q' / P' as two BF16 parts (32-byte rows); else E4M3.
-__host__ __device__ constexpr GenLayout gen_layout(int bits, int D, int G, bool kcw, bool vcw, bool bf16,
+// nh: query heads per unit (4 or 8): one column block per quad of heads.
+__host__ __device__ constexpr GenLayout gen_layout(int bits, int D, int G, bool kcw, bool vcw, bool bf16, int nh,
                                                    int stages) {
-  const int halves = D > 128 ? 2 : 1, ngc = D / G, ngt = kBlockTokens / G, w = bf16 ? 2 : 1;
+  const int halves = D > 128 ? 2 : 1, ngc = D / G, ngt = kBlockTokens / G, w = bf16 ? 2 : 1, hh = nh / 4;
   const int a_cols = w * ((D / 4 > 32 * halves) ? D / 4 : 32 * halves);
-  const int s_cols = 16 * (kcw ? ngt : ngc);
-  const int o_all = halves * 16 * (vcw ? ngt : ngc);
+  const int s_cols = 16 * (kcw ? ngt : ngc) * hh;
+  const int o_all = halves * 16 * (vcw ? ngt : ngc) * hh;
   const bool seq = a_cols + (s_cols > o_all ? s_cols : o_all) > 256;
   const int o_cols = seq ? o_all / halves : o_all;
   const int nsz = kBlockTokens * D / G;
   const int stage_bytes = 2 * (kBlockTokens * D * bits / 8) + 4 * nsz * 2;
   const int q_off = stages * stage_bytes;
-  const int p_off = q_off + D * 16 * w * (kcw ? ngt : 1);  // Q': D rows x (block per token group)
-  const int scratch_off = p_off + kBlockTokens * 16 * w * (vcw ? 1 : ngc);  // P': 128 rows x (block per channel group)
+  const int p_off = q_off + D * 16 * w * (kcw ? ngt : 1) * hh;  // Q': D rows x (block per token group, quad)
+  const int scratch_off = p_off + kBlockTokens * 16 * w * (vcw ? 1 : ngc) * hh;  // P': 128 rows x (block per channel group, quad)
   return GenLayout{nsz, stage_bytes, stages, q_off, p_off, scratch_off, scratch_off + kGenScratchBytes, 0, a_cols,
                    gen_pow2_cols(a_cols + (s_cols > o_cols ? s_cols : o_cols)), seq};
 }
@@ -76,10 +77,10 @@ struct GenLaunch {
 
 // Launch shape of the general kernel on a device with `smem_per_sm` bytes of
 // shared memory per SM (`smem_reserved_per_cta` of them taken per CTA).
-GenLaunch general_launch_shape(int bits, int k_scheme, int v_scheme, int head_dim, int group, bool bf16,
+GenLaunch general_launch_shape(int bits, int k_scheme, int v_scheme, int head_dim, int group, bool bf16, int nh,
                                int smem_per_sm, int smem_reserved_per_cta);
 
-cudaError_t launch_decode_general(int bits, int k_scheme, int v_scheme, int head_dim, int group, bool bf16,
+cudaError_t launch_decode_general(int bits, int k_scheme, int v_scheme, int head_dim, int group, bool bf16, int nh,
                                   const GenParams& p, int grid, const GenLaunch& shape, cudaStream_t stream);
 
 }  // namespace kvq

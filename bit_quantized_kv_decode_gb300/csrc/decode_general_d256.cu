@@ -1,4 +1,4 @@
-// General-geometry decode kernel instances for head dim 256, E4M3 operands.
+// General-geometry decode kernel instances for head dim 256, E4M3 operands, 4 query heads per unit.
 #include "decode_general.cuh"
 
 namespace kvq {
@@ -6,14 +6,14 @@ namespace kvq {
 cudaError_t launch_general_d256(int bits, bool kcw, bool vcw, int group, const GenParams& p, int grid,
                                 const GenLaunch& shape, cudaStream_t s) {
   if (bits == 4) {
-    if (group == 32) return gen::launch_schemes<4, 256, 32, false>(kcw, vcw, p, grid, shape, s);
-    if (group == 64) return gen::launch_schemes<4, 256, 64, false>(kcw, vcw, p, grid, shape, s);
-    if (group == 128) return gen::launch_schemes<4, 256, 128, false>(kcw, vcw, p, grid, shape, s);
+    if (group == 32) return gen::launch_schemes<4, 256, 32, false, 4>(kcw, vcw, p, grid, shape, s);
+    if (group == 64) return gen::launch_schemes<4, 256, 64, false, 4>(kcw, vcw, p, grid, shape, s);
+    if (group == 128) return gen::launch_schemes<4, 256, 128, false, 4>(kcw, vcw, p, grid, shape, s);
   }
   if (bits == 2) {
-    if (group == 32) return gen::launch_schemes<2, 256, 32, false>(kcw, vcw, p, grid, shape, s);
-    if (group == 64) return gen::launch_schemes<2, 256, 64, false>(kcw, vcw, p, grid, shape, s);
-    if (group == 128) return gen::launch_schemes<2, 256, 128, false>(kcw, vcw, p, grid, shape, s);
+    if (group == 32) return gen::launch_schemes<2, 256, 32, false, 4>(kcw, vcw, p, grid, shape, s);
+    if (group == 64) return gen::launch_schemes<2, 256, 64, false, 4>(kcw, vcw, p, grid, shape, s);
+    if (group == 128) return gen::launch_schemes<2, 256, 128, false, 4>(kcw, vcw, p, grid, shape, s);
   }
   return cudaErrorInvalidValue;
 }

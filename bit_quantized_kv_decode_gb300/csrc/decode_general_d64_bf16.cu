@@ -1,4 +1,4 @@
-// General-geometry decode kernel instances for head dim 64, BF16 operands.
+// General-geometry decode kernel instances for head dim 64, BF16 operands, 4 query heads per unit.
 #include "decode_general.cuh"
 
 namespace kvq {
@@ -6,12 +6,12 @@ namespace kvq {
 cudaError_t launch_general_d64_bf16(int bits, bool kcw, bool vcw, int group, const GenParams& p, int grid,
                                     const GenLaunch& shape, cudaStream_t s) {
   if (bits == 4) {
-    if (group == 32) return gen::launch_schemes<4, 64, 32, true>(kcw, vcw, p, grid, shape, s);
-    if (group == 64) return gen::launch_schemes<4, 64, 64, true>(kcw, vcw, p, grid, shape, s);
+    if (group == 32) return gen::launch_schemes<4, 64, 32, true, 4>(kcw, vcw, p, grid, shape, s);
+    if (group == 64) return gen::launch_schemes<4, 64, 64, true, 4>(kcw, vcw, p, grid, shape, s);
   }
   if (bits == 2) {
-    if (group == 32) return gen::launch_schemes<2, 64, 32, true>(kcw, vcw, p, grid, shape, s);
-    if (group == 64) return gen::launch_schemes<2, 64, 64, true>(kcw, vcw, p, grid, shape, s);
+    if (group == 32) return gen::launch_schemes<2, 64, 32, true, 4>(kcw, vcw, p, grid, shape, s);
+    if (group == 64) return gen::launch_schemes<2, 64, 64, true, 4>(kcw, vcw, p, grid, shape, s);
   }
   return cudaErrorInvalidValue;
 }

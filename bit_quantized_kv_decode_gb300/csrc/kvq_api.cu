@@ -120,6 +120,8 @@ kvq_status check_attn(const kvq_attn_desc* d) {
 // ceil(num_ctas / units).  At most max_blocks ranges per unit.
 struct GeneralPlan {
   GenLaunch launch;
+  int nh;            // query heads per unit: 8 (each KV block read once) or 4
+  int units;         // units per sequence
   int splits;
   size_t part_lse, part_o, total;  // workspace offsets and size
 };
@@ -137,9 +139,12 @@ kvq_status general_plan(const kvq_attn_desc* d, GeneralPlan* plan) {
       return KVQ_ERR_DEVICE;
     }
   }
+  plan->nh = heads_per_kv(d) == 8 ? 8 : 4;
+  plan->units = plan->nh == 8 ? d->cache.num_kv_heads : units_per_seq(d);
   plan->launch = general_launch_shape(d->cache.bits, d->cache.k_scheme, d->cache.v_scheme, d->cache.head_dim,
-                                      group_of(&d->cache), d->operand_mode == KVQ_OPERANDS_BF16, smem_sm, reserved);
-  const long long units = (long long)d->batch * units_per_seq(d);
+                                      group_of(&d->cache), d->operand_mode == KVQ_OPERANDS_BF16, plan->nh, smem_sm,
+                                      reserved);
+  const long long units = (long long)d->batch * plan->units;
   long long splits;
   if (d->num_ctas > 0) {
     splits = (d->num_ctas + units - 1) / units;
@@ -193,9 +198,9 @@ kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const ui
   p.batch = desc->batch; p.num_kv_heads = desc->cache.num_kv_heads; p.num_q_heads = desc->num_q_heads;
   p.max_blocks = desc->max_blocks; p.num_pages = desc->cache.num_pages;
   const int g = heads_per_kv(desc);
-  p.gq = g < kGroupQ ? g : kGroupQ;
-  p.units_per_seq = units_per_seq(desc);
-  p.kv_shift = g > kGroupQ ? 1 : 0;
+  p.gq = plan.nh == 8 ? 8 : (g < kGroupQ ? g : kGroupQ);
+  p.units_per_seq = plan.units;
+  p.kv_shift = 0;  // a unit is one KV head (up to 8 query heads)
   p.splits = plan.splits;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.flags = desc->flags;
@@ -205,7 +210,7 @@ kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const ui
   const int grid = desc->batch * p.units_per_seq * plan.splits;
   cudaError_t e = launch_decode_general(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme,
                                         desc->cache.head_dim, group_of(&desc->cache),
-                                        desc->operand_mode == KVQ_OPERANDS_BF16, p, grid, plan.launch, st);
+                                        desc->operand_mode == KVQ_OPERANDS_BF16, plan.nh, p, grid, plan.launch, st);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   e = launch_merge(p.part_o, p.part_lse, desc->batch * desc->num_q_heads, plan.splits, desc->cache.head_dim, out, lse,
                    st);

@@ -120,3 +120,115 @@ def test_decode_geometry_e2m1_unsupported():
         run_gpu(pb, flags=kvq.FLAG_E2M1_V)
     assert e.value.status == 2
 
+
+
+@pytest.mark.parametrize("D,G,bits,ks,vs", [(64, 32, 2, 1, 0), (256, 64, 4, 0, 1)])
+def test_decode_geometry_maximum_batch(D, G, bits, ks, vs):
+    """1024 sequences (the most a call takes), ragged 0..300 tokens with
+    empty ones: every sequence against the oracle."""
+    B = 1024
+    lens = np.random.default_rng(900 + D).integers(0, 301, size=B)
+    lens[::97] = 0
+    w = _w(D, G, bits, ks, vs, B=B, Hkv=1, Hq=4, L=300)
+    pb = make_problem(w, 910 + D, lens=lens.tolist())
+    res = run_gpu(pb)
+    assert res["status"] == 0
+    empty = np.flatnonzero(lens == 0)
+    assert np.all(res["out"][empty] == 0) and np.all(np.isneginf(res["lse"][empty]))
+    assert_attention_close(pb, res, 0)
+
+
+# (q scale, K scale, V scale): the prescale clamps of Q' and the group scales
+MAGNITUDES = {
+    "large_q_small_k": (1e3, 1e-3, 1.0),
+    "q_below_2^-120": (1e-37, 1.0, 1.0),
+    "zero_q": (0.0, 1.0, 1.0),
+    "fp16_subnormal_scales": (1e4, 1e-5, 1e-5),
+    "scales_near_fp16_max": (1e-4, 8e3, 8e3),
+}
+
+
+@pytest.mark.parametrize("case", sorted(MAGNITUDES))
+@pytest.mark.parametrize("D,G,bits,ks,vs", [(256, 64, 4, 1, 0), (64, 32, 2, 0, 1), (128, 32, 2, 1, 1)])
+def test_decode_geometry_extreme_magnitudes(case, D, G, bits, ks, vs):
+    import torch
+    qs, kscale, vscale = MAGNITUDES[case]
+    w = _w(D, G, bits, ks, vs, B=2, Hkv=2, Hq=8, L=600)
+    g = torch.Generator().manual_seed(1400 + D + G)
+    q = (torch.randn(2, 8, D, generator=g) * qs).to(torch.bfloat16)
+    k = torch.randn(2, 2, 600, D, generator=g) * kscale
+    v = torch.randn(2, 2, 600, D, generator=g) * vscale
+    k[1, :, 333:] = 0.0
+    v[1, :, 333:] = 0.0
+    pb = make_problem(w, 1400 + D, lens=[600, 333], q=q, k=k, v=v)
+    res = run_gpu(pb)
+    assert res["status"] == 0
+    assert np.all(np.isfinite(res["out"]))
+    assert_attention_close(pb, res, 0)
+
+
+@pytest.mark.parametrize("D,G,bits,ks,vs", [(256, 32, 4, 1, 0), (64, 64, 2, 0, 0)])
+def test_decode_geometry_blocks_far_below_running_max(D, G, bits, ks, vs):
+    """Later blocks' scores sit 120-400 natural-log units below block 0's
+    (the P' exponent clamp)."""
+    import torch
+    w = _w(D, G, bits, ks, vs, B=1, Hkv=1, Hq=4, L=700)
+    g = torch.Generator().manual_seed(88 + D)
+    q = torch.randn(1, 4, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 1, 700, D, generator=g)
+    v = torch.randn(1, 1, 700, D, generator=g)
+    qsum = q[0].float().sum(0)
+    u = qsum / qsum.norm()
+    gain = float((q[0].float() @ u).min()) / np.sqrt(float(D))
+    for j, sh in enumerate([0.0, -300.0, -150.0, -220.0, -120.0, -400.0]):
+        if sh != 0.0:
+            k[0, 0, 128 * j:128 * (j + 1)] += (sh / gain) * u
+    pb = make_problem(w, 89 + D, lens=[700], q=q, k=k, v=v)
+    res = run_gpu(pb)
+    assert res["status"] == 0
+    assert np.all(np.isfinite(res["out"]))
+    assert_attention_close(pb, res, 0)
+
+
+def test_decode_geometry_repeat_calls_identical():
+    """Same inputs, same launch shape -> the same bits (the kernel reduces in a
+    fixed order; no stale workspace state)."""
+    import torch
+    import bit_quantized_kv_decode_gb300 as kvq
+    w = _w(256, 64, 4, 1, 0, B=2, Hkv=2, Hq=8, L=2048)
+    pb = make_problem(w, 19, lens=[2048, 700])
+    dev = torch.device("cuda")
+    res = run_gpu(pb, num_ctas=7)
+    q, lens = pb.q.to(dev), pb.lens.to(dev)
+    ws = torch.empty(4 << 20, dtype=torch.uint8, device=dev)
+    outs = []
+    for _ in range(3):
+        o, l = kvq.decode_attn(res["desc"], q, res["k_cache"], res["v_cache"], lens, max_blocks=pb.max_blocks,
+                               num_ctas=7, workspace=ws)
+        outs.append((o.clone(), l.clone()))
+    torch.cuda.synchronize()
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    assert np.array_equal(outs[0][0].cpu().double().numpy(), res["out"])
+
+
+def test_decode_geometry_bad_lengths_and_pages_flagged():
+    import torch
+    import bit_quantized_kv_decode_gb300 as kvq
+    w = _w(64, 32, 4, 0, 0, B=2, Hkv=1, Hq=4, L=256, paged=True)
+    pb = make_problem(w, 4, lens=[256, 200])
+    dev = torch.device("cuda")
+    res = run_gpu(pb)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    pt = pb.page_table.to(dev)
+    bad_lens = torch.tensor([256, 999], dtype=torch.int32, device=dev)
+    o, l = kvq.decode_attn(res["desc"], pb.q.to(dev), res["k_cache"], res["v_cache"], bad_lens, pt, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & kvq.DEV_BAD_SEQ_LEN
+    assert np.all(o[1].cpu().numpy() == 0) and np.all(np.isneginf(l[1].cpu().numpy()))
+    st.zero_()
+    pt2 = pt.clone()
+    pt2[0, 1] = 10 ** 6
+    kvq.decode_attn(res["desc"], pb.q.to(dev), res["k_cache"], res["v_cache"], pb.lens.to(dev), pt2, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & kvq.DEV_BAD_PAGE

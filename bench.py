@@ -201,9 +201,9 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
     t_wall1 = time.time()
     if int(status.item()) != 0:
         raise RuntimeError(f"decode reported device status {int(status.item()):#x}")
-    general = w.head_dim != 128 or w.group != 128 or mode == 1  # block-range kernel + log-sum-exp merge kernel
+    general = w.head_dim != 128 or w.group != 128 or mode == 1  # plan, block-range and log-sum-exp merge kernels
     res = dict(ms=ms, per=per, bytes=algorithmic_bytes(w, c["lens_cpu"].tolist()), t0=t_wall0, t1=t_wall1,
-               launches=steps * (2 if general else 1), sets=sets, lens=c["lens_cpu"].tolist())
+               launches=steps * (3 if general else 1), sets=sets, lens=c["lens_cpu"].tolist())
     if e2e:
         # end to end through the public API with host buffers: H2D of this step's
         # query and lengths from pinned memory, decode, D2H of out and lse
@@ -497,7 +497,7 @@ def main():
                              "k_scheme": SCHEME_NAMES[w4.k_scheme], "v_scheme": SCHEME_NAMES[w4.v_scheme],
                              "ms_per_step": ms4, "GB/s": r4["bytes"] / (ms4 / 1e3) / 1e9, "latency_us": ms4 * 1e3,
                              "algorithmic_bytes": r4["bytes"], "l2": l2_note(r4), "operands": args.operands,
-                             "kernel": "kvq::decode_general_kernel + kvq::merge_kernel"})
+                             "kernel": "kvq::decode_general_kernel (+ plan and merge kernels)"})
     clk = clocks.summary(res["t0"], res["t1"])
     clocks.stop()
     if rank != 0:
@@ -520,7 +520,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": ("kvq::decode_kernel" if w.head_dim == 128 and w.group == 128 and mode == 0 else
-                                "kvq::decode_general_kernel + kvq::merge_kernel"),
+                                "kvq::decode_general_kernel (+ plan and merge kernels)"),
                      "traffic": None if mode else profile_traffic(w.name),
                      "algorithmic_bytes_per_launch": res["bytes"],
                      "duration_source": "CUDA events around each kvq_decode_attn call (counter memset + kernel)"},

@@ -1,9 +1,96 @@
 // Launch shape and dispatch of the general-geometry decode kernel
 // (decode_general.cuh); its instances are compiled per head dim, operand
 // type and heads per unit in decode_general_d{64,128,256}[_bf16][_h8].cu.
-#include "decode_general.h"
+#include "decode_general.cuh"
 
 namespace kvq {
+
+namespace {
+
+// The plan of a call, once: one CTA of 1024 threads (a thread per sequence)
+// computes gen_plan and writes the prefix and every decode CTA's assignment.
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) general_plan_kernel(const GenParams p, long long grid, int4* assign,
+                                                                    int* plan_ps) {
+  __shared__ int ps[kGenPlanInts];
+  __shared__ long long red[kPlanThreads / 32];
+  int* lens = ps + p.batch + 1;
+  gen::gen_plan<kPlanThreads>(p.seq_lens, p.batch, p.max_blocks, p.units_per_seq, p.n_target, ps, lens, red);
+  const int tid = threadIdx.x;
+  for (int b = tid; b < p.batch; b += kPlanThreads) {
+    const int len = p.seq_lens[b];
+    if (len < 0 || len > p.max_blocks * kBlockTokens) report(p.dev_status, KVQ_DEV_BAD_SEQ_LEN);
+  }
+  for (int b = tid; b <= p.batch; b += kPlanThreads) plan_ps[b] = ps[b];
+  for (long long c = tid; c < grid; c += kPlanThreads) {
+    int4 a = make_int4(-1, 0, 0, 0);
+    if (c < ps[p.batch]) {
+      const int b = gen::gen_find(ps, p.batch, (int)c);
+      const int nr = (ps[b + 1] - ps[b]) / p.units_per_seq;  // ranges per unit of sequence b
+      const int uh = ((int)c - ps[b]) / nr, split = ((int)c - ps[b]) % nr;
+      const int nblk = (lens[b] + kBlockTokens - 1) / kBlockTokens;
+      a = make_int4(b | (uh << 16), (int)((long long)split * nblk / nr), (int)((long long)(split + 1) * nblk / nr),
+                    lens[b]);
+    }
+    assign[c] = a;
+  }
+}
+
+// Log-sum-exp merge of the general kernel's parts: one warp per (sequence,
+// query head) row; the row's parts are the slots of its unit's ranges, from
+// the plan's prefix.
+constexpr int kMergeThreads = 256;
+
+__global__ void __launch_bounds__(kMergeThreads) general_merge_kernel(const GenParams p, int head_dim, float* out,
+                                                                      float* lse) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
+  if (row >= p.batch * p.num_q_heads) return;
+  const int b = row / p.num_q_heads, head = row % p.num_q_heads;
+  const int uh = head / p.gq, k = head % p.gq;
+  const int p0 = p.plan_ps[b], p1 = p.plan_ps[b + 1];
+  const int nr = (p1 - p0) / p.units_per_seq;  // ranges (parts) of the row's unit
+  const int c0 = p0 + uh * nr;
+  float m = -INFINITY;
+  for (int s = lane; s < nr; s += 32) m = fmaxf(m, p.part_lse[(size_t)(c0 + s) * p.gq + k]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+  float tot = 0.f;
+  for (int s = lane; s < nr; s += 32) tot += expf(p.part_lse[(size_t)(c0 + s) * p.gq + k] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+  const float inv = nr > 0 ? 1.0f / tot : 0.f;
+  float* dst = out + (size_t)row * head_dim;
+  for (int d = lane * 4; d < head_dim; d += 128) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < nr; ++s) {
+      const float w = expf(p.part_lse[(size_t)(c0 + s) * p.gq + k] - m) * inv;
+      const float4 v = *reinterpret_cast<const float4*>(p.part_o + ((size_t)(c0 + s) * p.gq + k) * head_dim + d);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(dst + d) = acc;
+  }
+  if (lane == 0) lse[row] = nr > 0 ? m + logf(tot) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_general_plan(const GenParams& p, long long grid, int4* assign, int* plan_ps, cudaStream_t stream) {
+  general_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, grid, assign, plan_ps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_general_merge(const GenParams& p, int head_dim, float* out, float* lse, cudaStream_t stream) {
+  const int rows = p.batch * p.num_q_heads;
+  if (rows == 0) return cudaSuccess;
+  constexpr int kRows = kMergeThreads / 32;
+  general_merge_kernel<<<(rows + kRows - 1) / kRows, kMergeThreads, 0, stream>>>(p, head_dim, out, lse);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_general_d64(int bits, bool kcw, bool vcw, int group, const GenParams& p, int grid,
                                const GenLaunch& shape, cudaStream_t s);

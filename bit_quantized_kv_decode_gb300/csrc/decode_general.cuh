@@ -140,6 +140,104 @@ __device__ __forceinline__ void convert_row(const unsigned char* blk, int nrows,
   }
 }
 
+// ------------------------------------------------------------------ plan
+// How the batch is cut into CTAs, computed the same way by every CTA of the
+// decode kernel and by the merge kernel from the sequence lengths (device
+// memory), so that ragged batches balance without a host round trip:
+// sequence b (nblk_b blocks per unit) gets S_b = clamp(floor(nblk_b * N / T),
+// 1, nblk_b) block ranges per unit (none when empty), where T is the blocks
+// of all units and N the CTA count the host aims at; ps[b] = sum over b' < b
+// of units * S_b', ps[B] = the CTAs with work (<= N + units of non-empty
+// sequences).  CTA c (ps[b] <= c < ps[b + 1]) takes unit (c - ps[b]) / S_b,
+// range (c - ps[b]) % S_b, and writes its part to slot c.
+__device__ __forceinline__ int gen_ranges(int nblk, long long total, long long n_target) {
+  if (nblk == 0) return 0;
+  const long long s = (long long)nblk * n_target / (total > 0 ? total : 1);
+  return (int)(s < 1 ? 1 : (s > nblk ? nblk : s));
+}
+// The plan of a batch with unequal lengths (lens already in shared memory):
+// one 64-bit division per sequence and a block-wide scan.  Out of line: the
+// common equal-length case keeps the kernel's own code compact.
+template <int NT>
+static __device__ __noinline__ void gen_plan_ragged(int B, int units, long long n_target, int* ps, const int* lens,
+                                                    long long* red, long long t) {
+  constexpr int kWarps = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int per = (B + NT - 1) / NT, b0 = tid * per, b1 = min(B, b0 + per);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(FULL, t, o);
+  if (lane == 0) red[w] = t;
+  __syncthreads();
+  long long total = 0;
+#pragma unroll
+  for (int i = 0; i < kWarps; ++i) total += red[i];
+  total *= units;
+  int cnt = 0;
+  for (int b = b0; b < b1; ++b) {  // this sequence's CTAs, kept in ps[b] until the scan
+    const int c = units * gen_ranges((lens[b] + kBlockTokens - 1) / kBlockTokens, total, n_target);
+    ps[b] = c;
+    cnt += c;
+  }
+  int incl = cnt;  // inclusive warp scan
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(FULL, incl, o);
+    if (lane >= o) incl += v;
+  }
+  __syncthreads();  // red is reused
+  if (lane == 31) red[w] = incl;
+  __syncthreads();
+  int run = incl - cnt;
+  for (int i = 0; i < w; ++i) run += (int)red[i];
+  for (int b = b0; b < b1; ++b) {
+    const int c = ps[b];
+    ps[b] = run;
+    run += c;
+  }
+  if (tid == NT - 1) ps[B] = run;
+}
+
+// NT threads; ps: shared int[B + 1]; lens: shared int[B] (the validated
+// lengths, 0 for a bad one); red: shared long long[NT / 32] scratch.  Each
+// thread reads the lengths of a run of consecutive sequences once.
+template <int NT>
+__device__ __forceinline__ void gen_plan(const int32_t* seq_lens, int B, int max_blocks, int units,
+                                         long long n_target, int* ps, int* lens, long long* red) {
+  const int tid = threadIdx.x;
+  const int per = (B + NT - 1) / NT, b0 = tid * per, b1 = min(B, b0 + per);
+  const int max_len = max_blocks * kBlockTokens;
+  int len0 = seq_lens[0];
+  if (len0 < 0 || len0 > max_len) len0 = 0;
+  long long t = 0;
+  bool same = true;
+  for (int b = b0; b < b1; ++b) {
+    int len = seq_lens[b];
+    if (len < 0 || len > max_len) len = 0;
+    lens[b] = len;
+    same = same && len == len0;
+    t += (len + kBlockTokens - 1) / kBlockTokens;
+  }
+  if (__syncthreads_and(same)) {  // equal lengths: S = min(N / units, nblk) ranges for every unit
+    const int nb = (len0 + kBlockTokens - 1) / kBlockTokens;
+    const long long all = (long long)B * units;
+    const int sq = nb == 0 ? 0 : (int)(n_target / all < 1 ? 1 : (n_target / all > nb ? nb : n_target / all));
+    for (int b = b0; b < b1; ++b) ps[b] = b * units * sq;
+    if (tid == NT - 1) ps[B] = B * units * sq;
+  } else {
+    gen_plan_ragged<NT>(B, units, n_target, ps, lens, red, t);
+  }
+  __syncthreads();
+}
+// Sequence of CTA (or slot) c: the b with ps[b] <= c < ps[b + 1] (c < ps[B]).
+__device__ __forceinline__ int gen_find(const int* ps, int B, int c) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ps[mid] <= c) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // NH: query heads per unit (4, or 8 with every KV block read once); they
 // come in quads of 4 -- one 16-column block (4 heads x 3 E4M3 or 2 BF16
 // parts) per quad of Q', S, P' and O.
@@ -180,44 +278,14 @@ __global__ void __launch_bounds__(kThreads, NH > 4 ? 2 : 4) decode_general_kerne
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-  const int unit = blockIdx.x / p.splits, split = blockIdx.x % p.splits;
-  const int b = unit / p.units_per_seq, uh = unit % p.units_per_seq, kvh = uh >> p.kv_shift;
-  int len = p.seq_lens[b];
-  if (len < 0 || len > p.max_blocks * kBlockTokens) {
-    if (split == 0 && uh == 0 && tid == 0) report(p.dev_status, KVQ_DEV_BAD_SEQ_LEN);
-    len = 0;
-  }
-  const int nblk = (len + kBlockTokens - 1) / kBlockTokens;
-  const int j0 = (int)((long long)split * nblk / p.splits), j1 = (int)((long long)(split + 1) * nblk / p.splits);
+  const int cta = blockIdx.x;
+  const int4 asg = p.assign[cta];  // written by general_plan_kernel: {b | unit << 16, j0, j1, length}
+  if (asg.x < 0) return;           // no work left for this CTA
+  const int b = asg.x & 0xffff, uh = asg.x >> 16, kvh = uh >> p.kv_shift;
+  const int j0 = asg.y, j1 = asg.z, len = asg.w;
   const size_t row0 = (size_t)b * p.num_q_heads + (size_t)uh * p.gq;  // first query head of the unit
-
-  if (j1 <= j0) {  // no block in this range: an empty part (weight 0 in the merge)
-    for (int k = 0; k < p.gq; ++k) {
-      for (int c = tid; c < D; c += kThreads) p.part_o[((row0 + k) * p.splits + split) * D + c] = 0.f;
-      if (tid == 0) p.part_lse[(row0 + k) * p.splits + split] = -INFINITY;
-    }
-    return;
-  }
-
-  if (tid == 0) {
-    for (int i = 0; i < stages + 2; ++i) mbar_init(&bars[i], 1);
-    fence_barrier_init();
-  }
-  for (int i = tid; i < (L.scratch_off - L.q_off) / 16; i += kThreads)
-    reinterpret_cast<uint4*>(qop)[i] = make_uint4(0u, 0u, 0u, 0u);  // unused operand columns stay zero
-  __syncwarp();  // converged for the .sync.aligned allocation
-  if (warp == 0) {
-    tmem_alloc(tbase, (uint32_t)LT.tmem_cols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tbase;
-  const uint32_t t_a = tmem + lane_off + LT.col_a;    // this warp's lanes of the operand region
-  const uint32_t t_so = tmem + lane_off + LT.col_so;  // ... of the S / O region
-  uint64_t* mma_bar = &bars[stages];
-  uint64_t* drain_bar = &bars[stages + 1];
+  float* part_o = p.part_o + (size_t)cta * p.gq * D;  // this CTA's slot: [gq][D] and [gq]
+  float* part_lse = p.part_lse + (size_t)cta * p.gq;
 
   const uint64_t limit = p.wait_limit_ns;
   int pend[4] = {-1, -1, -1, -1};  // thread 0: block whose copy into stage s is in flight
@@ -240,12 +308,30 @@ __global__ void __launch_bounds__(kThreads, NH > 4 ? 2 : 4) decode_general_kerne
     bulk_g2s(sz + 3 * szb, p.v_zero + blk * NSZ, szb, &bars[s]);
     pend[s] = j;
   };
-  if (tid == 0) {
+  if (tid == 0) {  // the first copies go out before the rest of the set-up
+    for (int i = 0; i < stages + 2; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
     for (int i = 0; i < stages && j0 + i < j1; ++i) {
       if (i == 0 && (p.flags & KVQ_FLAG_TEST_STALL) && blockIdx.x == 0) continue;  // test hook: withhold one block
       load(j0 + i, i);
     }
   }
+
+  for (int i = tid; i < (L.scratch_off - L.q_off) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(qop)[i] = make_uint4(0u, 0u, 0u, 0u);  // unused operand columns stay zero
+  __syncwarp();  // converged for the .sync.aligned allocation
+  if (warp == 0) {
+    tmem_alloc(tbase, (uint32_t)LT.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tbase;
+  const uint32_t t_a = tmem + lane_off + LT.col_a;    // this warp's lanes of the operand region
+  const uint32_t t_so = tmem + lane_off + LT.col_so;  // ... of the S / O region
+  uint64_t* mma_bar = &bars[stages];
+  uint64_t* drain_bar = &bars[stages + 1];
 
   // ---- per-unit query statistics (all NH head slots; empty slots are 0)
   const uint16_t* qb = p.q + row0 * D;
@@ -666,13 +752,13 @@ __global__ void __launch_bounds__(kThreads, NH > 4 ? 2 : 4) decode_general_kerne
       if (c < D) {
 #pragma unroll
         for (int k = 0; k < NH; ++k)
-          if (k < p.gq) p.part_o[((row0 + k) * p.splits + split) * D + c] = (oacc[hf][k] + zacc[hf][k]) / l_run[k];
+          if (k < p.gq) part_o[k * D + c] = (oacc[hf][k] + zacc[hf][k]) / l_run[k];
       }
     }
 #pragma unroll
     for (int k = 0; k < NH; ++k)
       if (tid == k && k < p.gq)
-        p.part_lse[(row0 + k) * p.splits + split] = (m_run[k] + __log2f(l_run[k])) * 0.69314718055994530942f;
+        part_lse[k] = (m_run[k] + __log2f(l_run[k])) * 0.69314718055994530942f;
   } else if (tid == 0) {
     report(p.dev_status, KVQ_DEV_TIMEOUT);
   }

@@ -17,12 +17,14 @@ struct GenParams {
   const uint16_t* v_zero;
   const int32_t* seq_lens;
   const int32_t* page_table;
-  float* part_o;    // [B * Hq][splits][D]: each range's output, normalised over the range
-  float* part_lse;  // [B * Hq][splits]: its log-sum-exp (natural log; -inf for an empty range)
+  float* part_o;    // [slots][gq][D]: each range's output, normalised over the range (slot = CTA)
+  float* part_lse;  // [slots][gq]: its log-sum-exp (natural log)
   uint32_t* dev_status;
   int batch, num_kv_heads, num_q_heads, max_blocks, num_pages;
   int gq, units_per_seq, kv_shift;  // units of work, as in DecodeParams
-  int splits;                       // block ranges per unit (grid = units * splits)
+  long long n_target;               // CTAs the plan aims at (see gen_plan in decode_general.cuh)
+  const int4* assign;               // [grid]: per CTA {b | unit << 16, j0, j1, length}; x < 0: no work
+  const int* plan_ps;               // [B + 1]: the plan's prefix (CTAs of sequences before b)
   float sm_scale_log2;
   uint32_t flags;
   uint64_t wait_limit_ns;
@@ -43,7 +45,8 @@ struct GenLayout {
   bool seq_halves;  // PV one channel half at a time
 };
 
-constexpr int kGenScratchBytes = 2304;  // reduction buffers, per-group values, barriers (2,168 used)
+constexpr int kGenPlanInts = 2 * 1024 + 4;  // the plan kernel's prefix (B + 1) and lengths (B) ints
+constexpr int kGenScratchBytes = 2304;       // reduction buffers, per-group values and barriers (2,168 used)
 
 __host__ __device__ constexpr int gen_pow2_cols(int used) {
   return used <= 32 ? 32 : used <= 64 ? 64 : used <= 128 ? 128 : used <= 256 ? 256 : 512;
@@ -82,5 +85,10 @@ GenLaunch general_launch_shape(int bits, int k_scheme, int v_scheme, int head_di
 
 cudaError_t launch_decode_general(int bits, int k_scheme, int v_scheme, int head_dim, int group, bool bf16, int nh,
                                   const GenParams& p, int grid, const GenLaunch& shape, cudaStream_t stream);
+// The plan of a call (gen_plan): prefix and per-CTA assignments into the
+// workspace (p.plan_ps, p.assign), one CTA; launched before the decode kernel.
+cudaError_t launch_general_plan(const GenParams& p, long long grid, int4* assign, int* plan_ps, cudaStream_t stream);
+// The log-sum-exp merge of the parts into out [B][Hq][head_dim] and lse [B][Hq].
+cudaError_t launch_general_merge(const GenParams& p, int head_dim, float* out, float* lse, cudaStream_t stream);
 
 }  // namespace kvq

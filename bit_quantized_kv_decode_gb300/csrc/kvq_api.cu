@@ -110,20 +110,25 @@ kvq_status check_attn(const kvq_attn_desc* d) {
     return KVQ_ERR_UNSUPPORTED;  // the E2M1 placement is built for head dim 128, groups of 128
   if (!(std::isfinite(d->sm_scale))) return KVQ_ERR_INVALID_ARG;
   if ((long long)d->batch * units_per_seq(d) * d->max_blocks > (1LL << 30)) return KVQ_ERR_UNSUPPORTED;
+  if (units_per_seq(d) >= (1 << 15)) return KVQ_ERR_UNSUPPORTED;  // the general kernel's CTA assignment packs the unit
   return KVQ_OK;
 }
 
-// General geometry: block ranges per (sequence, unit) and the launch shape.
-// With num_ctas = 0 the number of ranges per unit is chosen between one and
-// eight waves of resident CTAs so that the grid fills its last wave best
-// (fewest idle CTA slots), then the fewest ranges; with num_ctas > 0 it is
-// ceil(num_ctas / units).  At most max_blocks ranges per unit.
+// General geometry: the CTA count the device-side plan aims at (gen_plan in
+// decode_general.cuh cuts each sequence's units into ranges in proportion
+// to its length), the launch shape and the workspace.  The target is
+// units * S: with num_ctas = 0, S is chosen between one and eight waves of
+// resident CTAs so that a batch of equal lengths fills its last wave best
+// (fewest idle CTA slots), then the fewest ranges; with num_ctas > 0,
+// S = ceil(num_ctas / units).  At most max_blocks ranges per unit.
 struct GeneralPlan {
   GenLaunch launch;
   int nh;            // query heads per unit: 8 (each KV block read once) or 4
   int units;         // units per sequence
-  int splits;
-  size_t part_lse, part_o, total;  // workspace offsets and size
+  int gq;            // query heads a unit holds
+  long long n_target;
+  long long slots;   // grid = part slots: n_target + every unit (one range each at least)
+  size_t plan_ps, assign, part_lse, part_o, total;  // workspace offsets and size
 };
 
 kvq_status general_plan(const kvq_attn_desc* d, GeneralPlan* plan) {
@@ -161,11 +166,15 @@ kvq_status general_plan(const kvq_attn_desc* d, GeneralPlan* plan) {
   }
   if (splits > d->max_blocks) splits = d->max_blocks;
   if (splits < 1) splits = 1;
-  plan->splits = (int)splits;
-  const size_t rows = (size_t)d->batch * d->num_q_heads;
-  plan->part_lse = 0;
-  plan->part_o = round_up(rows * splits * sizeof(float), 256);
-  plan->total = plan->part_o + round_up(rows * splits * d->cache.head_dim * sizeof(float), 256);
+  const int g = heads_per_kv(d);
+  plan->gq = plan->nh == 8 ? 8 : (g < kGroupQ ? g : kGroupQ);
+  plan->n_target = units * splits;
+  plan->slots = plan->n_target + units;
+  plan->plan_ps = 0;
+  plan->assign = round_up((size_t)(d->batch + 1) * sizeof(int), 256);
+  plan->part_lse = plan->assign + round_up((size_t)plan->slots * 4 * sizeof(int), 256);
+  plan->part_o = plan->part_lse + round_up((size_t)plan->slots * plan->gq * sizeof(float), 256);
+  plan->total = plan->part_o + round_up((size_t)plan->slots * plan->gq * d->cache.head_dim * sizeof(float), 256);
   return KVQ_OK;
 }
 
@@ -195,25 +204,28 @@ kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const ui
   p.seq_lens = seq_lens; p.page_table = page_table; p.dev_status = dev_status;
   p.part_lse = reinterpret_cast<float*>(ws + plan.part_lse);
   p.part_o = reinterpret_cast<float*>(ws + plan.part_o);
+  p.assign = reinterpret_cast<const int4*>(ws + plan.assign);
+  p.plan_ps = reinterpret_cast<const int*>(ws + plan.plan_ps);
   p.batch = desc->batch; p.num_kv_heads = desc->cache.num_kv_heads; p.num_q_heads = desc->num_q_heads;
   p.max_blocks = desc->max_blocks; p.num_pages = desc->cache.num_pages;
-  const int g = heads_per_kv(desc);
-  p.gq = plan.nh == 8 ? 8 : (g < kGroupQ ? g : kGroupQ);
+  p.gq = plan.gq;
   p.units_per_seq = plan.units;
   p.kv_shift = 0;  // a unit is one KV head (up to 8 query heads)
-  p.splits = plan.splits;
+  p.n_target = plan.n_target;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.flags = desc->flags;
   p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
   p.nibble_mul = 1u << 28;
   p.minus_one = 0xffffffffu;
-  const int grid = desc->batch * p.units_per_seq * plan.splits;
-  cudaError_t e = launch_decode_general(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme,
+  const int grid = (int)plan.slots;
+  cudaError_t e = launch_general_plan(p, plan.slots, reinterpret_cast<int4*>(ws + plan.assign),
+                                      reinterpret_cast<int*>(ws + plan.plan_ps), st);
+  if (e != cudaSuccess) return KVQ_ERR_CUDA;
+  e = launch_decode_general(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme,
                                         desc->cache.head_dim, group_of(&desc->cache),
                                         desc->operand_mode == KVQ_OPERANDS_BF16, plan.nh, p, grid, plan.launch, st);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
-  e = launch_merge(p.part_o, p.part_lse, desc->batch * desc->num_q_heads, plan.splits, desc->cache.head_dim, out, lse,
-                   st);
+  e = launch_general_merge(p, desc->cache.head_dim, out, lse, st);
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

@@ -109,25 +109,37 @@ def test_e2m1_flag_validation(lib):
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
 
 
+def _general_ws(batch, units, splits, gq, head_dim):
+    """Workspace of the general kernel, each part 256-byte aligned: the plan's
+    prefix (batch + 1 ints), one 16-byte assignment per CTA, and one part slot
+    per CTA holding gq heads' lse and outputs; CTAs = the plan's target
+    (units x ranges) plus one per unit."""
+    r256 = lambda x: (x + 255) // 256 * 256
+    slots = units * splits + units
+    return r256((batch + 1) * 4) + r256(slots * 16) + r256(slots * gq * 4) + r256(slots * gq * head_dim * 4)
+
+
 def test_general_geometry_workspace_host_only(lib):
-    """Head dims 64 / 256 and groups of 32 / 64 take the block-range kernel:
-    its workspace holds one partial output and log-sum-exp per query head
-    and range, ranges = ceil(num_ctas / units) capped at max_blocks; both
-    operand modes; not the E2M1 V placement."""
+    """Head dims 64 / 256 and groups of 32 / 64 take the block-range kernel;
+    its target is ranges = ceil(num_ctas / units) per unit, capped at
+    max_blocks; both operand modes; not the E2M1 V placement."""
     n = ctypes.c_size_t()
     d = _lib.AttnDesc(_cache(4, 1, 0, hd=256, group=64, pages=16 * 64), 16, 32, 64, 0, 0.0, 304, 0)
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
-    rows, splits = 16 * 32, 3  # 128 units (16 sequences x 8 KV heads), 304 CTAs wanted
-    assert n.value == rows * splits * 4 + rows * splits * 256 * 4
+    assert n.value == _general_ws(16, 16 * 8, 3, 4, 256)  # 128 units, 304 CTAs wanted -> 3 ranges
     d = _lib.AttnDesc(_cache(2, 0, 1, hd=64, group=32, pages=16 * 64), 2, 16, 2, 0, 0.0, 100000, 0)
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
-    assert n.value == 256 + 2 * 16 * 2 * 64 * 4  # two ranges at most (max_blocks = 2)
+    assert n.value == _general_ws(2, 2 * 8, 2, 2, 64)  # two ranges at most (max_blocks = 2); 2 heads per unit
     bf16 = _lib.AttnDesc(_cache(2, 1, 0, hd=128, group=32), 8, 32, 32, 1, 0.0, 304, 0)
     assert lib.kvq_decode_workspace_size(ctypes.byref(bf16), ctypes.byref(n)) == 0
     # the BF16-operand mode takes the block-range kernel on every geometry
     bf16 = _lib.AttnDesc(_cache(4, 1, 0, pages=16 * 64), 16, 32, 64, 1, 0.0, 304, 0)
     assert lib.kvq_decode_workspace_size(ctypes.byref(bf16), ctypes.byref(n)) == 0
-    assert n.value == rows * splits * 4 + rows * splits * 128 * 4
+    assert n.value == _general_ws(16, 16 * 8, 3, 4, 128)
+    # 8 query heads per KV head: one 8-head unit per KV head
+    h8 = _lib.AttnDesc(_cache(4, 1, 0, hd=64, group=64, pages=16 * 64), 16, 64, 64, 0, 0.0, 304, 0)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(h8), ctypes.byref(n)) == 0
+    assert n.value == _general_ws(16, 16 * 8, 3, 8, 64)
     bad = _lib.AttnDesc(_cache(2, 1, 0, hd=128, group=32), 8, 32, 32, 0, 0.0, 304, _lib.FLAG_E2M1_V)
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
 

@@ -212,10 +212,11 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* 
  * smaller than the head dim, token-wise K and V fold per G-channel group.
  * Head dim 128 with groups of 128: work is split over persistent CTAs in
  * equal tile ranges; a sequence/head cut between CTAs is merged on the device
- * by log-sum-exp.  Other geometries (head dim 64 / 256, groups of 32 / 64):
- * a second kernel walks equal ranges of each (sequence, unit)'s blocks and a
- * log-sum-exp merge kernel combines the ranges (two launches); both operand
- * modes, not KVQ_FLAG_E2M1_V (KVQ_ERR_UNSUPPORTED).  Query heads
+ * by log-sum-exp.  Other geometries (head dim 64 / 256, groups of 32 / 64)
+ * and the BF16 mode: three launches -- a one-CTA plan cuts each (sequence,
+ * unit)'s blocks into ranges in proportion to the sequence's length, a
+ * second kernel decodes one range per CTA, and a log-sum-exp merge combines
+ * the ranges; not KVQ_FLAG_E2M1_V (KVQ_ERR_UNSUPPORTED).  Query heads
  * per KV head: 1, 2, 4 or 8 (a work unit takes up to 4 query heads of one KV
  * head, so with 8 each KV block is read twice).  sm_scale <= 0 means
  * 1 / sqrt(head_dim).
@@ -247,8 +248,9 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
  * loads the library until the process exits.  Returns KVQ_ERR_WORKSPACE when
  * a call needs more scratch than kvq_decode_workspace_size reports (head dim
  * 128, groups of 128: batch * num_kv_heads * 4 bytes of counters, twice that
- * with 8 query heads per KV head, plus 4 KiB per CTA; other geometries: one
- * head_dim + 1 floats per query head and block range);
+ * with 8 query heads per KV head, plus 4 KiB per CTA; other geometries and
+ * the BF16 mode: the plan (4 bytes per sequence, 16 per CTA) and head_dim + 1
+ * floats per query head and block range);
  * kvq_decode_attn with a caller workspace then
  * remains available.  Every call on a stream that is not being captured
  * looks up the array's address on the current device (the first such call

@@ -175,6 +175,13 @@ def rotation_sets(w, seed) -> int:
     return 1 if per_step > L2_BYTES else max(8, -(-2 * L2_BYTES // per_step))
 
 
+KERNEL_SPECIALISED = "kvq::decode_kernel"
+KERNEL_GENERAL = "kvq::decode_general_kernel (+ plan and merge kernels)"
+SPLIT_SPECIALISED = "persistent CTAs cut the tile order into equal ranges; cut units are merged in the kernel"
+SPLIT_GENERAL = ("a one-CTA plan cuts each unit's blocks into ranges in proportion to its sequence's length; "
+                 "one range per CTA; a log-sum-exp merge kernel combines the ranges")
+
+
 def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=True, mode=0, sets=None, flags=0):
     import bit_quantized_kv_decode_gb300 as kvq
     sets = rotation_sets(w, seed) if sets is None else sets
@@ -201,9 +208,10 @@ def measure_kvq(w, seed, steps, warmup, dev, k_scheme=None, v_scheme=None, e2e=T
     t_wall1 = time.time()
     if int(status.item()) != 0:
         raise RuntimeError(f"decode reported device status {int(status.item()):#x}")
-    general = w.head_dim != 128 or w.group != 128 or mode == 1  # plan, block-range and log-sum-exp merge kernels
+    general = kvq.decode_path(ad) == kvq._lib.PATH_GENERAL  # plan, block-range and log-sum-exp merge kernels
     res = dict(ms=ms, per=per, bytes=algorithmic_bytes(w, c["lens_cpu"].tolist()), t0=t_wall0, t1=t_wall1,
-               launches=steps * (3 if general else 1), sets=sets, lens=c["lens_cpu"].tolist())
+               launches=steps * (3 if general else 1), sets=sets, lens=c["lens_cpu"].tolist(), general=general,
+               kernel=KERNEL_GENERAL if general else KERNEL_SPECIALISED)
     if e2e:
         # end to end through the public API with host buffers: H2D of this step's
         # query and lengths from pinned memory, decode, D2H of out and lse
@@ -461,7 +469,7 @@ def main():
             ms2 = max_over_ranks(r2["ms"], world, dev)
             extra.append({"workload": w2.name, "k_scheme": SCHEME_NAMES[ks], "v_scheme": SCHEME_NAMES[vs],
                           "ms_per_step": ms2, "GB/s": r2["bytes"] / (ms2 / 1e3) / 1e9,
-                          "latency_us": ms2 * 1e3})
+                          "latency_us": ms2 * 1e3, "kernel": r2["kernel"]})
     e2m1 = []  # the 2-bit sweep again with the V codes placed as E2M1 in shared memory
     if not args.no_extra and w.name == DEFAULT_WORKLOAD and mode == 0:
         w2 = synth.WORKLOADS["b128_l32k_int2"]
@@ -470,7 +478,7 @@ def main():
             ms2 = max_over_ranks(r2["ms"], world, dev)
             e2m1.append({"workload": w2.name, "k_scheme": SCHEME_NAMES[ks], "v_scheme": SCHEME_NAMES[vs],
                          "v_operand": "E2M1 (code / 2) in shared memory", "ms_per_step": ms2,
-                         "GB/s": r2["bytes"] / (ms2 / 1e3) / 1e9, "latency_us": ms2 * 1e3})
+                         "GB/s": r2["bytes"] / (ms2 / 1e3) / 1e9, "latency_us": ms2 * 1e3, "kernel": r2["kernel"]})
     configs = []
     if not args.no_extra and w.name == DEFAULT_WORKLOAD:
         for name in ("b8_l4k_int2", "paged_ragged_int2"):
@@ -485,8 +493,8 @@ def main():
                             "seq_lens": (f"{len(lens3)} sequences, min {min(lens3)}, max {max(lens3)}, "
                                          f"mean {sum(lens3) / len(lens3):.0f} tokens" if w3.ragged else
                                          f"{len(lens3)} x {lens3[0]} tokens"),
-                            "paged": w3.paged, "split_kv": "persistent CTAs cut the tile order into equal "
-                                                          "ranges; cut units are merged in the kernel"})
+                            "paged": w3.paged, "kernel": r3["kernel"],
+                            "split_kv": SPLIT_GENERAL if r3["general"] else SPLIT_SPECIALISED})
     geometry = []  # head dims 64 / 256 and groups of 32 / 64: the general-geometry kernel
     if not args.no_extra and w.name == DEFAULT_WORKLOAD:
         for name in ("b32_l32k_d256_g64_int4", "b32_l32k_d128_g32_int2", "b32_l32k_d64_g32_int2"):
@@ -497,7 +505,7 @@ def main():
                              "k_scheme": SCHEME_NAMES[w4.k_scheme], "v_scheme": SCHEME_NAMES[w4.v_scheme],
                              "ms_per_step": ms4, "GB/s": r4["bytes"] / (ms4 / 1e3) / 1e9, "latency_us": ms4 * 1e3,
                              "algorithmic_bytes": r4["bytes"], "l2": l2_note(r4), "operands": args.operands,
-                             "kernel": "kvq::decode_general_kernel (+ plan and merge kernels)"})
+                             "kernel": r4["kernel"]})
     clk = clocks.summary(res["t0"], res["t1"])
     clocks.stop()
     if rank != 0:
@@ -519,11 +527,12 @@ def main():
                        **({"operands": "bf16 (exact BF16 codes, 2-part BF16 Q'/P')"} if mode else {})),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": ("kvq::decode_kernel" if w.head_dim == 128 and w.group == 128 and mode == 0 else
-                                "kvq::decode_general_kernel (+ plan and merge kernels)"),
-                     "traffic": None if mode else profile_traffic(w.name),
+                     "kernel": res["kernel"],
+                     "traffic": None if res["general"] else profile_traffic(w.name),
                      "algorithmic_bytes_per_launch": res["bytes"],
-                     "duration_source": "CUDA events around each kvq_decode_attn call (counter memset + kernel)"},
+                     "duration_source": ("CUDA events around each kvq_decode_attn call (plan, decode and merge "
+                                         "kernels)" if res["general"] else
+                                         "CUDA events around each kvq_decode_attn call (counter memset + kernel)")},
         "e2e": ({"value": total_bytes / (e2e_ms / 1e3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
                  "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]} if "e2e_ms" in res else None),
         "gpu_launches": res["launches"],

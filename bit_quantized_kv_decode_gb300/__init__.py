@@ -172,6 +172,14 @@ def workspace_size(desc: AttnDesc) -> int:
     return n.value
 
 
+def decode_path(desc: AttnDesc) -> int:
+    """The decode kernel a call with this descriptor runs: _lib.PATH_SPECIALISED
+    or _lib.PATH_GENERAL (kvq_decode_path)."""
+    n = ctypes.c_int32()
+    _lib.check(library().kvq_decode_path(ctypes.byref(desc), ctypes.byref(n)), "kvq_decode_path")
+    return n.value
+
+
 def decode_attn(desc: CacheDesc, q: torch.Tensor, k_cache, v_cache, seq_lens: torch.Tensor,
                 page_table: Optional[torch.Tensor] = None, max_blocks: Optional[int] = None,
                 mode: int = OPERANDS_FP8, sm_scale: float = 0.0, num_ctas: int = 0,

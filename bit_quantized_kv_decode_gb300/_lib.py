@@ -21,10 +21,12 @@ OPERANDS_FP8 = 0
 OPERANDS_BF16 = 1
 FLAG_TEST_STALL = 0x1
 FLAG_E2M1_V = 0x2
+PATH_SPECIALISED = 0
+PATH_GENERAL = 1
 
 # Every symbol include/kvq.h declares.
 EXPORTS = ("kvq_status_string", "kvq_version", "kvq_cache_bytes", "kvq_pack", "kvq_append", "kvq_dequant",
-           "kvq_decode_workspace_size", "kvq_decode_attn", "kvq_decode_attn_static", "kvq_merge")
+           "kvq_decode_workspace_size", "kvq_decode_path", "kvq_decode_attn", "kvq_decode_attn_static", "kvq_merge")
 
 
 class CacheDesc(ctypes.Structure):
@@ -77,6 +79,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.kvq_dequant.argtypes = [ctypes.POINTER(CacheDesc), I32, P, P, P, I32, I32, P, P, I32, P, P, P]
     lib.kvq_decode_workspace_size.restype = I32
     lib.kvq_decode_workspace_size.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(SZ)]
+    lib.kvq_decode_path.restype = I32
+    lib.kvq_decode_path.argtypes = [ctypes.POINTER(AttnDesc), ctypes.POINTER(I32)]
     lib.kvq_decode_attn.restype = I32
     lib.kvq_decode_attn.argtypes = [ctypes.POINTER(AttnDesc), P, P, P, P, P, P, P, P, P, P, P, P, SZ, P, P]
     lib.kvq_decode_attn_static.restype = I32

@@ -16,7 +16,8 @@ __global__ void __launch_bounds__(kPlanThreads) general_plan_kernel(const GenPar
   __shared__ int ps[kGenPlanInts];
   __shared__ long long red[kPlanThreads / 32];
   int* lens = ps + p.batch + 1;
-  gen::gen_plan<kPlanThreads>(p.seq_lens, p.batch, p.max_blocks, p.units_per_seq, p.n_target, ps, lens, red);
+  gen::gen_plan<kPlanThreads>(p.seq_lens, p.batch, p.max_blocks, p.units_per_seq, p.n_target, p.n_floor, ps, lens,
+                              red);
   const int tid = threadIdx.x;
   for (int b = tid; b < p.batch; b += kPlanThreads) {
     const int len = p.seq_lens[b];
@@ -120,10 +121,8 @@ cudaError_t launch_general_d256_bf16_h8(int bits, bool kcw, bool vcw, int group,
 GenLaunch general_launch_shape(int bits, int k_scheme, int v_scheme, int head_dim, int group, bool bf16, int nh,
                                int smem_per_sm, int smem_reserved_per_cta) {
   const bool kcw = k_scheme == KVQ_CHANNELWISE, vcw = v_scheme == KVQ_CHANNELWISE;
-  const int tmem_cols = gen_layout(bits, head_dim, group, kcw, vcw, bf16, nh, 2).tmem_cols;
   GenLaunch r;
-  r.ctas_per_sm = 512 / tmem_cols < 4 ? 512 / tmem_cols : 4;
-  if (nh > 4 && r.ctas_per_sm > 2) r.ctas_per_sm = 2;  // the 8-head instances take up to 255 registers
+  r.ctas_per_sm = gen_ctas_per_sm(bits, head_dim, group, kcw, vcw, bf16, nh);
   auto fits = [&](int ctas, int stages) {
     const long long need =
         gen_layout(bits, head_dim, group, kcw, vcw, bf16, nh, stages).total_bytes + smem_reserved_per_cta;

@@ -141,15 +141,22 @@ __device__ __forceinline__ void convert_row(const unsigned char* blk, int nrows,
 }
 
 // ------------------------------------------------------------------ plan
-// How the batch is cut into CTAs, computed the same way by every CTA of the
-// decode kernel and by the merge kernel from the sequence lengths (device
-// memory), so that ragged batches balance without a host round trip:
-// sequence b (nblk_b blocks per unit) gets S_b = clamp(floor(nblk_b * N / T),
-// 1, nblk_b) block ranges per unit (none when empty), where T is the blocks
-// of all units and N the CTA count the host aims at; ps[b] = sum over b' < b
-// of units * S_b', ps[B] = the CTAs with work (<= N + units of non-empty
-// sequences).  CTA c (ps[b] <= c < ps[b + 1]) takes unit (c - ps[b]) / S_b,
-// range (c - ps[b]) % S_b, and writes its part to slot c.
+// How the batch is cut into CTAs, computed once per call on the device (the
+// plan kernel) from the sequence lengths, so that ragged batches balance
+// without a host round trip.  With T the blocks of all units, the CTA count
+// aimed at is N = min(N_host, max(R, T / kGenRangeBlocks)): the host's count
+// (whole waves for max_blocks per unit), lowered when the actual lengths hold
+// less work -- to ranges of about kGenRangeBlocks blocks, but never below one
+// wave of resident CTAs R.  Sequence b (nblk_b blocks per unit) gets S_b =
+// clamp(floor(nblk_b * N / T), 1, nblk_b) block ranges per unit (none when
+// empty); ps[b] = sum over b' < b of units * S_b', ps[B] = the CTAs with work
+// (<= N + units of non-empty sequences).  CTA c (ps[b] <= c < ps[b + 1])
+// takes unit (c - ps[b]) / S_b, range (c - ps[b]) % S_b, and writes its part
+// to slot c.
+__device__ __forceinline__ long long gen_aim(long long total, long long n_host, long long n_floor) {
+  const long long want = total / kGenRangeBlocks > n_floor ? total / kGenRangeBlocks : n_floor;
+  return want < n_host ? want : n_host;
+}
 __device__ __forceinline__ int gen_ranges(int nblk, long long total, long long n_target) {
   if (nblk == 0) return 0;
   const long long s = (long long)nblk * n_target / (total > 0 ? total : 1);
@@ -159,8 +166,8 @@ __device__ __forceinline__ int gen_ranges(int nblk, long long total, long long n
 // one 64-bit division per sequence and a block-wide scan.  Out of line: the
 // common equal-length case keeps the kernel's own code compact.
 template <int NT>
-static __device__ __noinline__ void gen_plan_ragged(int B, int units, long long n_target, int* ps, const int* lens,
-                                                    long long* red, long long t) {
+static __device__ __noinline__ void gen_plan_ragged(int B, int units, long long n_target, long long n_floor, int* ps,
+                                                    const int* lens, long long* red, long long t) {
   constexpr int kWarps = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int per = (B + NT - 1) / NT, b0 = tid * per, b1 = min(B, b0 + per);
@@ -172,6 +179,7 @@ static __device__ __noinline__ void gen_plan_ragged(int B, int units, long long 
 #pragma unroll
   for (int i = 0; i < kWarps; ++i) total += red[i];
   total *= units;
+  n_target = gen_aim(total, n_target, n_floor);
   int cnt = 0;
   for (int b = b0; b < b1; ++b) {  // this sequence's CTAs, kept in ps[b] until the scan
     const int c = units * gen_ranges((lens[b] + kBlockTokens - 1) / kBlockTokens, total, n_target);
@@ -202,7 +210,7 @@ static __device__ __noinline__ void gen_plan_ragged(int B, int units, long long 
 // thread reads the lengths of a run of consecutive sequences once.
 template <int NT>
 __device__ __forceinline__ void gen_plan(const int32_t* seq_lens, int B, int max_blocks, int units,
-                                         long long n_target, int* ps, int* lens, long long* red) {
+                                         long long n_target, long long n_floor, int* ps, int* lens, long long* red) {
   const int tid = threadIdx.x;
   const int per = (B + NT - 1) / NT, b0 = tid * per, b1 = min(B, b0 + per);
   const int max_len = max_blocks * kBlockTokens;
@@ -220,11 +228,12 @@ __device__ __forceinline__ void gen_plan(const int32_t* seq_lens, int B, int max
   if (__syncthreads_and(same)) {  // equal lengths: S = min(N / units, nblk) ranges for every unit
     const int nb = (len0 + kBlockTokens - 1) / kBlockTokens;
     const long long all = (long long)B * units;
+    n_target = gen_aim(all * nb, n_target, n_floor);
     const int sq = nb == 0 ? 0 : (int)(n_target / all < 1 ? 1 : (n_target / all > nb ? nb : n_target / all));
     for (int b = b0; b < b1; ++b) ps[b] = b * units * sq;
     if (tid == NT - 1) ps[B] = B * units * sq;
   } else {
-    gen_plan_ragged<NT>(B, units, n_target, ps, lens, red, t);
+    gen_plan_ragged<NT>(B, units, n_target, n_floor, ps, lens, red, t);
   }
   __syncthreads();
 }
@@ -242,7 +251,8 @@ __device__ __forceinline__ int gen_find(const int* ps, int B, int c) {
 // come in quads of 4 -- one 16-column block (4 heads x 3 E4M3 or 2 BF16
 // parts) per quad of Q', S, P' and O.
 template <int BITS, bool KCW, bool VCW, int D, int G, bool BF16, int NH>
-__global__ void __launch_bounds__(kThreads, NH > 4 ? 2 : 4) decode_general_kernel(const GenParams p, int stages) {
+__global__ void __launch_bounds__(kThreads, gen_min_ctas(BITS, D, G, KCW, VCW, BF16, NH))
+decode_general_kernel(const GenParams p, int stages) {
   constexpr int kKBytes = kBlockTokens * D * BITS / 8;  // K (and V) codes of a block
   constexpr int kElems = BF16 ? 16 : 32;                // contraction elements per MMA
   constexpr int kCm = BF16 ? 256 : 128;                 // bytes of one B block per 8 rows

@@ -22,7 +22,8 @@ struct GenParams {
   uint32_t* dev_status;
   int batch, num_kv_heads, num_q_heads, max_blocks, num_pages;
   int gq, units_per_seq, kv_shift;  // units of work, as in DecodeParams
-  long long n_target;               // CTAs the plan aims at (see gen_plan in decode_general.cuh)
+  long long n_target;               // CTAs the plan aims at for max_blocks per unit (see gen_plan in decode_general.cuh)
+  long long n_floor;                // ... and at least, when the lengths hold less work: one wave of resident CTAs
   const int4* assign;               // [grid]: per CTA {b | unit << 16, j0, j1, length}; x < 0: no work
   const int* plan_ps;               // [B + 1]: the plan's prefix (CTAs of sequences before b)
   float sm_scale_log2;
@@ -46,6 +47,7 @@ struct GenLayout {
 };
 
 constexpr int kGenPlanInts = 2 * 1024 + 4;  // the plan kernel's prefix (B + 1) and lengths (B) ints
+constexpr int kGenRangeBlocks = 20;         // blocks per range the plan aims at when the lengths are short of max_blocks
 constexpr int kGenScratchBytes = 2304;       // reduction buffers, per-group values and barriers (2,168 used)
 
 __host__ __device__ constexpr int gen_pow2_cols(int used) {
@@ -70,6 +72,27 @@ __host__ __device__ constexpr GenLayout gen_layout(int bits, int D, int G, bool 
   const int scratch_off = p_off + kBlockTokens * 16 * w * (vcw ? 1 : ngc) * hh;  // P': 128 rows x (block per channel group, quad)
   return GenLayout{nsz, stage_bytes, stages, q_off, p_off, scratch_off, scratch_off + kGenScratchBytes, 0, a_cols,
                    gen_pow2_cols(a_cols + (s_cols > o_cols ? s_cols : o_cols)), seq};
+}
+
+// Resident CTAs per SM of an instance: as many as tensor memory (512
+// columns per SM) and shared memory (228 KB per SM, 1 KB of it reserved per
+// CTA, with a 2-stage copy ring) hold, up to a cap.  More CTAs hide more of
+// each CTA's serial chain (copy wait, conversion, QK^T, softmax, PV); the
+// caps are where more stopped paying (measured: 4-head units up to 8, 8-head
+// units 4 with 4-bit and 5 with 2-bit codes, whose registers -- up to 168 per
+// thread -- spill below 96).  The kernel's launch bounds take the same count
+// (never below 4 for 4-head units), so its registers always fit.
+constexpr int kGenSmemPerSm = 228 * 1024, kGenSmemPerCta = 1024;
+__host__ __device__ constexpr int gen_ctas_per_sm(int bits, int D, int G, bool kcw, bool vcw, bool bf16, int nh) {
+  const int t = 512 / gen_layout(bits, D, G, kcw, vcw, bf16, nh, 2).tmem_cols;
+  const int m = kGenSmemPerSm / (gen_layout(bits, D, G, kcw, vcw, bf16, nh, 2).total_bytes + kGenSmemPerCta);
+  const int cap = nh > 4 ? (bits == 4 ? 4 : 5) : 8;
+  const int c = t < m ? t : m;
+  return c < cap ? c : cap;
+}
+__host__ __device__ constexpr int gen_min_ctas(int bits, int D, int G, bool kcw, bool vcw, bool bf16, int nh) {
+  const int c = gen_ctas_per_sm(bits, D, G, kcw, vcw, bf16, nh);
+  return nh > 4 ? c : (c > 4 ? c : 4);
 }
 
 struct GenLaunch {

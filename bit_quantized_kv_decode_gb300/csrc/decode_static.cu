@@ -27,7 +27,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "kvq_internal.h"
+#include "kvq_entry.h"
 
 namespace kvq {
 namespace {
@@ -72,7 +72,7 @@ extern "C" KVQ_API kvq_status kvq_decode_attn_static(const kvq_attn_desc* desc, 
                                                      const int32_t* seq_lens, const int32_t* page_table, float* out,
                                                      float* lse, uint32_t* dev_status, void* stream) {
   size_t need = 0;
-  kvq_status s = kvq_decode_workspace_size(desc, &need);
+  kvq_status s = kvq::decode_workspace_bounded(desc, kvq::kKvqStaticScratchBytes, &need);
   if (s != KVQ_OK) return s;
   if (need > kvq::kKvqStaticScratchBytes) return KVQ_ERR_WORKSPACE;  // larger than the fixed scratch
   s = kvq::check_device(nullptr);  // an unsupported device is KVQ_ERR_DEVICE, before any symbol lookup
@@ -80,6 +80,7 @@ extern "C" KVQ_API kvq_status kvq_decode_attn_static(const kvq_attn_desc* desc, 
   void* scratch = nullptr;
   s = kvq::scratch_on_current_device(static_cast<cudaStream_t>(stream), &scratch);
   if (s != KVQ_OK) return s;
-  return kvq_decode_attn(desc, q, k_codes, k_scale, k_zero, v_codes, v_scale, v_zero, seq_lens, page_table, out, lse,
-                         scratch, kvq::kKvqStaticScratchBytes, dev_status, stream);
+  return kvq::decode_attn_bounded(desc, q, k_codes, k_scale, k_zero, v_codes, v_scale, v_zero, seq_lens, page_table,
+                                  out, lse, scratch, kvq::kKvqStaticScratchBytes, kvq::kKvqStaticScratchBytes,
+                                  dev_status, stream);
 }

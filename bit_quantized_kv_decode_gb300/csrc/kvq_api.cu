@@ -6,9 +6,12 @@
 #include <cstdint>
 
 #include "decode_general.h"
-#include "kvq_internal.h"
+#include "kvq_entry.h"
 
 namespace kvq {
+#ifdef KVQ_PROFILE
+static unsigned long long* g_prof_counters = nullptr;
+#endif
 namespace {
 
 constexpr int kMaxBatchDecode = 1024;
@@ -34,13 +37,6 @@ kvq_status check_cache(const kvq_cache_desc* c) {
 
 // The specialised decode kernel's geometry; others take the general kernel.
 bool default_geometry(const kvq_cache_desc* c) { return c->head_dim == kHeadDim && group_of(c) == 128; }
-// Decode calls the block-range kernel takes: every geometry but the default,
-// and every BF16-operand call (it runs the BF16 mode faster than the
-// specialised kernel, whose tensor memory holds one K and one V tile of
-// BF16 codes).
-bool use_general(const kvq_attn_desc* d) {
-  return !default_geometry(&d->cache) || d->operand_mode == KVQ_OPERANDS_BF16;
-}
 
 }  // namespace
 
@@ -85,6 +81,34 @@ int units_per_seq(const kvq_attn_desc* d) {
   return g > kGroupQ ? d->cache.num_kv_heads * (g / kGroupQ) : d->cache.num_kv_heads;
 }
 
+// Decode calls the block-range kernel takes: every geometry but the default
+// and every BF16-operand call (the specialised kernel is built for E4M3
+// operands at head dim 128, groups of 128); of the rest (E4M3, default
+// geometry), those it runs faster, measured on GB300 at B = 128, L = 32K:
+// 8 query heads per KV head (one read of each block for all 8 heads, where
+// the specialised kernel's units hold 4 and read every block twice: 47% vs
+// 35% of HBM peak with 4-bit codes), and with 4 heads per unit the scheme
+// pairs with token-wise K or channel-wise V at 2 bits (47-48% vs 43%, 40%
+// vs 38% with both channel-wise) and token-wise K with channel-wise V at 4
+// bits (83% vs 78%).  Small calls stay in the specialised kernel (its
+// persistent CTAs start faster: 10.5% vs 7% at B = 8, L = 4K), and so do
+// calls with the E2M1 V placement, which only it builds.
+// Calls the specialised kernel takes (any query heads per KV head it builds).
+bool specialised_ok(const kvq_attn_desc* d) {
+  return default_geometry(&d->cache) && d->operand_mode == KVQ_OPERANDS_FP8;
+}
+constexpr long long kGeneralMinBlocks = 32768;  // (sequence, unit, block) triples of max_blocks per unit
+bool use_general(const kvq_attn_desc* d) {
+  if (!default_geometry(&d->cache) || d->operand_mode == KVQ_OPERANDS_BF16) return true;
+  if (d->flags & KVQ_FLAG_E2M1_V) return false;
+  const int g = heads_per_kv(d);
+  if ((long long)d->batch * units_per_seq(d) * d->max_blocks < kGeneralMinBlocks) return false;
+  if (g == 8) return true;
+  if (g != kGroupQ) return false;
+  const bool kcw = d->cache.k_scheme == KVQ_CHANNELWISE, vcw = d->cache.v_scheme == KVQ_CHANNELWISE;
+  return d->cache.bits == 2 ? (!kcw || vcw) : (!kcw && vcw);
+}
+
 WorkspaceLayout workspace_layout(int batch, int units, int num_ctas) {
   WorkspaceLayout w;
   w.counters = 0;
@@ -118,16 +142,19 @@ kvq_status check_attn(const kvq_attn_desc* d) {
 // decode_general.cuh cuts each sequence's units into ranges in proportion
 // to its length), the launch shape and the workspace.  The target is
 // units * S: with num_ctas = 0, S is chosen between one and eight waves of
-// resident CTAs so that a batch of equal lengths fills its last wave best
-// (fewest idle CTA slots), then the fewest ranges; with num_ctas > 0,
-// S = ceil(num_ctas / units).  At most max_blocks ranges per unit.
+// resident CTAs so that a batch of max_blocks per unit fills its last wave
+// best (fewest idle CTA slots), then the fewest ranges, and the plan may aim
+// lower (down to one wave) when the actual lengths hold less work; with
+// num_ctas > 0, S = ceil(num_ctas / units), kept as given.  At most
+// max_blocks ranges per unit.
 struct GeneralPlan {
   GenLaunch launch;
   int nh;            // query heads per unit: 8 (each KV block read once) or 4
   int units;         // units per sequence
   int gq;            // query heads a unit holds
   long long n_target;
-  long long slots;   // grid = part slots: n_target + every unit (one range each at least)
+  long long n_floor;  // the fewest CTAs the plan may aim at (one wave; n_target with num_ctas > 0)
+  long long slots;    // grid = part slots: n_target + every unit (one range each at least)
   size_t plan_ps, assign, part_lse, part_o, total;  // workspace offsets and size
 };
 
@@ -150,11 +177,11 @@ kvq_status general_plan(const kvq_attn_desc* d, GeneralPlan* plan) {
                                       group_of(&d->cache), d->operand_mode == KVQ_OPERANDS_BF16, plan->nh, smem_sm,
                                       reserved);
   const long long units = (long long)d->batch * plan->units;
+  const long long resident = (long long)plan->launch.ctas_per_sm * sm;
   long long splits;
   if (d->num_ctas > 0) {
     splits = (d->num_ctas + units - 1) / units;
   } else {
-    const long long resident = (long long)plan->launch.ctas_per_sm * sm;
     const long long lo = (resident + units - 1) / units, hi = (8 * resident + units - 1) / units;
     splits = lo;
     double best = -1.0;
@@ -169,6 +196,7 @@ kvq_status general_plan(const kvq_attn_desc* d, GeneralPlan* plan) {
   const int g = heads_per_kv(d);
   plan->gq = plan->nh == 8 ? 8 : (g < kGroupQ ? g : kGroupQ);
   plan->n_target = units * splits;
+  plan->n_floor = d->num_ctas > 0 ? plan->n_target : resident;
   plan->slots = plan->n_target + units;
   plan->plan_ps = 0;
   plan->assign = round_up((size_t)(d->batch + 1) * sizeof(int), 256);
@@ -212,6 +240,7 @@ kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const ui
   p.units_per_seq = plan.units;
   p.kv_shift = 0;  // a unit is one KV head (up to 8 query heads)
   p.n_target = plan.n_target;
+  p.n_floor = plan.n_floor;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.flags = desc->flags;
   p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
@@ -229,14 +258,112 @@ kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const ui
   return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
+// The kernel a checked call takes and its workspace: the general one where
+// use_general says so, unless its workspace would exceed `limit` bytes and
+// the specialised kernel takes the call (E4M3 operands, head dim 128, groups
+// of 128), whose workspace is then the one returned.
+kvq_status decode_route(const kvq_attn_desc* desc, size_t limit, bool* general, size_t* bytes) {
+  kvq_status s;
+  *general = use_general(desc);
+  if (*general) {
+    GeneralPlan plan;
+    s = general_plan(desc, &plan);
+    if (s != KVQ_OK) return s;
+    *bytes = plan.total;
+    if (plan.total <= limit || !specialised_ok(desc)) return KVQ_OK;
+    *general = false;
+  }
+  int sm = 0;
+  if (desc->num_ctas == 0) {
+    s = check_device(&sm);
+    if (s != KVQ_OK) return s;
+  }
+  const int ctas = resolve_ctas(desc, sm);
+  *bytes = workspace_layout(desc->batch, units_per_seq(desc), ctas).total;
+  return KVQ_OK;
+}
+
 }  // namespace
+
+kvq_status decode_workspace_bounded(const kvq_attn_desc* desc, size_t limit, size_t* bytes) {
+  kvq_status s = check_attn(desc);
+  if (s != KVQ_OK) return s;
+  if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
+  bool general = false;
+  return decode_route(desc, limit, &general, bytes);
+}
+
+kvq_status decode_attn_bounded(const kvq_attn_desc* desc, const uint16_t* q, const uint8_t* k_codes,
+                               const uint16_t* k_scale, const uint16_t* k_zero, const uint8_t* v_codes,
+                               const uint16_t* v_scale, const uint16_t* v_zero, const int32_t* seq_lens,
+                               const int32_t* page_table, float* out, float* lse, void* workspace,
+                               size_t workspace_bytes, size_t limit, uint32_t* dev_status, void* stream) {
+  kvq_status s = check_attn(desc);
+  if (s != KVQ_OK) return s;
+  // cache arrays are read with 16-byte bulk copies; the rest with scalar accesses
+  const void* bulk[] = {k_codes, k_scale, k_zero, v_codes, v_scale, v_zero};
+  for (const void* ptr : bulk)
+    if (ptr == nullptr || !aligned16(ptr)) return KVQ_ERR_INVALID_ARG;
+  if (q == nullptr || seq_lens == nullptr || out == nullptr || lse == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(out) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return KVQ_ERR_INVALID_ARG;
+  if (page_table != nullptr && (reinterpret_cast<uintptr_t>(page_table) & 3u)) return KVQ_ERR_INVALID_ARG;
+  if (page_table == nullptr && (long long)desc->batch * desc->max_blocks > desc->cache.num_pages)
+    return KVQ_ERR_INVALID_ARG;
+  int sm = 0;
+  s = check_device(&sm);
+  if (s != KVQ_OK) return s;
+  bool general = false;
+  size_t need = 0;
+  s = decode_route(desc, limit, &general, &need);
+  if (s != KVQ_OK) return s;
+  const float sm_scale = desc->sm_scale > 0.0f ? desc->sm_scale : 1.0f / std::sqrt((float)desc->cache.head_dim);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (general) return decode_general(desc, q, k_codes, k_scale, k_zero, v_codes, v_scale, v_zero, seq_lens,
+                                     page_table, out, lse, workspace, workspace_bytes, dev_status, sm_scale, st);
+  const int ctas = resolve_ctas(desc, sm);
+  const WorkspaceLayout w = workspace_layout(desc->batch, units_per_seq(desc), ctas);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVQ_ERR_WORKSPACE;
+  if (workspace_bytes < w.total) return KVQ_ERR_WORKSPACE;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  if (cudaMemsetAsync(ws + w.counters, 0, (size_t)desc->batch * units_per_seq(desc) * kCounterGroups * sizeof(int),
+                      st) !=
+      cudaSuccess)
+    return KVQ_ERR_CUDA;
+  DecodeParams p{};
+  p.q = q; p.k_codes = k_codes; p.k_scale = k_scale; p.k_zero = k_zero;
+  p.v_codes = v_codes; p.v_scale = v_scale; p.v_zero = v_zero;
+  p.seq_lens = seq_lens; p.page_table = page_table; p.out = out; p.lse = lse; p.dev_status = dev_status;
+  p.counters = reinterpret_cast<int*>(ws + w.counters);
+  p.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
+  p.part_o = reinterpret_cast<float*>(ws + w.part_o);
+  p.batch = desc->batch; p.num_kv_heads = desc->cache.num_kv_heads; p.num_q_heads = desc->num_q_heads;
+  p.max_blocks = desc->max_blocks; p.num_pages = desc->cache.num_pages; p.num_ctas = ctas;
+  {
+    const int g = heads_per_kv(desc);
+    p.gq = g < kGroupQ ? g : kGroupQ;
+    p.units_per_seq = units_per_seq(desc);
+    p.kv_shift = g > kGroupQ ? 1 : 0;
+  }
+  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+  p.flags = desc->flags;
+  p.nibble_mul = 1u << 28;
+  p.minus_one = 0xffffffffu;
+  p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
+#ifdef KVQ_PROFILE
+  p.prof = g_prof_counters;
+#endif
+  cudaError_t e = launch_decode(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme, p, st);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+}
+
 }  // namespace kvq
 
 using namespace kvq;
 
 #ifdef KVQ_PROFILE
-static unsigned long long* g_prof_counters = nullptr;
-extern "C" KVQ_API void kvq_prof_set(unsigned long long* counters) { g_prof_counters = counters; }
+extern "C" KVQ_API void kvq_prof_set(unsigned long long* counters) { kvq::g_prof_counters = counters; }
 #endif
 
 extern "C" {
@@ -343,23 +470,14 @@ KVQ_API kvq_status kvq_dequant(const kvq_cache_desc* cache, int32_t which, const
 }
 
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* bytes) {
+  return kvq::decode_workspace_bounded(desc, SIZE_MAX, bytes);
+}
+
+KVQ_API kvq_status kvq_decode_path(const kvq_attn_desc* desc, int32_t* path) {
   kvq_status s = check_attn(desc);
   if (s != KVQ_OK) return s;
-  if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
-  if (use_general(desc)) {
-    GeneralPlan plan;
-    s = general_plan(desc, &plan);
-    if (s != KVQ_OK) return s;
-    *bytes = plan.total;
-    return KVQ_OK;
-  }
-  int sm = 0;
-  if (desc->num_ctas == 0) {
-    s = check_device(&sm);
-    if (s != KVQ_OK) return s;
-  }
-  const int ctas = resolve_ctas(desc, sm);
-  *bytes = workspace_layout(desc->batch, units_per_seq(desc), ctas).total;
+  if (path == nullptr) return KVQ_ERR_INVALID_ARG;
+  *path = use_general(desc) ? KVQ_PATH_GENERAL : KVQ_PATH_SPECIALISED;
   return KVQ_OK;
 }
 
@@ -368,61 +486,8 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
                                    const uint16_t* v_scale, const uint16_t* v_zero, const int32_t* seq_lens,
                                    const int32_t* page_table, float* out, float* lse, void* workspace,
                                    size_t workspace_bytes, uint32_t* dev_status, void* stream) {
-  kvq_status s = check_attn(desc);
-  if (s != KVQ_OK) return s;
-  // cache arrays are read with 16-byte bulk copies; the rest with scalar accesses
-  const void* bulk[] = {k_codes, k_scale, k_zero, v_codes, v_scale, v_zero};
-  for (const void* ptr : bulk)
-    if (ptr == nullptr || !aligned16(ptr)) return KVQ_ERR_INVALID_ARG;
-  if (q == nullptr || seq_lens == nullptr || out == nullptr || lse == nullptr) return KVQ_ERR_INVALID_ARG;
-  if (!aligned16(q) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
-      (reinterpret_cast<uintptr_t>(out) & 3u) || (reinterpret_cast<uintptr_t>(lse) & 3u))
-    return KVQ_ERR_INVALID_ARG;
-  if (page_table != nullptr && (reinterpret_cast<uintptr_t>(page_table) & 3u)) return KVQ_ERR_INVALID_ARG;
-  if (page_table == nullptr && (long long)desc->batch * desc->max_blocks > desc->cache.num_pages)
-    return KVQ_ERR_INVALID_ARG;
-  int sm = 0;
-  s = check_device(&sm);
-  if (s != KVQ_OK) return s;
-  const float sm_scale = desc->sm_scale > 0.0f ? desc->sm_scale : 1.0f / std::sqrt((float)desc->cache.head_dim);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (use_general(desc)) return decode_general(desc, q, k_codes, k_scale, k_zero, v_codes, v_scale,
-                                                             v_zero, seq_lens, page_table, out, lse, workspace,
-                                                             workspace_bytes, dev_status, sm_scale, st);
-  const int ctas = resolve_ctas(desc, sm);
-  const WorkspaceLayout w = workspace_layout(desc->batch, units_per_seq(desc), ctas);
-  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KVQ_ERR_WORKSPACE;
-  if (workspace_bytes < w.total) return KVQ_ERR_WORKSPACE;
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  if (cudaMemsetAsync(ws + w.counters, 0, (size_t)desc->batch * units_per_seq(desc) * kCounterGroups * sizeof(int),
-                      st) !=
-      cudaSuccess)
-    return KVQ_ERR_CUDA;
-  DecodeParams p{};
-  p.q = q; p.k_codes = k_codes; p.k_scale = k_scale; p.k_zero = k_zero;
-  p.v_codes = v_codes; p.v_scale = v_scale; p.v_zero = v_zero;
-  p.seq_lens = seq_lens; p.page_table = page_table; p.out = out; p.lse = lse; p.dev_status = dev_status;
-  p.counters = reinterpret_cast<int*>(ws + w.counters);
-  p.part_lse = reinterpret_cast<float*>(ws + w.part_lse);
-  p.part_o = reinterpret_cast<float*>(ws + w.part_o);
-  p.batch = desc->batch; p.num_kv_heads = desc->cache.num_kv_heads; p.num_q_heads = desc->num_q_heads;
-  p.max_blocks = desc->max_blocks; p.num_pages = desc->cache.num_pages; p.num_ctas = ctas;
-  {
-    const int g = heads_per_kv(desc);
-    p.gq = g < kGroupQ ? g : kGroupQ;
-    p.units_per_seq = units_per_seq(desc);
-    p.kv_shift = g > kGroupQ ? 1 : 0;
-  }
-  p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-  p.flags = desc->flags;
-  p.nibble_mul = 1u << 28;
-  p.minus_one = 0xffffffffu;
-  p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
-#ifdef KVQ_PROFILE
-  p.prof = g_prof_counters;
-#endif
-  cudaError_t e = launch_decode(desc->cache.bits, desc->cache.k_scheme, desc->cache.v_scheme, p, st);
-  return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA;
+  return kvq::decode_attn_bounded(desc, q, k_codes, k_scale, k_zero, v_codes, v_scale, v_zero, seq_lens, page_table,
+                                  out, lse, workspace, workspace_bytes, SIZE_MAX, dev_status, stream);
 }
 
 KVQ_API kvq_status kvq_merge(const float* o_parts, const float* lse_parts, int32_t rows, int32_t splits,

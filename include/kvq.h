@@ -202,6 +202,14 @@ KVQ_API kvq_status kvq_dequant(const kvq_cache_desc* cache, int32_t which, const
  * device when desc->num_ctas == 0). */
 KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* bytes);
 
+/* Which decode kernel kvq_decode_attn runs for `desc` (host only, no device
+ * needed): *path = KVQ_PATH_SPECIALISED (persistent tile-range kernel, head
+ * dim 128, groups of 128, E4M3 operands) or KVQ_PATH_GENERAL (plan, block-
+ * range and merge kernels).  The rule is the one kvq_decode_attn describes. */
+#define KVQ_PATH_SPECIALISED 0
+#define KVQ_PATH_GENERAL 1
+KVQ_API kvq_status kvq_decode_path(const kvq_attn_desc* desc, int32_t* path);
+
 /*
  * Decode attention over the packed cache, affine-folded (abstract; [SUM] 解説):
  * token-wise K scales the partial q.code by s and adds z * sum(q); channel-
@@ -210,16 +218,25 @@ KVQ_API kvq_status kvq_decode_workspace_size(const kvq_attn_desc* desc, size_t* 
  * each G-token group's partial product by s and adds z * sum(p) of that
  * group ([SUM] 限界と未検証の範囲: per-group application); with groups
  * smaller than the head dim, token-wise K and V fold per G-channel group.
- * Head dim 128 with groups of 128: work is split over persistent CTAs in
- * equal tile ranges; a sequence/head cut between CTAs is merged on the device
- * by log-sum-exp.  Other geometries (head dim 64 / 256, groups of 32 / 64)
- * and the BF16 mode: three launches -- a one-CTA plan cuts each (sequence,
- * unit)'s blocks into ranges in proportion to the sequence's length, a
- * second kernel decodes one range per CTA, and a log-sum-exp merge combines
- * the ranges; not KVQ_FLAG_E2M1_V (KVQ_ERR_UNSUPPORTED).  Query heads
- * per KV head: 1, 2, 4 or 8 (a work unit takes up to 4 query heads of one KV
- * head, so with 8 each KV block is read twice).  sm_scale <= 0 means
- * 1 / sqrt(head_dim).
+ * Two kernels (kvq_decode_path tells which one a call takes).  The
+ * specialised one (head dim 128, groups of 128, E4M3 operands) splits the
+ * work over persistent CTAs in equal tile ranges; a sequence/head cut
+ * between CTAs is merged on the device by log-sum-exp; its units take up to
+ * 4 query heads, so with 8 query heads per KV head it reads each KV block
+ * twice.  The general one runs three launches -- a one-CTA plan cuts each
+ * (sequence, unit)'s blocks into ranges in proportion to the sequence's
+ * length, a second kernel decodes one range per CTA (units of 4 or 8 query
+ * heads: each KV block is read once), and a log-sum-exp merge combines the
+ * ranges.  The general kernel takes every other geometry (head dim 64 / 256,
+ * groups of 32 / 64) and the BF16 mode, and, on the specialised kernel's
+ * geometry in E4M3, the calls it runs faster: 8 query heads per KV head; 4
+ * with 2-bit codes unless K is channel-wise and V token-wise; 4 with 4-bit
+ * codes, K token-wise and V channel-wise -- each only when batch x units x
+ * max_blocks >= 32768 (units per sequence: the KV heads, twice that with 8
+ * query heads per KV head); smaller calls, other head counts (1, 2) and
+ * KVQ_FLAG_E2M1_V stay in the specialised kernel.  KVQ_FLAG_E2M1_V on
+ * another geometry or in the BF16 mode: KVQ_ERR_UNSUPPORTED.  Query heads
+ * per KV head: 1, 2, 4 or 8.  sm_scale <= 0 means 1 / sqrt(head_dim).
  *   q        bf16 [batch][num_q_heads][head_dim]
  *   k_codes, v_codes, k_scale, k_zero, v_scale, v_zero: cache arrays
  *   seq_lens int32 [batch], each in [0, max_blocks*128]
@@ -246,13 +263,14 @@ KVQ_API kvq_status kvq_decode_attn(const kvq_attn_desc* desc, const uint16_t* q,
  * kvq_decode_attn minus the workspace: the split-merge scratch lives in a
  * fixed 4 MiB device array owned by the library, held on every device that
  * loads the library until the process exits.  Returns KVQ_ERR_WORKSPACE when
- * a call needs more scratch than kvq_decode_workspace_size reports (head dim
- * 128, groups of 128: batch * num_kv_heads * 4 bytes of counters, twice that
- * with 8 query heads per KV head, plus 4 KiB per CTA; other geometries and
- * the BF16 mode: the plan (4 bytes per sequence, 16 per CTA) and head_dim + 1
- * floats per query head and block range);
- * kvq_decode_attn with a caller workspace then
- * remains available.  Every call on a stream that is not being captured
+ * a call needs more scratch than that (the specialised kernel: batch *
+ * num_kv_heads * 4 bytes of counters, twice that with 8 query heads per KV
+ * head, plus 4 KiB per CTA; the general kernel: the plan (4 bytes per
+ * sequence, 16 per CTA) and head_dim + 1 floats per query head and block
+ * range).  A call kvq_decode_attn would run in the general kernel on the
+ * specialised kernel's geometry (E4M3 operands) runs in the specialised
+ * kernel here when the general kernel's scratch would not fit.
+ * kvq_decode_attn with a caller workspace remains available.  Every call on a stream that is not being captured
  * looks up the array's address on the current device (the first such call
  * loads the module); a call inside a stream capture reuses the address of
  * the last uncaptured call on that device, so make one ordinary call on each

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import __graft_entry__ as entry
 from bit_quantized_kv_decode_gb300 import _lib
@@ -69,7 +70,8 @@ def test_cache_bytes(lib):
 
 
 def test_workspace_size_host_only(lib):
-    d = _lib.AttnDesc(_cache(4, pages=128 * 256), 128, 32, 256, 0, 0.0, 304, 0)
+    # 4-bit K channel-wise / V token-wise: the specialised kernel
+    d = _lib.AttnDesc(_cache(4, 1, 0, pages=128 * 256), 128, 32, 256, 0, 0.0, 304, 0)
     n = ctypes.c_size_t()
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
     # counters (one per sequence x kv head) + part lse + part out, each 256-byte aligned
@@ -82,9 +84,9 @@ def test_workspace_size_host_only(lib):
         d = _lib.AttnDesc(_cache(4, pages=128 * 256), 128, hq, 256, 0, 0.0, 304, 0)
         assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
         assert n.value == 128 * 8 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
-    d = _lib.AttnDesc(_cache(4, pages=128 * 256), 128, 64, 256, 0, 0.0, 304, 0)  # 8: two units per KV head
+    d = _lib.AttnDesc(_cache(4, pages=8 * 32), 8, 64, 32, 0, 0.0, 304, 0)  # 8, small call: two units per KV head
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
-    assert n.value == 128 * 16 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
+    assert n.value == 8 * 16 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
     bad = _lib.AttnDesc(_cache(4), 0, 32, 256, 0, 0.0, 304, 0)
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
     bad = _lib.AttnDesc(_cache(4), 2048, 32, 256, 0, 0.0, 304, 0)
@@ -144,6 +146,61 @@ def test_general_geometry_workspace_host_only(lib):
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
 
 
+def _spec_ws(batch, units, ctas):
+    """Workspace of the specialised kernel, each part 256-byte aligned:
+    arrival counters (one int per unit), part lse and part outputs (two parts
+    of 4 heads per CTA)."""
+    r256 = lambda x: (x + 255) // 256 * 256
+    return r256(batch * units * 4) + r256(ctas * 2 * 4 * 4) + r256(ctas * 2 * 4 * 128 * 4)
+
+
+def test_default_geometry_routing_host_only(lib):
+    """E4M3 operands at head dim 128, groups of 128: the calls the general
+    kernel runs faster (8 query heads per KV head; 2-bit codes unless K is
+    channel-wise and V token-wise; 4-bit codes with K token-wise and V
+    channel-wise) take it once they hold at least 32,768 (sequence, unit,
+    block) triples; the rest, smaller calls and the E2M1 V placement take the
+    specialised kernel.  Read from the workspace each layout needs."""
+    n = ctypes.c_size_t()
+    big = dict(batch=128, max_blocks=256)  # 128 x 8 x 256 = 262,144 triples
+    cases = [  # (bits, k, v, q heads, expected kernel)
+        (2, 0, 0, 32, "general"), (2, 0, 1, 32, "general"), (2, 1, 1, 32, "general"), (2, 1, 0, 32, "spec"),
+        (4, 0, 1, 32, "general"), (4, 1, 0, 32, "spec"), (4, 0, 0, 32, "spec"), (4, 1, 1, 32, "spec"),
+        (4, 1, 0, 64, "general"), (2, 0, 0, 64, "general"), (2, 0, 0, 16, "spec"), (2, 0, 0, 8, "spec"),
+    ]
+    path = ctypes.c_int32()
+    for bits, k, v, hq, want in cases:
+        d = _lib.AttnDesc(_cache(bits, k, v, pages=128 * 256), big["batch"], hq, big["max_blocks"], 0, 0.0, 304, 0)
+        assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+        assert lib.kvq_decode_path(ctypes.byref(d), ctypes.byref(path)) == 0
+        assert path.value == (_lib.PATH_GENERAL if want == "general" else _lib.PATH_SPECIALISED), (bits, k, v, hq)
+        g = hq // 8
+        if want == "general":
+            units = 8 * 128
+            splits = -(-304 // units)
+            assert n.value == _general_ws(128, units, splits, 8 if g == 8 else 4, 128), (bits, k, v, hq)
+        else:
+            units = 16 if g == 8 else 8
+            assert n.value == _spec_ws(128, units, 304), (bits, k, v, hq)
+    # the same pairs in a small call (8 x 8 x 32 = 2,048 triples) stay specialised
+    for bits, k, v in ((2, 0, 0), (4, 0, 1)):
+        d = _lib.AttnDesc(_cache(bits, k, v, pages=8 * 32), 8, 32, 32, 0, 0.0, 304, 0)
+        assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+        assert n.value == _spec_ws(8, 8, 304)
+    # the E2M1 V placement: specialised at any size
+    d = _lib.AttnDesc(_cache(2, 0, 0, pages=128 * 256), 128, 32, 256, 0, 0.0, 304, _lib.FLAG_E2M1_V)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+    assert n.value == _spec_ws(128, 8, 304)
+    assert lib.kvq_decode_path(ctypes.byref(d), ctypes.byref(path)) == 0 and path.value == _lib.PATH_SPECIALISED
+    # other geometries and the BF16 mode: general at any size; bad descriptors are refused
+    for d in (_lib.AttnDesc(_cache(4, 1, 0, hd=256, group=64, pages=64), 2, 32, 4, 0, 0.0, 304, 0),
+              _lib.AttnDesc(_cache(2, 1, 0, pages=64), 2, 32, 4, 1, 0.0, 304, 0)):
+        assert lib.kvq_decode_path(ctypes.byref(d), ctypes.byref(path)) == 0 and path.value == _lib.PATH_GENERAL
+    bad = _lib.AttnDesc(_cache(4), 128, 24, 256, 0, 0.0, 304, 0)  # 3 query heads per KV head
+    assert lib.kvq_decode_path(ctypes.byref(bad), ctypes.byref(path)) == 2
+    assert lib.kvq_decode_path(ctypes.byref(d), None) == 1
+
+
 def test_validation_precedes_device(lib):
     """Bad arguments are rejected on the host (no device needed)."""
     c = _cache(4)
@@ -180,3 +237,19 @@ def test_no_device_reports_device_error(lib):
     c = _cache(4)
     fake = ctypes.c_void_p(0x10000)
     assert lib.kvq_pack(ctypes.byref(c), 0, fake, 1, 128, None, None, 1, fake, fake, fake, None, None) == 5
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-only: on a GPU machine the call would launch")
+def test_static_entry_routes_within_its_scratch_host_only(lib):
+    """The static entry's 4 MiB scratch: a call the general kernel would take
+    with a larger workspace goes to the specialised kernel when that one takes
+    it (E4M3, head dim 128, groups of 128) -- the call then passes the scratch
+    check and stops at the device check (no GPU here) -- and is refused with
+    KVQ_ERR_WORKSPACE when it does not (BF16 operands)."""
+    fake = ctypes.c_void_p(0x10000)
+    n = ctypes.c_size_t()
+    d = _lib.AttnDesc(_cache(2, 0, 0, pages=128 * 256), 128, 32, 256, 0, 0.0, 304, 0)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0 and n.value > 4 << 20
+    assert lib.kvq_decode_attn_static(ctypes.byref(d), *([fake] * 7), fake, None, fake, fake, None, None) == 5
+    bf16 = _lib.AttnDesc(_cache(2, 0, 0, pages=128 * 256), 128, 32, 256, 1, 0.0, 304, 0)
+    assert lib.kvq_decode_attn_static(ctypes.byref(bf16), *([fake] * 7), fake, None, fake, fake, None, None) == 3

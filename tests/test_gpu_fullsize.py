@@ -4,8 +4,8 @@ times (default grid, one call over the whole batch), on sampled outputs.
 The whole cache is packed on the GPU from the seeded generators (as bench.py
 does); for a sample of (sequence, kv head) units the same pre-quantization
 values are drawn again, handed to the oracle, which packs, dequantizes and
-attends in fp64, and the unit's four query heads are compared with the
-decode output.  Tolerances as in the other parity tests.
+attends in fp64, and the unit's query heads (4, or 8 per KV head) are
+compared with the decode output.  Tolerances as in the other parity tests.
 """
 import numpy as np
 import pytest
@@ -39,7 +39,8 @@ def _oracle_unit(w, c, b, h, ks, vs, dev):
     cs = synth.outlier_channels(w, SEED, dev)
     k = synth.kv_unit(w, SEED, 0, b, h, n, dev, cs[h]).cpu().numpy()[None, None]
     v = synth.kv_unit(w, SEED, 1, b, h, n, dev).cpu().numpy()[None, None]
-    qb = c["q"][b:b + 1, 4 * h:4 * h + 4].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    g = w.num_q_heads // w.num_kv_heads
+    qb = c["q"][b:b + 1, g * h:g * h + g].cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
     ref = orc.reference_decode(qb, k, v, np.array([n], dtype=np.int32), w.bits, ks, vs, None, (n + 127) // 128,
                                group=w.group)
     return ref["out"][0], ref["lse"][0]
@@ -47,11 +48,15 @@ def _oracle_unit(w, c, b, h, ks, vs, dev):
 
 @pytest.mark.parametrize("wl,ks,vs", [
     ("b128_l32k_int4", 1, 0),
+    ("b128_l32k_int4", 0, 1),
+    ("b128_l32k_int4_q8", 1, 0),
+    ("b128_l32k_int2_q8", 0, 0),
     ("b128_l32k_int2", 0, 0),
     ("b128_l32k_int2", 0, 1),
     ("b128_l32k_int2", 1, 0),
     ("b128_l32k_int2", 1, 1),
     ("paged_ragged_int2", 1, 0),
+    ("paged_ragged_int2", 0, 0),
     ("b32_l32k_d256_g64_int4", 1, 0),
     ("b32_l32k_d128_g32_int2", 1, 0),
     ("b32_l32k_d64_g32_int2", 1, 0),
@@ -60,7 +65,12 @@ def _oracle_unit(w, c, b, h, ks, vs, dev):
 def test_full_size_sampled_units(wl, ks, vs):
     import bit_quantized_kv_decode_gb300 as kvq
     dev = torch.device("cuda")
-    w = synth.WORKLOADS[wl]
+    if wl.endswith("_q8"):  # 8 query heads per KV head
+        w = synth.WORKLOADS[wl[:-3]]
+        w = synth.shrink(w, num_q_heads=8 * w.num_kv_heads, name=wl)
+    else:
+        w = synth.WORKLOADS[wl]
+    g = w.num_q_heads // w.num_kv_heads
     c = bench.build_cache(w, SEED, dev, ks, vs)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     out, lse = kvq.decode_attn(c["desc"], c["q"], c["k"], c["v"], c["lens"], c["pt"], c["max_blocks"],
@@ -72,8 +82,8 @@ def test_full_size_sampled_units(wl, ks, vs):
         ro, rl = _oracle_unit(w, c, b, h, ks, vs, dev)
         ref_o.append(ro)
         ref_l.append(rl)
-        got_o.append(out[b, 4 * h:4 * h + 4].double().cpu().numpy())
-        got_l.append(lse[b, 4 * h:4 * h + 4].double().cpu().numpy())
+        got_o.append(out[b, g * h:g * h + g].double().cpu().numpy())
+        got_l.append(lse[b, g * h:g * h + g].double().cpu().numpy())
     ref_o, ref_l, got_o, got_l = map(np.stack, (ref_o, ref_l, got_o, got_l))
     rms = float(np.sqrt((ref_o ** 2).mean()))
     err = float(np.abs(got_o - ref_o).max()) / rms

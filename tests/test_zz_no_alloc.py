@@ -87,3 +87,51 @@ def test_static_scratch_rejects_oversized_calls():
     fake = ctypes.c_void_p(0x10000)
     st = lib.kvq_decode_attn_static(ctypes.byref(ad), *([fake] * 7), fake, None, fake, fake, None, None)
     assert st == 3  # KVQ_ERR_WORKSPACE, before any launch
+
+
+def test_static_scratch_falls_back_to_specialised_kernel():
+    """A call kvq_decode_attn runs in the general kernel (2-bit codes, K and V
+    token-wise, B=64, L=16K: 65,536 (sequence, kv head, block) triples) whose
+    general-kernel scratch exceeds the fixed array runs in the specialised
+    kernel instead: the static output matches the workspace entry point's
+    (general kernel) within the two kernels' tolerances, and the oracle on
+    sampled units."""
+    import bench
+    import bit_quantized_kv_decode_gb300 as kvq
+    from bit_quantized_kv_decode_gb300 import _lib
+    from tests.test_gpu_fullsize import SEED, _oracle_unit, _sample_units
+    dev = torch.device("cuda")
+    w = synth.shrink(synth.WORKLOADS["b128_l32k_int2"], batch=64, max_seq_len=16384, k_scheme=0, v_scheme=0,
+                     name="b64_l16k_int2_tt")
+    c = bench.build_cache(w, SEED, dev, 0, 0)
+    ad = kvq.attn_desc(c["desc"], w.batch, c["max_blocks"], num_q_heads=w.num_q_heads)
+    assert kvq.decode_path(ad) == _lib.PATH_GENERAL
+    assert kvq.workspace_size(ad) > 4 << 20
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    out_g, lse_g = kvq.decode_attn(c["desc"], c["q"], c["k"], c["v"], c["lens"], c["pt"], c["max_blocks"],
+                                   dev_status=st)
+    out = torch.empty_like(out_g)
+    lse = torch.empty_like(lse_g)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        kvq.decode_attn_static(c["desc"], c["q"], c["k"], c["v"], c["lens"], max_blocks=c["max_blocks"], out=out,
+                               lse=lse, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        rms = float(out_g.double().pow(2).mean().sqrt())
+        assert float((out.double() - out_g.double()).abs().max()) <= 2 * TOL[0] * rms
+        assert float((lse.double() - lse_g.double()).abs().max()) <= 2 * LSE_TOL[0]
+    got_o, ref_o, got_l, ref_l = [], [], [], []
+    for b, h in _sample_units(w, c["lens_cpu"], SEED + 5)[:8]:
+        ro, rl = _oracle_unit(w, c, b, h, 0, 0, dev)
+        ref_o.append(ro)
+        ref_l.append(rl)
+        got_o.append(out[b, 4 * h:4 * h + 4].double().cpu().numpy())
+        got_l.append(lse[b, 4 * h:4 * h + 4].double().cpu().numpy())
+    ref_o, ref_l, got_o, got_l = map(np.stack, (ref_o, ref_l, got_o, got_l))
+    rms = float(np.sqrt((ref_o ** 2).mean()))
+    assert float(np.abs(got_o - ref_o).max()) <= TOL[0] * rms
+    assert float(np.abs(got_l - ref_l).max()) <= LSE_TOL[0]
+    del c
+    torch.cuda.empty_cache()

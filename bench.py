@@ -433,7 +433,11 @@ def main():
                     help="override the workload's batch (smaller cases for profiler captures)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--q-per-kv", type=int, choices=(1, 2, 4, 8), default=None,
-                    help="query heads per KV head (the workloads use 4); 8 reads every KV block twice")
+                    help="query heads per KV head (the workloads use 4)")
+    ap.add_argument("--k-scheme", choices=("token", "channel"), default=None,
+                    help="override the workload's K quantization axis")
+    ap.add_argument("--v-scheme", choices=("token", "channel"), default=None,
+                    help="override the workload's V quantization axis")
     ap.add_argument("--operands", choices=("fp8", "bf16"), default="fp8",
                     help="tensor-core operand mode: fp8 (default) or the bf16 mode")
     args = ap.parse_args()
@@ -443,6 +447,10 @@ def main():
         w = synth.shrink(w, batch=args.batch, name=f"{w.name}_b{args.batch}")
     if args.q_per_kv is not None and args.q_per_kv * w.num_kv_heads != w.num_q_heads:
         w = synth.shrink(w, num_q_heads=args.q_per_kv * w.num_kv_heads, name=f"{w.name}_g{args.q_per_kv}")
+    for which, arg in (("k_scheme", args.k_scheme), ("v_scheme", args.v_scheme)):
+        code = {v: k for k, v in SCHEME_NAMES.items()}.get(arg)
+        if arg is not None and code != getattr(w, which):
+            w = synth.shrink(w, **{which: code}, name=f"{w.name}_{which[0]}{arg[0]}")
     if args.impl == "reference":
         return run_reference(args, w)
 

@@ -144,18 +144,19 @@ __device__ __forceinline__ void convert_row(const unsigned char* blk, int nrows,
 // How the batch is cut into CTAs, computed once per call on the device (the
 // plan kernel) from the sequence lengths, so that ragged batches balance
 // without a host round trip.  With T the blocks of all units, the CTA count
-// aimed at is N = min(N_host, max(R, T / kGenRangeBlocks)): the host's count
+// aimed at is N = min(N_host, R * max(1, ceil(T / kGenRangeBlocks / R))): the host's count
 // (whole waves for max_blocks per unit), lowered when the actual lengths hold
-// less work -- to ranges of about kGenRangeBlocks blocks, but never below one
-// wave of resident CTAs R.  Sequence b (nblk_b blocks per unit) gets S_b =
+// less work -- to ranges of about kGenRangeBlocks blocks, rounded up to whole
+// waves of resident CTAs R (one at least).  Sequence b (nblk_b blocks per unit) gets S_b =
 // clamp(floor(nblk_b * N / T), 1, nblk_b) block ranges per unit (none when
 // empty); ps[b] = sum over b' < b of units * S_b', ps[B] = the CTAs with work
 // (<= N + units of non-empty sequences).  CTA c (ps[b] <= c < ps[b + 1])
 // takes unit (c - ps[b]) / S_b, range (c - ps[b]) % S_b, and writes its part
 // to slot c.
 __device__ __forceinline__ long long gen_aim(long long total, long long n_host, long long n_floor) {
-  const long long want = total / kGenRangeBlocks > n_floor ? total / kGenRangeBlocks : n_floor;
-  return want < n_host ? want : n_host;
+  const long long w = n_floor > 0 ? n_floor : 1;
+  const long long want = (total / kGenRangeBlocks + w - 1) / w * w;  // whole waves, at least one
+  return want < w ? (w < n_host ? w : n_host) : (want < n_host ? want : n_host);
 }
 __device__ __forceinline__ int gen_ranges(int nblk, long long total, long long n_target) {
   if (nblk == 0) return 0;

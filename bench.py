@@ -341,23 +341,28 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profile_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
+def profile_traffic(workload: str, general: bool = False):
+    """DRAM bytes per decode launch from the committed ncu record of the kernel
+    that ran (`profiles/decode[_general]_<workload>_traffic.json`), if it was
     captured from the current kernel source (else None)."""
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.json")
+    path = os.path.join(ROOT, "profiles", f"decode_{'general_' if general else ''}{workload}_traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_source_sha256") != kernel_source_hash():
+    if rec.get("kernel_source_sha256") != kernel_source_hash(general):
         return None
     return rec.get("dram_bytes_per_launch")
 
 
-def kernel_source_hash():
+def kernel_source_hash(general: bool = False):
+    """SHA-256 of the sources a decode kernel is compiled from."""
+    names = ("decode.cuh", "kvq_ptx.cuh", "kvq_internal.h")
+    if general:
+        names = ("decode_general.cuh", "decode_general.h") + names
     h = hashlib.sha256()
-    for name in ("decode.cuh", "kvq_ptx.cuh", "kvq_internal.h"):
+    for name in names:
         with open(os.path.join(ROOT, "bit_quantized_kv_decode_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -536,7 +541,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": res["kernel"],
-                     "traffic": None if res["general"] else profile_traffic(w.name),
+                     "traffic": profile_traffic(w.name, res["general"]) if mode == 0 else None,
                      "algorithmic_bytes_per_launch": res["bytes"],
                      "duration_source": ("CUDA events around each kvq_decode_attn call (plan, decode and merge "
                                          "kernels)" if res["general"] else

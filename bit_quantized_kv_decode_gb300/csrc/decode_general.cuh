@@ -98,6 +98,39 @@ __device__ __forceinline__ void warp_reduce_store(float (&v)[N], float* buf) {
   if ((lane & ((32 >> kLog) - 1)) == 0) buf[(threadIdx.x >> 5) * N + (lane >> (5 - kLog))] = r;
   __syncwarp();
 }
+// The per-warp maxima of N values into buf[warp][N]: one redux.sync.max.f32
+// per value (independent instructions whose latencies overlap, where the
+// butterfly above chains log2(32) exchanges), lane i storing value i.
+template <int N>
+__device__ __forceinline__ void warp_max_store(const float (&v)[N], float* buf) {
+  static_assert(N <= 32, "N");
+  const int lane = threadIdx.x & 31;
+  float mine = 0.f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float r = warp_max_redux(v[i]);
+    mine = lane == i ? r : mine;
+  }
+  if (lane < N) buf[(threadIdx.x >> 5) * N + lane] = mine;
+  __syncwarp();
+}
+// Largest of D non-negative fp16 values in shared memory (bits; they order as
+// integers), computed by each warp on its own: no cross-warp exchange.
+template <int D>
+__device__ __forceinline__ uint32_t max_f16_bits(const uint16_t* v) {
+  const int lane = threadIdx.x & 31;
+  uint32_t m;
+  if (D == 64) {
+    m = reinterpret_cast<const uint32_t*>(v)[lane];
+  } else if (D == 128) {
+    const uint2 w = reinterpret_cast<const uint2*>(v)[lane];
+    m = __vmaxu2(w.x, w.y);
+  } else {
+    const uint4 w = reinterpret_cast<const uint4*>(v)[lane];
+    m = __vmaxu2(__vmaxu2(w.x, w.y), __vmaxu2(w.z, w.w));
+  }
+  return __reduce_max_sync(FULL, max(m & 0xffffu, m >> 16));
+}
 // Block-wide result i from buf[4][N] (after a barrier).
 template <int N>
 __device__ __forceinline__ float sum4(const float* buf, int i) {
@@ -271,6 +304,10 @@ decode_general_kernel(const GenParams p, int stages) {
   constexpr int NM = VCW ? NH : 2 * NH;                 // block-max reduction: heads (+ largest V scale)
   constexpr int NZ = VCW ? NH : 4 * NGC;                // per-group p sums (token-wise V: one quad at a time)
   constexpr bool kQszSmem = NH > 4;                     // token-wise K's q sums in shared memory
+  // token-wise V with few (group, head) pairs: each thread keeps its token's
+  // running sum of p * z per channel group and head, reduced once per range
+  // (else the per-group sums are reduced across the CTA at every block)
+  constexpr bool kZp = !VCW && NGC * NH <= 8;
   extern __shared__ __align__(1024) unsigned char smem[];
   const GenLayout L = gen_layout(BITS, D, G, KCW, VCW, BF16, NH, stages);  // shared-memory offsets
   constexpr GenLayout LT = gen_layout(BITS, D, G, KCW, VCW, BF16, NH, 2);  // tensor-memory columns
@@ -282,8 +319,7 @@ decode_general_kernel(const GenParams p, int stages) {
   float* red_m = red_c + 128;                                     // [4][16] block maxima
   float* red_z = red_m + 64;                                      // [2][4][32] per-group p (z) sums
   float* qsz_s = red_z + 256;                                     // [8][8] token-wise K q sums (NH = 8)
-  uint32_t* eg_w = reinterpret_cast<uint32_t*>(qsz_s + 64);       // [4][4] per-warp largest K scale of group g
-  uint64_t* bars = reinterpret_cast<uint64_t*>(eg_w + 16);        // stages [4], mma, drain
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qsz_s + 64 + 16);  // stages [4], mma, drain
   uint32_t* tbase = reinterpret_cast<uint32_t*>(bars + 6);
   int* ok_flag = reinterpret_cast<int*>(tbase + 1);
 
@@ -363,7 +399,7 @@ decode_general_kernel(const GenParams p, int stages) {
     float t[NH];
 #pragma unroll
     for (int k = 0; k < NH; ++k) t[k] = qmax[k];
-    warp_reduce_store<NH, true>(t, red_m);
+    warp_max_store<NH>(t, red_m);
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < NH; ++k) qmax[k] = max4<NH>(red_m, k);
@@ -430,6 +466,7 @@ decode_general_kernel(const GenParams p, int stages) {
     for (int i = 0; i < kQv; ++i) qk[k][i] = BF16 ? qv[k][i] : qv[k][i] * pow2_head(qmax[k]);
 
   float m_run[NH], l_thr[NH], oacc[kHalves][NH], zacc[kHalves][NH];
+  float zp[kZp ? NGC : 1][kZp ? NH : 1];  // kZp: this token's running sum of p * z
 #pragma unroll
   for (int k = 0; k < NH; ++k) {
     m_run[k] = -INFINITY;
@@ -437,6 +474,10 @@ decode_general_kernel(const GenParams p, int stages) {
 #pragma unroll
     for (int hf = 0; hf < kHalves; ++hf) oacc[hf][k] = zacc[hf][k] = 0.f;
   }
+#pragma unroll
+  for (int g = 0; g < (kZp ? NGC : 1); ++g)
+#pragma unroll
+    for (int k = 0; k < (kZp ? NH : 1); ++k) zp[g][k] = 0.f;
 
   bool ok = true;
   uint32_t mma_phase = 0u;
@@ -457,23 +498,13 @@ decode_general_kernel(const GenParams p, int stages) {
     convert_row<BITS, BF16, D * BITS / 128>(st, kBlockTokens, tid, t_a, p.nibble_mul, p.minus_one);
     tc_wait_st();
 
-    // ---- channel-wise K: Q'_g = q * s_g per token group g, and q . z_g
-    if (KCW && !BF16) {  // largest scale of each group: the E4M3 Q' prescale
-      {
-        uint32_t mx[NGT];
+    // ---- channel-wise K: Q'_g = q * s_g per token group g, and q . z_g;
+    //      the largest scale of each group (the E4M3 Q' prescale), found by
+    //      every warp on its own
+    uint32_t e16[KCW && !BF16 ? NGT : 1];
+    if (KCW && !BF16) {
 #pragma unroll
-        for (int g = 0; g < NGT; ++g) {
-          uint32_t m = 0u;  // fp16 bits of non-negative values order as integers
-#pragma unroll
-          for (int i = 0; i < kQv; ++i)
-            if (tid + 128 * i < D) m = max(m, (uint32_t)ksz[g * D + tid + 128 * i]);
-          mx[g] = __reduce_max_sync(FULL, m);
-        }
-        if ((tid & 31) == 0)
-#pragma unroll
-          for (int g = 0; g < NGT; ++g) eg_w[warp * 4 + g] = mx[g];
-      }
-      __syncthreads();
+      for (int g = 0; g < NGT; ++g) e16[g] = f16_exp_field(max_f16_bits<D>(ksz + g * D));
     }
     if (KCW) {
       float t[NH * NGT];  // q . z_g, value g * NH + k
@@ -481,8 +512,7 @@ decode_general_kernel(const GenParams p, int stages) {
       for (int k = 0; k < NH * NGT; ++k) t[k] = 0.f;
 #pragma unroll
       for (int g = 0; g < NGT; ++g) {
-        const float fg =
-            BF16 ? 1.0f : pow2_group(f16_exp_field(max(max(eg_w[g], eg_w[4 + g]), max(eg_w[8 + g], eg_w[12 + g]))));
+        const float fg = BF16 ? 1.0f : pow2_group(e16[KCW && !BF16 ? g : 0]);
 #pragma unroll
         for (int i = 0; i < kQv; ++i) {
           const int c = tid + 128 * i;
@@ -540,8 +570,12 @@ decode_general_kernel(const GenParams p, int stages) {
     for (int k = 0; k < NH; ++k) sc[k] = 0.f;
     if (KCW) {
       const int g = l / G;  // warp-uniform (G >= 32)
-      const float fs =
-          BF16 ? 1.0f : pow2_group_inv(f16_exp_field(max(max(eg_w[g], eg_w[4 + g]), max(eg_w[8 + g], eg_w[12 + g]))));
+      float fs = 1.0f;
+      if (!BF16) {
+#pragma unroll
+        for (int gg = 0; gg < (KCW && !BF16 ? NGT : 1); ++gg)
+          if (gg == g) fs = pow2_group_inv(e16[gg]);
+      }
 #pragma unroll
       for (int hq = 0; hq < HH; ++hq) {
         uint32_t v[12];
@@ -586,13 +620,20 @@ decode_general_kernel(const GenParams p, int stages) {
                                       p.minus_one);
 
     // ---- online softmax over the block: block maxima (and the largest V scale)
-    {
-      float t[NM];
+    {  // red_m[warp][NM]: value k < NH the head maxima, NM - 1 the largest V scale
+      const int lane = tid & 31;
+      float mine = 0.f;
 #pragma unroll
-      for (int k = 0; k < NH; ++k) t[k] = sc[k];
-#pragma unroll
-      for (int k = NH; k < NM; ++k) t[k] = vmax;
-      warp_reduce_store<NM, true>(t, red_m);
+      for (int k = 0; k < NH; ++k) {
+        const float r = warp_max_redux(sc[k]);
+        mine = lane == k ? r : mine;
+      }
+      if (!VCW) {
+        const float r = warp_max_redux(vmax);
+        mine = lane == NM - 1 ? r : mine;
+      }
+      if (lane < NM) red_m[warp * NM + lane] = mine;
+      __syncwarp();
     }
     tc_wait_st();
     __syncthreads();
@@ -615,7 +656,14 @@ decode_general_kernel(const GenParams p, int stages) {
     // per-group sums: token-wise V: sum_l p_l z_(l,g) per channel group (one
     // head quad per buffer); channel-wise V: sum_(l in g) p_l per token group
     // (a warp's tokens lie in one group)
-    if (!VCW) {
+    if (kZp) {
+#pragma unroll
+      for (int g = 0; g < (kZp ? NGC : 1); ++g) {
+        const float z_lg = valid ? h2f(vzz[l * NGC + g]) : 0.f;
+#pragma unroll
+        for (int k = 0; k < (kZp ? NH : 1); ++k) zp[g][k] = fmaf(zp[g][k], alpha[k], pr[k] * z_lg);
+      }
+    } else if (!VCW) {
 #pragma unroll
       for (int hq = 0; hq < HH; ++hq) {
         float t[NZ];
@@ -728,7 +776,7 @@ decode_general_kernel(const GenParams p, int stages) {
             for (int h = 0; h < 4; ++h) {
               const int k = 4 * hq + h;
               add[k] = parts<BF16>(v, h) * pinv[k];
-              zacc[hf][k] = fmaf(zacc[hf][k], alpha[k], sum4<NZ>(red_z + hq * 128, g * 4 + h));
+              if (!kZp) zacc[hf][k] = fmaf(zacc[hf][k], alpha[k], sum4<NZ>(red_z + hq * 128, g * 4 + h));
             }
           }
         }
@@ -753,10 +801,27 @@ decode_general_kernel(const GenParams p, int stages) {
       for (int k = 0; k < NH; ++k) t[k] = l_thr[k];
       warp_reduce_store<NH, false>(t, red_m);
     }
+    if (kZp) {  // the range's sum of p * z per channel group and head: red_z[warp][g * NH + k]
+      constexpr int NP = kZp ? NGC * NH : 1;
+      float t[NP];
+#pragma unroll
+      for (int g = 0; g < (kZp ? NGC : 1); ++g)
+#pragma unroll
+        for (int k = 0; k < (kZp ? NH : 1); ++k) t[g * NH + k] = zp[g][k];
+      warp_reduce_store<NP, false>(t, red_z);
+    }
     __syncthreads();
     float l_run[NH];
 #pragma unroll
     for (int k = 0; k < NH; ++k) l_run[k] = sum4<NH>(red_m, k);
+    if (kZp) {
+#pragma unroll
+      for (int hf = 0; hf < kHalves; ++hf) {
+        const int g = (hf * 128 + tid < D ? hf * 128 + tid : 0) / G;
+#pragma unroll
+        for (int k = 0; k < NH; ++k) zacc[hf][k] = sum4<kZp ? NGC * NH : 1>(red_z, g * NH + k);
+      }
+    }
 #pragma unroll
     for (int hf = 0; hf < kHalves; ++hf) {
       const int c = hf * 128 + tid;

@@ -81,32 +81,25 @@ int units_per_seq(const kvq_attn_desc* d) {
   return g > kGroupQ ? d->cache.num_kv_heads * (g / kGroupQ) : d->cache.num_kv_heads;
 }
 
-// Decode calls the block-range kernel takes: every geometry but the default
-// and every BF16-operand call (the specialised kernel is built for E4M3
-// operands at head dim 128, groups of 128); of the rest (E4M3, default
-// geometry), those it runs faster, measured on GB300 at B = 128, L = 32K:
-// 8 query heads per KV head (one read of each block for all 8 heads, where
-// the specialised kernel's units hold 4 and read every block twice: 47% vs
-// 35% of HBM peak with 4-bit codes), and with 4 heads per unit the scheme
-// pairs with token-wise K or channel-wise V at 2 bits (47-48% vs 43%, 40%
-// vs 38% with both channel-wise) and token-wise K with channel-wise V at 4
-// bits (83% vs 78%).  Small calls stay in the specialised kernel (its
-// persistent CTAs start faster: 10.5% vs 7% at B = 8, L = 4K), and so do
-// calls with the E2M1 V placement, which only it builds.
 // Calls the specialised kernel takes (any query heads per KV head it builds).
 bool specialised_ok(const kvq_attn_desc* d) {
   return default_geometry(&d->cache) && d->operand_mode == KVQ_OPERANDS_FP8;
 }
-constexpr long long kGeneralMinBlocks = 32768;  // (sequence, unit, block) triples of max_blocks per unit
+// Decode calls the block-range (general) kernel takes: every geometry but
+// the default and every BF16-operand call (the specialised kernel is built
+// for E4M3 operands at head dim 128, groups of 128), and on that geometry
+// every call of real size -- measured faster there for every scheme pair and
+// query-head count on GB300 at B = 128, L = 32K (INT4 K-cw/V-tw 74.5% of the
+// HBM peak against 71.6%, INT2 K-/V-token-wise 51% against 44%, 8 query
+// heads per KV head 54% against 35%) and at B = 32, L = 4K (8 heads: 15-17%
+// against 13-15%).  Small calls stay in the specialised kernel, whose
+// persistent CTAs start faster (10% against 7% at B = 8, L = 4K), and so do
+// calls with the E2M1 V placement, which only it builds.
+constexpr long long kGeneralMinBlocks = 8192;  // (sequence, unit, block) triples of max_blocks per unit
 bool use_general(const kvq_attn_desc* d) {
-  if (!default_geometry(&d->cache) || d->operand_mode == KVQ_OPERANDS_BF16) return true;
+  if (!specialised_ok(d)) return true;
   if (d->flags & KVQ_FLAG_E2M1_V) return false;
-  const int g = heads_per_kv(d);
-  if ((long long)d->batch * units_per_seq(d) * d->max_blocks < kGeneralMinBlocks) return false;
-  if (g == 8) return true;
-  if (g != kGroupQ) return false;
-  const bool kcw = d->cache.k_scheme == KVQ_CHANNELWISE, vcw = d->cache.v_scheme == KVQ_CHANNELWISE;
-  return d->cache.bits == 2 ? (!kcw || vcw) : (!kcw && vcw);
+  return (long long)d->batch * units_per_seq(d) * d->max_blocks >= kGeneralMinBlocks;
 }
 
 WorkspaceLayout workspace_layout(int batch, int units, int num_ctas) {

@@ -70,20 +70,20 @@ def test_cache_bytes(lib):
 
 
 def test_workspace_size_host_only(lib):
-    # 4-bit K channel-wise / V token-wise: the specialised kernel
-    d = _lib.AttnDesc(_cache(4, 1, 0, pages=128 * 256), 128, 32, 256, 0, 0.0, 304, 0)
+    # a small call (8 x 8 x 32 triples of (sequence, kv head, block)): the specialised kernel
+    d = _lib.AttnDesc(_cache(4, 1, 0, pages=8 * 32), 8, 32, 32, 0, 0.0, 304, 0)
     n = ctypes.c_size_t()
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
     # counters (one per sequence x kv head) + part lse + part out, each 256-byte aligned
-    assert n.value == 128 * 8 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
+    assert n.value == 8 * 8 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
     bad = _lib.AttnDesc(_cache(4), 128, 24, 256, 0, 0.0, 304, 0)  # 3 query heads per KV head: not built
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
     bad = _lib.AttnDesc(_cache(4), 128, 20, 256, 0, 0.0, 304, 0)  # not a multiple of the KV heads
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2
     for hq in (8, 16):  # 1 and 2 query heads per KV head: one unit per KV head
-        d = _lib.AttnDesc(_cache(4, pages=128 * 256), 128, hq, 256, 0, 0.0, 304, 0)
+        d = _lib.AttnDesc(_cache(4, pages=8 * 32), 8, hq, 32, 0, 0.0, 304, 0)
         assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
-        assert n.value == 128 * 8 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
+        assert n.value == 8 * 8 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
     d = _lib.AttnDesc(_cache(4, pages=8 * 32), 8, 64, 32, 0, 0.0, 304, 0)  # 8, small call: two units per KV head
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
     assert n.value == 8 * 16 * 4 + 304 * 2 * 4 * 4 + 304 * 2 * 4 * 128 * 4
@@ -155,38 +155,35 @@ def _spec_ws(batch, units, ctas):
 
 
 def test_default_geometry_routing_host_only(lib):
-    """E4M3 operands at head dim 128, groups of 128: the calls the general
-    kernel runs faster (8 query heads per KV head; 2-bit codes unless K is
-    channel-wise and V token-wise; 4-bit codes with K token-wise and V
-    channel-wise) take it once they hold at least 32,768 (sequence, unit,
-    block) triples; the rest, smaller calls and the E2M1 V placement take the
-    specialised kernel.  Read from the workspace each layout needs."""
+    """E4M3 operands at head dim 128, groups of 128: every call holding at
+    least 8,192 (sequence, unit, block) triples of max_blocks per unit takes
+    the general kernel, whatever its scheme pair and query heads per KV head;
+    smaller calls and the E2M1 V placement take the specialised kernel.  Read
+    from kvq_decode_path and from the workspace each layout needs."""
     n = ctypes.c_size_t()
-    big = dict(batch=128, max_blocks=256)  # 128 x 8 x 256 = 262,144 triples
-    cases = [  # (bits, k, v, q heads, expected kernel)
-        (2, 0, 0, 32, "general"), (2, 0, 1, 32, "general"), (2, 1, 1, 32, "general"), (2, 1, 0, 32, "spec"),
-        (4, 0, 1, 32, "general"), (4, 1, 0, 32, "spec"), (4, 0, 0, 32, "spec"), (4, 1, 1, 32, "spec"),
-        (4, 1, 0, 64, "general"), (2, 0, 0, 64, "general"), (2, 0, 0, 16, "spec"), (2, 0, 0, 8, "spec"),
-    ]
     path = ctypes.c_int32()
-    for bits, k, v, hq, want in cases:
-        d = _lib.AttnDesc(_cache(bits, k, v, pages=128 * 256), big["batch"], hq, big["max_blocks"], 0, 0.0, 304, 0)
-        assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
-        assert lib.kvq_decode_path(ctypes.byref(d), ctypes.byref(path)) == 0
-        assert path.value == (_lib.PATH_GENERAL if want == "general" else _lib.PATH_SPECIALISED), (bits, k, v, hq)
-        g = hq // 8
-        if want == "general":
-            units = 8 * 128
-            splits = -(-304 // units)
-            assert n.value == _general_ws(128, units, splits, 8 if g == 8 else 4, 128), (bits, k, v, hq)
-        else:
-            units = 16 if g == 8 else 8
-            assert n.value == _spec_ws(128, units, 304), (bits, k, v, hq)
-    # the same pairs in a small call (8 x 8 x 32 = 2,048 triples) stay specialised
-    for bits, k, v in ((2, 0, 0), (4, 0, 1)):
+    for bits in (2, 4):
+        for k in (0, 1):
+            for v in (0, 1):
+                for hq in (8, 16, 32, 64):
+                    g = hq // 8
+                    d = _lib.AttnDesc(_cache(bits, k, v, pages=128 * 256), 128, hq, 256, 0, 0.0, 304, 0)
+                    assert lib.kvq_decode_path(ctypes.byref(d), ctypes.byref(path)) == 0
+                    assert path.value == _lib.PATH_GENERAL, (bits, k, v, hq)
+                    assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
+                    units = 8 * 128  # one unit per KV head (8 heads: one 8-head unit)
+                    assert n.value == _general_ws(128, units, 1, 8 if g == 8 else min(g, 4), 128), (bits, k, v, hq)
+    # the threshold: 32 x 16 units x 16 blocks = 8,192 triples (8 heads) -> general, one block less -> specialised
+    for mb, want in ((16, _lib.PATH_GENERAL), (15, _lib.PATH_SPECIALISED)):
+        d = _lib.AttnDesc(_cache(2, 1, 0, pages=32 * 16), 32, 64, mb, 0, 0.0, 304, 0)
+        assert lib.kvq_decode_path(ctypes.byref(d), ctypes.byref(path)) == 0 and path.value == want, mb
+    # a small call (8 x 8 x 32 = 2,048 triples) stays specialised
+    for bits, k, v in ((2, 0, 0), (4, 1, 0)):
         d = _lib.AttnDesc(_cache(bits, k, v, pages=8 * 32), 8, 32, 32, 0, 0.0, 304, 0)
         assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0
         assert n.value == _spec_ws(8, 8, 304)
+        assert lib.kvq_decode_path(ctypes.byref(d), ctypes.byref(path)) == 0
+        assert path.value == _lib.PATH_SPECIALISED
     # the E2M1 V placement: specialised at any size
     d = _lib.AttnDesc(_cache(2, 0, 0, pages=128 * 256), 128, 32, 256, 0, 0.0, 304, _lib.FLAG_E2M1_V)
     assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 0

@@ -178,7 +178,7 @@ def rotation_sets(w, seed) -> int:
 KERNEL_SPECIALISED = "kvq::decode_kernel"
 KERNEL_GENERAL = "kvq::decode_general_kernel (+ plan and merge kernels)"
 SPLIT_SPECIALISED = "persistent CTAs cut the tile order into equal ranges; cut units are merged in the kernel"
-SPLIT_GENERAL = ("a one-CTA plan cuts each unit's blocks into ranges in proportion to its sequence's length; "
+SPLIT_GENERAL = ("a plan kernel cuts each unit's blocks into ranges in proportion to its sequence's length; "
                  "one range per CTA; a log-sum-exp merge kernel combines the ranges")
 
 

@@ -7,9 +7,12 @@ namespace kvq {
 
 namespace {
 
-// The plan of a call, once: one CTA of 1024 threads (a thread per sequence)
-// computes gen_plan and writes the prefix and every decode CTA's assignment.
+// The plan of a call: every CTA of 1024 threads (a thread per sequence)
+// computes gen_plan in its own shared memory -- a few microseconds, no
+// exchange between CTAs -- and writes the assignments of its own 1024 decode
+// CTAs; the first CTA also writes the prefix and reports bad lengths.
 constexpr int kPlanThreads = 1024;
+constexpr int kPlanMaxCtas = 64;  // more decode CTAs than 64 x 1024: the CTAs loop
 
 __global__ void __launch_bounds__(kPlanThreads) general_plan_kernel(const GenParams p, long long grid, int4* assign,
                                                                     int* plan_ps) {
@@ -19,12 +22,15 @@ __global__ void __launch_bounds__(kPlanThreads) general_plan_kernel(const GenPar
   gen::gen_plan<kPlanThreads>(p.seq_lens, p.batch, p.max_blocks, p.units_per_seq, p.n_target, p.n_floor, ps, lens,
                               red);
   const int tid = threadIdx.x;
-  for (int b = tid; b < p.batch; b += kPlanThreads) {
-    const int len = p.seq_lens[b];
-    if (len < 0 || len > p.max_blocks * kBlockTokens) report(p.dev_status, KVQ_DEV_BAD_SEQ_LEN);
+  if (blockIdx.x == 0) {
+    for (int b = tid; b < p.batch; b += kPlanThreads) {
+      const int len = p.seq_lens[b];
+      if (len < 0 || len > p.max_blocks * kBlockTokens) report(p.dev_status, KVQ_DEV_BAD_SEQ_LEN);
+    }
+    for (int b = tid; b <= p.batch; b += kPlanThreads) plan_ps[b] = ps[b];
   }
-  for (int b = tid; b <= p.batch; b += kPlanThreads) plan_ps[b] = ps[b];
-  for (long long c = tid; c < grid; c += kPlanThreads) {
+  const long long step = (long long)gridDim.x * kPlanThreads;
+  for (long long c = (long long)blockIdx.x * kPlanThreads + tid; c < grid; c += step) {
     int4 a = make_int4(-1, 0, 0, 0);
     if (c < ps[p.batch]) {
       const int b = gen::gen_find(ps, p.batch, (int)c);
@@ -81,7 +87,9 @@ __global__ void __launch_bounds__(kMergeThreads) general_merge_kernel(const GenP
 }  // namespace
 
 cudaError_t launch_general_plan(const GenParams& p, long long grid, int4* assign, int* plan_ps, cudaStream_t stream) {
-  general_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, grid, assign, plan_ps);
+  const long long ctas = (grid + kPlanThreads - 1) / kPlanThreads;
+  general_plan_kernel<<<(int)(ctas < 1 ? 1 : (ctas > kPlanMaxCtas ? kPlanMaxCtas : ctas)), kPlanThreads, 0, stream>>>(
+      p, grid, assign, plan_ps);
   return cudaGetLastError();
 }
 
@@ -131,7 +139,7 @@ GenLaunch general_launch_shape(int bits, int k_scheme, int v_scheme, int head_di
   // deepest copy ring (4 stages at most) that keeps the CTAs tensor memory allows
   for (;;) {
     r.stages = 0;
-    for (int st = 4; st >= 2; --st)
+    for (int st = 4; st >= (gen_single_stage(bits, head_dim, group, kcw, vcw, bf16, nh) ? 1 : 2); --st)
       if (fits(r.ctas_per_sm, st)) { r.stages = st; break; }
     if (r.stages != 0 || r.ctas_per_sm == 1) break;
     --r.ctas_per_sm;

@@ -223,7 +223,7 @@ KVQ_API kvq_status kvq_decode_path(const kvq_attn_desc* desc, int32_t* path);
  * work over persistent CTAs in equal tile ranges; a sequence/head cut
  * between CTAs is merged on the device by log-sum-exp; its units take up to
  * 4 query heads, so with 8 query heads per KV head it reads each KV block
- * twice.  The general one runs three launches -- a one-CTA plan cuts each
+ * twice.  The general one runs three launches -- a plan kernel cuts each
  * (sequence, unit)'s blocks into ranges in proportion to the sequence's
  * length, a second kernel decodes one range per CTA (units of 4 or 8 query
  * heads: each KV block is read once), and a log-sum-exp merge combines the

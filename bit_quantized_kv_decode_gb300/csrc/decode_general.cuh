@@ -89,16 +89,17 @@ __device__ __forceinline__ float warp_reduce_t(float (&v)[N]) {
   }
   return r;
 }
-// ... and the per-warp results into buf[warp][N] (one lane per value).
+// ... and the per-warp results into buf[N][4] (value-major: one 16-byte row
+// of the 4 warps' results per value, read back with one vector load).
 template <int N, bool MAX>
 __device__ __forceinline__ void warp_reduce_store(float (&v)[N], float* buf) {
   constexpr int kLog = N == 1 ? 0 : N == 2 ? 1 : N == 4 ? 2 : N == 8 ? 3 : N == 16 ? 4 : 5;
   const float r = warp_reduce_t<N, MAX>(v);
   const int lane = threadIdx.x & 31;
-  if ((lane & ((32 >> kLog) - 1)) == 0) buf[(threadIdx.x >> 5) * N + (lane >> (5 - kLog))] = r;
+  if ((lane & ((32 >> kLog) - 1)) == 0) buf[(lane >> (5 - kLog)) * 4 + (threadIdx.x >> 5)] = r;
   __syncwarp();
 }
-// The per-warp maxima of N values into buf[warp][N]: one redux.sync.max.f32
+// The per-warp maxima of N values into buf[N][4]: one redux.sync.max.f32
 // per value (independent instructions whose latencies overlap, where the
 // butterfly above chains log2(32) exchanges), lane i storing value i.
 template <int N>
@@ -111,7 +112,7 @@ __device__ __forceinline__ void warp_max_store(const float (&v)[N], float* buf) 
     const float r = warp_max_redux(v[i]);
     mine = lane == i ? r : mine;
   }
-  if (lane < N) buf[(threadIdx.x >> 5) * N + lane] = mine;
+  if (lane < N) buf[lane * 4 + (threadIdx.x >> 5)] = mine;
   __syncwarp();
 }
 // Largest of D non-negative fp16 values in shared memory (bits; they order as
@@ -131,14 +132,16 @@ __device__ __forceinline__ uint32_t max_f16_bits(const uint16_t* v) {
   }
   return __reduce_max_sync(FULL, max(m & 0xffffu, m >> 16));
 }
-// Block-wide result i from buf[4][N] (after a barrier).
+// Block-wide result i from buf[N][4] (after a barrier): one 16-byte load.
 template <int N>
 __device__ __forceinline__ float sum4(const float* buf, int i) {
-  return (buf[i] + buf[N + i]) + (buf[2 * N + i] + buf[3 * N + i]);
+  const float4 v = reinterpret_cast<const float4*>(buf)[i];
+  return (v.x + v.y) + (v.z + v.w);
 }
 template <int N>
 __device__ __forceinline__ float max4(const float* buf, int i) {
-  return fmaxf(fmaxf(buf[i], buf[N + i]), fmaxf(buf[2 * N + i], buf[3 * N + i]));
+  const float4 v = reinterpret_cast<const float4*>(buf)[i];
+  return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
 }
 
 // Thread 0 waits (bounded) for the phase; the whole CTA learns the outcome,
@@ -321,9 +324,9 @@ decode_general_kernel(const GenParams p, int stages) {
 
   unsigned char* qop = smem + L.q_off;  // [D rows][NBQ blocks]
   unsigned char* pop = smem + L.p_off;  // [128 rows][NBP blocks]
-  float* red_c = reinterpret_cast<float*>(smem + L.scratch_off);  // [4][32] q . z_g (channel-wise K)
-  float* red_m = red_c + 128;                                     // [4][16] block maxima
-  float* red_z = red_m + 64;                                      // [2][4][32] per-group p (z) sums
+  float* red_c = reinterpret_cast<float*>(smem + L.scratch_off);  // [32][4 warps] q . z_g (channel-wise K)
+  float* red_m = red_c + 128;                                     // [16][4] block maxima
+  float* red_z = red_m + 64;                                      // [2][32][4] per-group p (z) sums
   float* qsz_s = red_z + 256;                                     // [8][8] token-wise K q sums (NH = 8)
   uint64_t* bars = reinterpret_cast<uint64_t*>(qsz_s + 64 + 16);  // stages [4], mma, drain
   uint32_t* tbase = reinterpret_cast<uint32_t*>(bars + 6);
@@ -626,7 +629,7 @@ decode_general_kernel(const GenParams p, int stages) {
                                       p.minus_one);
 
     // ---- online softmax over the block: block maxima (and the largest V scale)
-    {  // red_m[warp][NM]: value k < NH the head maxima, NM - 1 the largest V scale
+    {  // red_m[NM][warp]: value k < NH the head maxima, NM - 1 the largest V scale
       const int lane = tid & 31;
       float mine = 0.f;
 #pragma unroll
@@ -638,7 +641,7 @@ decode_general_kernel(const GenParams p, int stages) {
         const float r = warp_max_redux(vmax);
         mine = lane == NM - 1 ? r : mine;
       }
-      if (lane < NM) red_m[warp * NM + lane] = mine;
+      if (lane < NM) red_m[lane * 4 + warp] = mine;
       __syncwarp();
     }
     tc_wait_st();
@@ -770,7 +773,7 @@ decode_general_kernel(const GenParams p, int stages) {
                 float psum = 0.f;  // sum of p over the group's tokens (the warps covering them)
 #pragma unroll
                 for (int w = 0; w < 4; ++w)
-                  if ((32 * w) / G == g) psum += red_z[w * NZ + k];
+                  if ((32 * w) / G == g) psum += red_z[k * 4 + w];
                 add[k] = fmaf(s_gc, parts<BF16>(v, h) * pinv[k], fmaf(z_gc, psum, add[k]));
               }
             }
@@ -811,7 +814,7 @@ decode_general_kernel(const GenParams p, int stages) {
       for (int k = 0; k < NH; ++k) t[k] = l_thr[k];
       warp_reduce_store<NH, false>(t, red_m);
     }
-    if (kZp) {  // the range's sum of p * z per channel group and head: red_z[warp][g * NH + k]
+    if (kZp) {  // the range's sum of p * z per channel group and head: red_z[g * NH + k][warp]
       constexpr int NP = kZp ? NGC * NH : 1;
       float t[NP];
 #pragma unroll

@@ -515,8 +515,8 @@ decode_general_kernel(const GenParams p, int stages) {
 #pragma unroll
       for (int g = 0; g < NGT; ++g) e16[g] = f16_exp_field(max_f16_bits<D>(ksz + g * D));
     }
+    float t[KCW ? NH * NGT : 1];  // channel-wise K: q . z_g (this thread's channels), value g * NH + k
     if (KCW) {
-      float t[NH * NGT];  // q . z_g, value g * NH + k
 #pragma unroll
       for (int k = 0; k < NH * NGT; ++k) t[k] = 0.f;
 #pragma unroll
@@ -540,7 +540,6 @@ decode_general_kernel(const GenParams p, int stages) {
           }
         }
       }
-      warp_reduce_store<NH * NGT, false>(t, red_c);
       fence_proxy_async_smem();
     }
 
@@ -563,7 +562,10 @@ decode_general_kernel(const GenParams p, int stages) {
       }
       tc_commit(mma_bar);
     }
-    // while QK^T runs: the largest V scale of this token (token-wise V)
+    // while QK^T runs: the warps' sums of q . z_g (channel-wise K; read after
+    // the barrier that ends the wait for QK^T) and the largest V scale of
+    // this token (token-wise V)
+    if (KCW) warp_reduce_store<KCW ? NH * NGT : 1, false>(t, red_c);
     float vmax = 0.f;
     if (!VCW && valid) {
 #pragma unroll

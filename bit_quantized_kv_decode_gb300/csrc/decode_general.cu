@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(kPlanThreads) general_plan_kernel(const GenPar
   __shared__ int ps[kGenPlanInts];
   __shared__ long long red[kPlanThreads / 32];
   int* lens = ps + p.batch + 1;
+  gen::grid_dep_launch();  // the decode kernel may launch now; it waits for this grid before reading the plan
   gen::gen_plan<kPlanThreads>(p.seq_lens, p.batch, p.max_blocks, p.units_per_seq, p.n_target, p.n_floor, ps, lens,
                               red);
   const int tid = threadIdx.x;
@@ -51,6 +52,7 @@ constexpr int kMergeThreads = 256;
 
 __global__ void __launch_bounds__(kMergeThreads) general_merge_kernel(const GenParams p, int head_dim, float* out,
                                                                       float* lse) {
+  gen::grid_dep_wait();  // the decode kernel's parts (this kernel may start while it finishes)
   const int lane = threadIdx.x & 31;
   const int row = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);
   if (row >= p.batch * p.num_q_heads) return;
@@ -59,6 +61,33 @@ __global__ void __launch_bounds__(kMergeThreads) general_merge_kernel(const GenP
   const int p0 = p.plan_ps[b], p1 = p.plan_ps[b + 1];
   const int nr = (p1 - p0) / p.units_per_seq;  // ranges (parts) of the row's unit
   const int c0 = p0 + uh * nr;
+  float* dst = out + (size_t)row * head_dim;
+  if (nr <= 32) {  // one part per lane: its weight computed once, broadcast by shuffles
+    const float ls = lane < nr ? p.part_lse[(size_t)(c0 + lane) * p.gq + k] : -INFINITY;
+    float m = ls;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+    const float e = lane < nr ? expf(ls - m) : 0.f;
+    float tot = e;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
+    const float w = nr > 0 ? e / tot : 0.f;
+    for (int d = lane * 4; d < head_dim; d += 128) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int s = 0; s < nr; ++s) {
+        const float ws = __shfl_sync(FULL, w, s);
+        const float4 v = *reinterpret_cast<const float4*>(p.part_o + ((size_t)(c0 + s) * p.gq + k) * head_dim + d);
+        acc.x = fmaf(ws, v.x, acc.x);
+        acc.y = fmaf(ws, v.y, acc.y);
+        acc.z = fmaf(ws, v.z, acc.z);
+        acc.w = fmaf(ws, v.w, acc.w);
+      }
+      *reinterpret_cast<float4*>(dst + d) = acc;
+    }
+    if (lane == 0) lse[row] = nr > 0 ? m + logf(tot) : -INFINITY;
+    return;
+  }
   float m = -INFINITY;
   for (int s = lane; s < nr; s += 32) m = fmaxf(m, p.part_lse[(size_t)(c0 + s) * p.gq + k]);
 #pragma unroll
@@ -67,8 +96,7 @@ __global__ void __launch_bounds__(kMergeThreads) general_merge_kernel(const GenP
   for (int s = lane; s < nr; s += 32) tot += expf(p.part_lse[(size_t)(c0 + s) * p.gq + k] - m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULL, tot, o);
-  const float inv = nr > 0 ? 1.0f / tot : 0.f;
-  float* dst = out + (size_t)row * head_dim;
+  const float inv = 1.0f / tot;
   for (int d = lane * 4; d < head_dim; d += 128) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s = 0; s < nr; ++s) {
@@ -97,8 +125,16 @@ cudaError_t launch_general_merge(const GenParams& p, int head_dim, float* out, f
   const int rows = p.batch * p.num_q_heads;
   if (rows == 0) return cudaSuccess;
   constexpr int kRows = kMergeThreads / 32;
-  general_merge_kernel<<<(rows + kRows - 1) / kRows, kMergeThreads, 0, stream>>>(p, head_dim, out, lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + kRows - 1) / kRows));
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_instance
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, general_merge_kernel, p, head_dim, out, lse);
 }
 
 cudaError_t launch_general_d64(int bits, bool kcw, bool vcw, int group, const GenParams& p, int grid,

@@ -115,6 +115,14 @@ __device__ __forceinline__ void warp_max_store(const float (&v)[N], float* buf) 
   if (lane < N) buf[lane * 4 + (threadIdx.x >> 5)] = mine;
   __syncwarp();
 }
+// Programmatic dependent launch (sm_90+): a kernel launched with the
+// programmatic-serialization attribute may start while the kernel before it
+// in the stream still runs; grid_dep_wait() blocks until that kernel has
+// completed and its memory is visible (a no-op without the attribute), and
+// grid_dep_launch() lets the next such kernel start launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Largest of D non-negative fp16 values in shared memory (bits; they order as
 // integers), computed by each warp on its own: no cross-warp exchange.
 template <int D>
@@ -335,6 +343,8 @@ decode_general_kernel(const GenParams p, int stages) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
   const int cta = blockIdx.x;
+  grid_dep_wait();    // the plan kernel's assignments (this kernel may start while it runs)
+  grid_dep_launch();  // the merge kernel may launch (it waits for this grid to complete)
   const int4 asg = p.assign[cta];  // written by general_plan_kernel: {b | unit << 16, j0, j1, length}
   if (asg.x < 0) return;           // no work left for this CTA
   const int b = asg.x & 0xffff, uh = asg.x >> 16, kvh = uh >> p.kv_shift;
@@ -875,8 +885,19 @@ cudaError_t launch_instance(const GenParams& p, int grid, const GenLaunch& shape
   auto kern = decode_general_kernel<BITS, KCW, VCW, D, G, BF16, NH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)shape.smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, shape.smem, stream>>>(p, shape.stages);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs start while the plan kernel runs
+  // and wait for it in the kernel (grid_dep_wait)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = shape.smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p, (int)shape.stages);
 }
 
 template <int BITS, int D, int G, bool BF16, int NH>

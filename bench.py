@@ -357,14 +357,18 @@ def profile_traffic(workload: str, general: bool = False):
 
 
 def kernel_source_hash(general: bool = False):
-    """SHA-256 of the sources a decode kernel is compiled from."""
+    """SHA-256 of the sources a decode kernel is compiled from, line comments
+    and trailing blanks removed (a change of wording is not a new kernel)."""
+    import re
     names = ("decode.cuh", "kvq_ptx.cuh", "kvq_internal.h")
     if general:
         names = ("decode_general.cuh", "decode_general.h") + names
     h = hashlib.sha256()
     for name in names:
-        with open(os.path.join(ROOT, "bit_quantized_kv_decode_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "bit_quantized_kv_decode_gb300", "csrc", name), encoding="utf-8") as f:
+            text = f.read()
+        code = "\n".join(line.rstrip() for line in re.sub(r"//[^\n]*", "", text).splitlines() if line.strip())
+        h.update(code.encode("utf-8"))
     return h.hexdigest()
 
 

@@ -13,6 +13,10 @@
 //    as q*2^-9.  Section "限界と未検証の範囲": accumulator folds are applied one
 //    quantization group at a time.
 //
+// kvq_decode_attn runs this kernel for small calls (its persistent CTAs start
+// faster) and for the E2M1 V placement; calls of real size take the
+// block-range kernel of decode_general.cuh, measured faster there.
+//
 // GB300 design (this library's; the pages' Blackwell pipeline is prior art):
 //  * swap-AB MMAs: tokens (QK^T) or channels (PV) are the M = 128 rows, the
 //    4 GQA query heads x operand splits are N = 16 columns;

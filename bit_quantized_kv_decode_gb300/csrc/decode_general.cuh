@@ -1,6 +1,8 @@
-// Decode attention for the cache geometries the specialised kernel does not
-// take: head dims 64 and 256, groups of 32 or 64 elements (with any head
-// dim).  One warpgroup per CTA runs every step of a 128-token block in turn
+// Decode attention for every cache geometry (head dims 64, 128 and 256,
+// groups of 32, 64 or 128 elements) and both operand modes; the host sends
+// it every call of real size (the specialised kernel of decode.cuh keeps
+// small calls and the E2M1 V placement).  One warpgroup per CTA runs every
+// step of a 128-token block in turn
 // -- bulk copies into a ring of stages, codes to E4M3 operands in tensor
 // memory, Q' and P' operands in shared memory, tcgen05 MMAs with the
 // accumulators in tensor memory, the affine folds and an online softmax --

@@ -49,3 +49,18 @@ def test_general_kernel_default_geometry_ranges(num_ctas):
     res = run_gpu(pb, num_ctas=num_ctas)
     assert res["status"] == 0
     assert_attention_close(pb, res, 0)
+
+
+@pytest.mark.parametrize("bits,kcw,vcw", [(4, 1, 0), (2, 0, 0)])
+def test_general_kernel_default_geometry_stall_reports_timeout(bits, kcw, vcw):
+    """A withheld copy (test hook: the first CTA skips its first block) makes
+    that CTA's bounded wait run out: the call returns with KVQ_DEV_TIMEOUT set,
+    nothing hangs, and the next call is correct (a 4-bit and a 2-bit instance,
+    whose copy rings refill at different points of a block)."""
+    import bit_quantized_kv_decode_gb300 as kvq
+    pb = make_problem(_workload(bits, kcw, vcw, 4), seed=970 + bits, lens=LENS)
+    res = run_gpu(pb, flags=kvq.FLAG_TEST_STALL)
+    assert res["status"] & kvq.DEV_TIMEOUT
+    again = run_gpu(pb)
+    assert again["status"] == 0
+    assert_attention_close(pb, again, 0)

@@ -514,19 +514,24 @@ decode_general_kernel(const GenParams p, int stages) {
     const int l = tid;
     const bool valid = l < nv;
 
+    // ---- channel-wise K: the largest scale of each group (the E4M3 Q'
+    //      prescale), found by every warp on its own; with one token group
+    //      ahead of the K conversion, which hides its latency (with several,
+    //      after it: the values held across it cost more than they hide)
+    uint32_t e16[KCW && !BF16 ? NGT : 1];
+    auto group_maxima = [&]() {
+#pragma unroll
+      for (int g = 0; g < (KCW && !BF16 ? NGT : 1); ++g) e16[g] = f16_exp_field(max_f16_bits<D>(ksz + g * D));
+    };
+    if (KCW && !BF16 && NGT == 1) group_maxima();
+
     // ---- K codes -> E4M3 operand (rows = tokens)
     __syncwarp();
     convert_row<BITS, BF16, D * BITS / 128>(st, kBlockTokens, tid, t_a, p.nibble_mul, p.minus_one);
     tc_wait_st();
+    if (KCW && !BF16 && NGT > 1) group_maxima();
 
-    // ---- channel-wise K: Q'_g = q * s_g per token group g, and q . z_g;
-    //      the largest scale of each group (the E4M3 Q' prescale), found by
-    //      every warp on its own
-    uint32_t e16[KCW && !BF16 ? NGT : 1];
-    if (KCW && !BF16) {
-#pragma unroll
-      for (int g = 0; g < NGT; ++g) e16[g] = f16_exp_field(max_f16_bits<D>(ksz + g * D));
-    }
+    // ---- channel-wise K: Q'_g = q * s_g per token group g, and q . z_g
     float t[KCW ? NH * NGT : 1];  // channel-wise K: q . z_g (this thread's channels), value g * NH + k
     if (KCW) {
 #pragma unroll
@@ -546,7 +551,7 @@ decode_general_kernel(const GenParams p, int stages) {
               *reinterpret_cast<uint4*>(qop + b_off<BF16>(a_pos<BITS, BF16>(c), g * HH + hq, NBQ)) =
                   BF16 ? split2_bf16(v) : split3_e4m3(v);
             }
-            const float zgc = h2f(kzz[g * D + c]);
+            const float zgc = h2f(kzz[g * D + c]) * p.sm_scale_log2;  // the offsets in log2 score units
 #pragma unroll
             for (int k = 0; k < NH; ++k) t[g * NH + k] = fmaf(qv[k][i], zgc, t[g * NH + k]);
           }
@@ -605,7 +610,7 @@ decode_general_kernel(const GenParams p, int stages) {
         ld_block<BF16>(t_so + 16 * (g * HH + hq), v);
         float cz[4];
 #pragma unroll
-        for (int h = 0; h < 4; ++h) cz[h] = sum4<NH * NGT>(red_c, g * NH + 4 * hq + h) * p.sm_scale_log2;
+        for (int h = 0; h < 4; ++h) cz[h] = sum4<NH * NGT>(red_c, g * NH + 4 * hq + h);
         tc_wait_ld();
 #pragma unroll
         for (int h = 0; h < 4; ++h) sc[4 * hq + h] = fmaf(parts<BF16>(v, h), mult[4 * hq + h] * fs, cz[h]);

@@ -228,13 +228,11 @@ KVQ_API kvq_status kvq_decode_path(const kvq_attn_desc* desc, int32_t* path);
  * length, a second kernel decodes one range per CTA (units of 4 or 8 query
  * heads: each KV block is read once), and a log-sum-exp merge combines the
  * ranges.  The general kernel takes every other geometry (head dim 64 / 256,
- * groups of 32 / 64) and the BF16 mode, and, on the specialised kernel's
- * geometry in E4M3, the calls it runs faster: 8 query heads per KV head; 4
- * with 2-bit codes unless K is channel-wise and V token-wise; 4 with 4-bit
- * codes, K token-wise and V channel-wise -- each only when batch x units x
- * max_blocks >= 32768 (units per sequence: the KV heads, twice that with 8
- * query heads per KV head); smaller calls, other head counts (1, 2) and
- * KVQ_FLAG_E2M1_V stay in the specialised kernel.  KVQ_FLAG_E2M1_V on
+ * groups of 32 / 64) and the BF16 mode, and on the specialised kernel's
+ * geometry (E4M3) every call with batch x units x max_blocks >= 8192 (units
+ * per sequence: the KV heads, twice that with 8 query heads per KV head),
+ * where it was measured faster for every scheme pair and head count; smaller
+ * calls and KVQ_FLAG_E2M1_V stay in the specialised kernel.  KVQ_FLAG_E2M1_V on
  * another geometry or in the BF16 mode: KVQ_ERR_UNSUPPORTED.  Query heads
  * per KV head: 1, 2, 4 or 8.  sm_scale <= 0 means 1 / sqrt(head_dim).
  *   q        bf16 [batch][num_q_heads][head_dim]

@@ -338,7 +338,7 @@ decode_general_kernel(const GenParams p, int stages) {
   float* red_m = red_c + 128;                                     // [16][4] block maxima
   float* red_z = red_m + 64;                                      // [2][32][4] per-group p (z) sums
   float* qsz_s = red_z + 256;                                     // [8][8] token-wise K q sums (NH = 8)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qsz_s + 64 + 16);  // stages [4], mma, drain
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qsz_s + 64 + 16);  // (16 spare floats) stages [4], mma, drain
   uint32_t* tbase = reinterpret_cast<uint32_t*>(bars + 6);
   int* ok_flag = reinterpret_cast<int*>(tbase + 1);
 

@@ -317,10 +317,10 @@ decode_general_kernel(const GenParams p, int stages) {
   constexpr int NM = VCW ? NH : 2 * NH;                 // block-max reduction: heads (+ largest V scale)
   constexpr int NZ = VCW ? NH : 4 * NGC;                // per-group p sums (token-wise V: one quad at a time)
   constexpr bool kQszSmem = NH > 4;                     // token-wise K's q sums in shared memory
-  // token-wise V with few (group, head) pairs: each thread keeps its token's
-  // running sum of p * z per channel group and head, reduced once per range
-  // (else the per-group sums are reduced across the CTA at every block)
-  constexpr bool kZp = !VCW && NGC * NH <= 8;
+  // token-wise V with up to 16 (group, head) pairs: each thread keeps its
+  // token's running sum of p * z per channel group and head, reduced once per
+  // range (else the per-group sums are reduced across the CTA at every block)
+  constexpr bool kZp = !VCW && NGC * NH <= 16;
   extern __shared__ __align__(1024) unsigned char smem[];
   const GenLayout L = gen_layout(BITS, D, G, KCW, VCW, BF16, NH, stages);  // shared-memory offsets
   constexpr GenLayout LT = gen_layout(BITS, D, G, KCW, VCW, BF16, NH, 2);  // tensor-memory columns

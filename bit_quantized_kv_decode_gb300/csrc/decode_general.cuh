@@ -154,17 +154,28 @@ __device__ __forceinline__ float max4(const float* buf, int i) {
   return fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
 }
 
-// Thread 0 waits (bounded) for the phase; the whole CTA learns the outcome,
-// so that a wait that runs out leaves every thread on the same path.  Ends
-// with the warp converged: the tcgen05.ld / st that follow are .sync.aligned
+// A wait that runs out sets the CTA's sticky `fail` word in shared memory;
+// every thread reads it after the next CTA barrier, so that all of them leave
+// the block loop at the same barrier.  (A plain barrier and a shared word:
+// the barrier-reduction form, __syncthreads_and, measured 2-5% slower.)
+//
+// Thread 0 waits (bounded) for the phase, then the CTA barrier.  Ends with
+// the warp converged: the tcgen05.ld / st that follow are .sync.aligned
 // (every lane of the warp must execute them together).
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, int* ok_flag, uint64_t limit) {
-  if (threadIdx.x == 0) *ok_flag = mbar_wait_bounded(bar, parity, nullptr, limit) ? 1 : 0;
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, volatile int* fail, uint64_t limit) {
+  if (threadIdx.x == 0 && !mbar_wait_bounded(bar, parity, nullptr, limit)) *fail = 1;
   __syncthreads();
-  const bool ok = *ok_flag != 0;
+  const bool ok = *fail == 0;
   if (ok) (void)mbar_try_wait(bar, parity);  // completed: observe it in every thread
   __syncwarp();
   return ok;
+}
+// Every lane of the warp waits (bounded) for the phase, without a CTA
+// barrier (each warp then reads only its own lanes of the accumulator); a
+// wait that runs out sets `fail`, read after the next CTA barrier.
+__device__ __forceinline__ void warp_wait(uint64_t* bar, uint32_t parity, volatile int* fail, uint64_t limit) {
+  const bool ok = mbar_wait_bounded(bar, parity, nullptr, limit);
+  if (!__all_sync(FULL, ok)) *fail = 1;
 }
 
 // Codes of `CHUNKS` 16-byte chunks of row `row` (chunk-major block layout
@@ -325,22 +336,30 @@ decode_general_kernel(const GenParams p, int stages) {
   const GenLayout L = gen_layout(BITS, D, G, KCW, VCW, BF16, NH, stages);  // shared-memory offsets
   constexpr GenLayout LT = gen_layout(BITS, D, G, KCW, VCW, BF16, NH, 2);  // tensor-memory columns
   constexpr bool kSeq = LT.seq_halves;
-  // 4-bit E4M3 codes with token-wise V: the next copy into a stage goes out
-  // as PV starts (nothing reads the stage after that barrier) rather than at
-  // the end of the block (+0.5% INT4 K-cw/V-tw, +1-2% at head dim 256; 2-bit
-  // codes measured 0.3% and the BF16 mode 2.8% slower, so they keep the
-  // refill at the end)
-  constexpr bool kEarlyRefill = !VCW && BITS == 4 && !BF16 && !kSeq;
+  // Refills: the next copy into a stage goes out as PV starts (nothing reads
+  // the stage after that barrier; with channel-wise V and one token group per
+  // channel half, kVPre, the epilogue's V scales and offsets are read into
+  // registers before it), and no CTA barrier ends the block (the next
+  // block's copy wait is the one); the other channel-wise V instances refill
+  // after a barrier at the end of the block.  A thread of the last warp
+  // issues the refills: thread 0 issues the MMAs and waits for the copies,
+  // and a refill on its path delays every warp (measured, refills moved off
+  // thread 0: +4.7 points of the peak on INT4 K-cw/V-tw, +3.3 on INT2
+  // K-/V-token-wise; early refills for channel-wise V: +2-5).
+  constexpr bool kVPre = VCW && NGT * kHalves <= 2;
+  constexpr bool kEarlyRefill = !VCW || kVPre;
+  constexpr int kRefillTid = kThreads - 32;
 
   unsigned char* qop = smem + L.q_off;  // [D rows][NBQ blocks]
   unsigned char* pop = smem + L.p_off;  // [128 rows][NBP blocks]
   float* red_c = reinterpret_cast<float*>(smem + L.scratch_off);  // [32][4 warps] q . z_g (channel-wise K)
   float* red_m = red_c + 128;                                     // [16][4] block maxima
   float* red_z = red_m + 64;                                      // [2][32][4] per-group p (z) sums
-  float* qsz_s = red_z + 256;                                     // [8][8] token-wise K q sums (NH = 8)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qsz_s + 64 + 16);  // (16 spare floats) stages [4], mma, drain
+  float* qsz_s = red_z + 256;  // [8][8] token-wise K q sums (NH = 8); channel-wise K, kMultSmem: the multipliers
+  int* pend = reinterpret_cast<int*>(qsz_s + 64);                 // [4] block whose copy into stage s is in flight
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qsz_s + 64 + 16);  // (12 spare words) stages [4], mma, drain
   uint32_t* tbase = reinterpret_cast<uint32_t*>(bars + 6);
-  int* ok_flag = reinterpret_cast<int*>(tbase + 1);
+  volatile int* fail = reinterpret_cast<volatile int*>(tbase + 1);  // a wait ran out (see cta_wait)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -356,8 +375,7 @@ decode_general_kernel(const GenParams p, int stages) {
   float* part_lse = p.part_lse + (size_t)cta * p.gq;
 
   const uint64_t limit = p.wait_limit_ns;
-  int pend[4] = {-1, -1, -1, -1};  // thread 0: block whose copy into stage s is in flight
-  auto load = [&](int j, int s) {  // thread 0: block j of the unit into stage s
+  auto load = [&](int j, int s) {  // one thread: block j of the unit into stage s
     int page = p.page_table ? p.page_table[(size_t)b * p.max_blocks + j] : b * p.max_blocks + j;
     if (page < 0 || page >= p.num_pages) {
       report(p.dev_status, KVQ_DEV_BAD_PAGE);
@@ -377,6 +395,8 @@ decode_general_kernel(const GenParams p, int stages) {
     pend[s] = j;
   };
   if (tid == 0) {  // the first copies go out before the rest of the set-up
+    for (int i = 0; i < 4; ++i) pend[i] = -1;
+    *fail = 0;
     for (int i = 0; i < stages + 2; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
     for (int i = 0; i < stages && j0 + i < j1; ++i) {
@@ -430,6 +450,16 @@ decode_general_kernel(const GenParams p, int stages) {
   for (int k = 0; k < NH; ++k)
     mult[k] = BF16 ? p.sm_scale_log2  // exact BF16 codes, no prescale
                    : 512.0f * (KCW ? pow2_head_inv(qmax[k]) : pow2_prescale_inv(qmax[k])) * p.sm_scale_log2;
+  // channel-wise K (E4M3) where registers are short (8 heads at 5 CTAs per
+  // SM, 96 registers a thread; 2-bit codes at 8, 64 a thread): q . z_g is
+  // taken against the prescaled q, so that q itself is not kept, and with 8
+  // heads the multipliers wait in shared memory (the q sums' buffer, unused
+  // by this scheme).  (Measured: 8 heads +2.5-3 points of the peak with 4-bit
+  // codes, +1.3-2.5 with 2-bit; 4 heads 2-bit +1.1-1.5; 4-bit codes with 4
+  // heads, whose registers suffice, lost 2-4 points, the BF16 mode 0-0.2.)
+  constexpr bool kQkZ = KCW && !BF16 && (NH > 4 || BITS == 2);
+  constexpr bool kMultSmem = kQkZ && NH > 4;
+  if (kMultSmem && tid < NH) qsz_s[tid] = mult[tid];
   float qsz[kQszSmem ? 1 : NGC][NH];  // token-wise K: sum of q over channel group g, times the log2 scale
   if (!KCW) {
     // Q' = q * 2^k (k per head) in three E4M3 parts at row a_pos(c), one
@@ -504,7 +534,7 @@ decode_general_kernel(const GenParams p, int stages) {
   uint32_t mma_phase = 0u;
   for (int j = j0; j < j1; ++j) {
     const int s = (j - j0) % stages;
-    if (!cta_wait(&bars[s], (uint32_t)((j - j0) / stages) & 1u, ok_flag, limit)) { ok = false; break; }
+    if (!cta_wait(&bars[s], (uint32_t)((j - j0) / stages) & 1u, fail, limit)) { ok = false; break; }
     const unsigned char* st = smem + s * L.stage_bytes;
     const uint16_t* ksz = reinterpret_cast<const uint16_t*>(st + 2 * kKBytes);
     const uint16_t* kzz = ksz + NSZ;
@@ -551,9 +581,11 @@ decode_general_kernel(const GenParams p, int stages) {
               *reinterpret_cast<uint4*>(qop + b_off<BF16>(a_pos<BITS, BF16>(c), g * HH + hq, NBQ)) =
                   BF16 ? split2_bf16(v) : split3_e4m3(v);
             }
-            const float zgc = h2f(kzz[g * D + c]) * p.sm_scale_log2;  // the offsets in log2 score units
+            // the offsets in log2 score units; or, kQkZ, times 2^-9 against the
+            // prescaled q (the score multiplier holds 2^9 / prescale)
+            const float zgc = h2f(kzz[g * D + c]) * (kQkZ ? 1.0f / 512.0f : p.sm_scale_log2);
 #pragma unroll
-            for (int k = 0; k < NH; ++k) t[g * NH + k] = fmaf(qv[k][i], zgc, t[g * NH + k]);
+            for (int k = 0; k < NH; ++k) t[g * NH + k] = fmaf(kQkZ ? qk[k][i] : qv[k][i], zgc, t[g * NH + k]);
           }
         }
       }
@@ -588,7 +620,16 @@ decode_general_kernel(const GenParams p, int stages) {
 #pragma unroll
       for (int g = 0; g < NGC; ++g) vmax = fmaxf(vmax, h2f(vsz[l * NGC + g]));
     }
-    if (!cta_wait(mma_bar, mma_phase, ok_flag, limit)) { ok = false; break; }
+    // token-wise K: each warp waits for QK^T on its own and reads its lanes
+    // of S (one CTA barrier less per block); channel-wise K waits as a CTA,
+    // which also completes red_c.  (Channel-wise K with per-warp waits, q . z_g
+    // then added after the block-maxima barrier, measured 1-4 points slower.)
+    if (!KCW) {
+      warp_wait(mma_bar, mma_phase, fail, limit);
+    } else if (!cta_wait(mma_bar, mma_phase, fail, limit)) {
+      ok = false;
+      break;
+    }
     mma_phase ^= 1u;
     tc_fence_after();
 
@@ -613,7 +654,11 @@ decode_general_kernel(const GenParams p, int stages) {
         for (int h = 0; h < 4; ++h) cz[h] = sum4<NH * NGT>(red_c, g * NH + 4 * hq + h);
         tc_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 4; ++h) sc[4 * hq + h] = fmaf(parts<BF16>(v, h), mult[4 * hq + h] * fs, cz[h]);
+        for (int h = 0; h < 4; ++h) {
+          const int k = 4 * hq + h;
+          sc[k] = kQkZ ? (kMultSmem ? qsz_s[k] : mult[k]) * fmaf(parts<BF16>(v, h), fs, cz[h])
+                       : fmaf(parts<BF16>(v, h), mult[k] * fs, cz[h]);
+        }
       }
     } else {
 #pragma unroll
@@ -665,6 +710,7 @@ decode_general_kernel(const GenParams p, int stages) {
     }
     tc_wait_st();
     __syncthreads();
+    if (*fail) { ok = false; break; }  // a per-warp QK^T wait ran out
     float bmax[NH];
 #pragma unroll
     for (int k = 0; k < NH; ++k) bmax[k] = max4<NM>(red_m, k);
@@ -734,12 +780,25 @@ decode_general_kernel(const GenParams p, int stages) {
 #pragma unroll
     for (int k = 0; k < NH; ++k) pinv[k] = __uint_as_float((uint32_t)((BF16 ? 121 : 130) + pe[k]) << 23);
 
+    float vpre_s[kVPre ? kHalves : 1][kVPre ? NGT : 1], vpre_z[kVPre ? kHalves : 1][kVPre ? NGT : 1];
+    if (kVPre) {
+#pragma unroll
+      for (int hf = 0; hf < (kVPre ? kHalves : 1); ++hf)
+#pragma unroll
+        for (int g = 0; g < (kVPre ? NGT : 1); ++g) {
+          const int c = hf * 128 + tid;
+          vpre_s[hf][g] = c < D ? h2f(vsz[g * D + c]) : 0.f;
+          vpre_z[hf][g] = c < D ? h2f(vzz[g * D + c]) : 0.f;
+        }
+    }
+
     // ---- PV: O[channel][column block] per M = 128 half of the channels, then
     //      the epilogue: channel c = 128 hf + tid; undo the P' prescale, fold V
 #pragma unroll
     for (int pass = 0; pass < (kSeq ? kHalves : 1); ++pass) {
       tc_fence_before();
       __syncthreads();
+      if (pass > 0 && *fail) { ok = false; break; }  // pass 0's PV wait
       tc_fence_after();
       if (tid == 0) {
 #pragma unroll
@@ -760,12 +819,12 @@ decode_general_kernel(const GenParams p, int stages) {
           }
         }
         tc_commit(mma_bar);
-        if (kEarlyRefill) {  // token-wise V: nothing reads the stage after this barrier
-          pend[s] = -1;
-          if (j + stages < j1) load(j + stages, s);
-        }
       }
-      if (!cta_wait(mma_bar, mma_phase, ok_flag, limit)) { ok = false; break; }
+      if (kEarlyRefill && pass == 0 && tid == kRefillTid) {  // nothing reads the stage after this barrier
+        pend[s] = -1;
+        if (j + stages < j1) load(j + stages, s);
+      }
+      warp_wait(mma_bar, mma_phase, fail, limit);  // each warp reads its own lanes of O
       mma_phase ^= 1u;
       tc_fence_after();
 #pragma unroll
@@ -785,7 +844,8 @@ decode_general_kernel(const GenParams p, int stages) {
               ld_block<BF16>(o + 16 * (g * HH + hq), v);
               tc_wait_ld();
               if (g * G >= nv || c >= D) continue;  // no valid token in this group / no such channel
-              const float s_gc = h2f(vsz[g * D + c]), z_gc = h2f(vzz[g * D + c]);
+              const float s_gc = kVPre ? vpre_s[kVPre ? hf : 0][kVPre ? g : 0] : h2f(vsz[g * D + c]);
+              const float z_gc = kVPre ? vpre_z[kVPre ? hf : 0][kVPre ? g : 0] : h2f(vzz[g * D + c]);
 #pragma unroll
               for (int h = 0; h < 4; ++h) {
                 const int k = 4 * hq + h;
@@ -817,13 +877,20 @@ decode_general_kernel(const GenParams p, int stages) {
       }
     }
     if (!ok) break;
-    tc_fence_before();
-    __syncthreads();  // stage s, Q', P', S / O and the reduction buffers are free again
-    if (tid == 0 && !kEarlyRefill) {
-      pend[s] = -1;
-      if (j + stages < j1) load(j + stages, s);
+    if (!kEarlyRefill) {
+      tc_fence_before();
+      __syncthreads();  // stage s, Q', P', S / O and the reduction buffers are free again
+      if (*fail) { ok = false; break; }
+      if (tid == kRefillTid) {
+        pend[s] = -1;
+        if (j + stages < j1) load(j + stages, s);
+      }
     }
   }
+
+  // the last PV wait's outcome; every refill (and its pend entry) is issued
+  __syncthreads();
+  ok = ok && *fail == 0;
 
   // ---- this range's part: O / l and lse = m + ln l per head
   if (ok) {

@@ -79,9 +79,10 @@ __host__ __device__ constexpr GenLayout gen_layout(int bits, int D, int G, bool 
 // CTA, with a 2-stage copy ring, see gen_single_stage) hold, up to a cap.  More CTAs hide more of
 // each CTA's serial chain (copy wait, conversion, QK^T, softmax, PV); the
 // caps are where more stopped paying (measured: 4-head units up to 8, 8-head
-// units 5 -- 4 with 4-bit codes, K channel-wise and V token-wise, whose
-// registers spill at 96 per thread).  The kernel's launch bounds take the same count
-// (never below 4 for 4-head units), so its registers always fit.
+// units 5, whose 96 registers a thread the kernel keeps within by holding the
+// channel-wise K multipliers in shared memory).  The kernel's launch bounds
+// take the same count (never below 4 for 4-head units), so its registers
+// always fit.
 constexpr int kGenSmemPerSm = 228 * 1024, kGenSmemPerCta = 1024;
 // One exception to the 2-stage ring: 4-bit codes with K and V token-wise at
 // head dim 128, groups of 128 (E4M3, 4 heads) run 8 CTAs with one stage
@@ -94,7 +95,7 @@ __host__ __device__ constexpr int gen_ctas_per_sm(int bits, int D, int G, bool k
   const int t = 512 / gen_layout(bits, D, G, kcw, vcw, bf16, nh, 2).tmem_cols;
   const int st = gen_single_stage(bits, D, G, kcw, vcw, bf16, nh) ? 1 : 2;
   const int m = kGenSmemPerSm / (gen_layout(bits, D, G, kcw, vcw, bf16, nh, st).total_bytes + kGenSmemPerCta);
-  const int cap = nh > 4 ? (bits == 4 && kcw && !vcw ? 4 : 5) : 8;
+  const int cap = nh > 4 ? 5 : 8;
   const int c = t < m ? t : m;
   return c < cap ? c : cap;
 }

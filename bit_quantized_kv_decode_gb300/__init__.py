@@ -14,16 +14,16 @@ import torch
 
 from . import _lib
 from ._lib import (CHANNELWISE, DEV_BAD_PAGE, DEV_BAD_SEQ_LEN, DEV_NONFINITE, DEV_TIMEOUT, FLAG_E2M1_V, FLAG_TEST_STALL,
-                   OPERANDS_BF16, OPERANDS_FP8, TOKENWISE, AttnDesc, CacheDesc, KvqError)
+                   FLAG_TEST_STALL_MMA, OPERANDS_BF16, OPERANDS_FP8, TOKENWISE, AttnDesc, CacheDesc, KvqError)
 
 BLOCK_TOKENS = 128
 HEAD_DIM = 128
 GROUP_Q = 4
 
 __all__ = ["CacheDesc", "AttnDesc", "KvqError", "TOKENWISE", "CHANNELWISE", "OPERANDS_FP8", "OPERANDS_BF16",
-           "DEV_BAD_SEQ_LEN", "DEV_BAD_PAGE", "DEV_NONFINITE", "DEV_TIMEOUT", "FLAG_TEST_STALL", "FLAG_E2M1_V", "cache_desc",
-           "attn_desc", "cache_bytes", "block_bytes", "sz_per_block", "alloc_cache", "pack", "append", "dequant", "workspace_size",
-           "decode_attn", "decode_attn_static", "merge", "library"]
+           "DEV_BAD_SEQ_LEN", "DEV_BAD_PAGE", "DEV_NONFINITE", "DEV_TIMEOUT", "FLAG_TEST_STALL", "FLAG_TEST_STALL_MMA",
+           "FLAG_E2M1_V", "cache_desc", "attn_desc", "cache_bytes", "block_bytes", "sz_per_block", "alloc_cache", "pack",
+           "append", "dequant", "workspace_size", "decode_attn", "decode_attn_static", "merge", "library"]
 
 
 def library() -> ctypes.CDLL:

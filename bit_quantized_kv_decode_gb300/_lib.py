@@ -20,6 +20,7 @@ CHANNELWISE = 1
 OPERANDS_FP8 = 0
 OPERANDS_BF16 = 1
 FLAG_TEST_STALL = 0x1
+FLAG_TEST_STALL_MMA = 0x4
 FLAG_E2M1_V = 0x2
 PATH_SPECIALISED = 0
 PATH_GENERAL = 1

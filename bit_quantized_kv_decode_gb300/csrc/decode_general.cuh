@@ -397,7 +397,10 @@ decode_general_kernel(const GenParams p, int stages) {
   if (tid == 0) {  // the first copies go out before the rest of the set-up
     for (int i = 0; i < 4; ++i) pend[i] = -1;
     *fail = 0;
-    for (int i = 0; i < stages + 2; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < stages; ++i) mbar_init(&bars[i], 1);
+    // test hook: this CTA's MMA barrier takes two signals a phase, so its first QK^T wait runs out
+    mbar_init(&bars[stages], ((p.flags & KVQ_FLAG_TEST_STALL_MMA) && cta == 0) ? 2u : 1u);
+    mbar_init(&bars[stages + 1], 1);
     fence_barrier_init();
     for (int i = 0; i < stages && j0 + i < j1; ++i) {
       if (i == 0 && (p.flags & KVQ_FLAG_TEST_STALL) && blockIdx.x == 0) continue;  // test hook: withhold one block

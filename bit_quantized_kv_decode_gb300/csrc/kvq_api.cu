@@ -119,7 +119,8 @@ kvq_status check_attn(const kvq_attn_desc* d) {
   if (d->batch > kMaxBatchDecode) return KVQ_ERR_UNSUPPORTED;
   if (heads_per_kv(d) == 0) return KVQ_ERR_UNSUPPORTED;  // 1, 2, 4 or 8 query heads per KV head
   if (d->operand_mode != KVQ_OPERANDS_FP8 && d->operand_mode != KVQ_OPERANDS_BF16) return KVQ_ERR_INVALID_ARG;
-  if (d->num_ctas < 0 || (d->flags & ~(KVQ_FLAG_TEST_STALL | KVQ_FLAG_E2M1_V)) != 0) return KVQ_ERR_INVALID_ARG;
+  if (d->num_ctas < 0 || (d->flags & ~(KVQ_FLAG_TEST_STALL | KVQ_FLAG_TEST_STALL_MMA | KVQ_FLAG_E2M1_V)) != 0)
+    return KVQ_ERR_INVALID_ARG;
   if ((d->flags & KVQ_FLAG_E2M1_V) &&
       (d->cache.bits != 2 || d->operand_mode != KVQ_OPERANDS_FP8 || heads_per_kv(d) != kGroupQ))
     return KVQ_ERR_UNSUPPORTED;  // the E2M1 placement is built for these only
@@ -236,7 +237,8 @@ kvq_status decode_general(const kvq_attn_desc* desc, const uint16_t* q, const ui
   p.n_floor = plan.n_floor;
   p.sm_scale_log2 = sm_scale * 1.4426950408889634f;
   p.flags = desc->flags;
-  p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
+  p.wait_limit_ns =
+      (desc->flags & (KVQ_FLAG_TEST_STALL | KVQ_FLAG_TEST_STALL_MMA)) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
   p.nibble_mul = 1u << 28;
   p.minus_one = 0xffffffffu;
   const int grid = (int)plan.slots;
@@ -343,7 +345,8 @@ kvq_status decode_attn_bounded(const kvq_attn_desc* desc, const uint16_t* q, con
   p.flags = desc->flags;
   p.nibble_mul = 1u << 28;
   p.minus_one = 0xffffffffu;
-  p.wait_limit_ns = (desc->flags & KVQ_FLAG_TEST_STALL) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
+  p.wait_limit_ns =
+      (desc->flags & (KVQ_FLAG_TEST_STALL | KVQ_FLAG_TEST_STALL_MMA)) ? 50ull * 1000 * 1000 : 2ull * 1000 * 1000 * 1000;
 #ifdef KVQ_PROFILE
   p.prof = g_prof_counters;
 #endif

@@ -117,6 +117,12 @@ typedef struct kvq_attn_desc {
 /* Test hook: the loader withholds one tile so that every waiting stage runs
  * into its time limit; the call must end with KVQ_DEV_TIMEOUT set. */
 #define KVQ_FLAG_TEST_STALL 0x1u
+/* Test hook (general kernel; the specialised kernel ignores it): the first
+ * CTA's MMA completion barrier waits for two signals a phase, so the wait
+ * for its first QK^T product (per warp with token-wise K, CTA-wide with
+ * channel-wise K) runs into its time limit; the call must end with
+ * KVQ_DEV_TIMEOUT set. */
+#define KVQ_FLAG_TEST_STALL_MMA 0x4u
 /* 2-bit caches: feed the V codes to the tensor cores as E2M1 values
  * (code / 2, two 2-bit fields per nibble taken with one mask each) staged in
  * shared memory -- the placement of the rag-lover.com summary of arXiv

@@ -107,8 +107,10 @@ def test_e2m1_flag_validation(lib):
               _lib.AttnDesc(_cache(2, 1, 0), 8, 64, 32, 0, 0.0, 304, _lib.FLAG_E2M1_V),   # 8 query heads per KV head
               _lib.AttnDesc(_cache(2, 1, 0), 8, 16, 32, 0, 0.0, 304, _lib.FLAG_E2M1_V)):  # 2 query heads per KV head
         assert lib.kvq_decode_workspace_size(ctypes.byref(d), ctypes.byref(n)) == 2
-    bad = _lib.AttnDesc(_cache(2, 1, 0), 8, 32, 32, 0, 0.0, 304, 0x4)  # unknown flag bit
+    bad = _lib.AttnDesc(_cache(2, 1, 0), 8, 32, 32, 0, 0.0, 304, 0x8)  # unknown flag bit
     assert lib.kvq_decode_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 1
+    hook = _lib.AttnDesc(_cache(2, 1, 0), 8, 32, 32, 0, 0.0, 304, _lib.FLAG_TEST_STALL_MMA)  # the MMA stall test hook
+    assert lib.kvq_decode_workspace_size(ctypes.byref(hook), ctypes.byref(n)) == 0
 
 
 def _general_ws(batch, units, splits, gq, head_dim):

@@ -110,6 +110,23 @@ def test_decode_geometry_stall_reports_timeout():
     assert_attention_close(pb, res, 0)
 
 
+@pytest.mark.parametrize("D,G,bits,ks,vs", [(256, 64, 4, 0, 1), (128, 32, 2, 0, 0), (64, 32, 4, 1, 0)])
+def test_decode_geometry_mma_stall_reports_timeout(D, G, bits, ks, vs):
+    """The MMA stall hook: the first CTA's MMA barrier waits for two signals a
+    phase, so its first QK^T wait runs out (per warp with token-wise K, the
+    failure read at the next CTA barrier; CTA-wide with channel-wise K): the
+    call returns with the timeout bit set, nothing hangs, and the next call
+    is correct."""
+    import bit_quantized_kv_decode_gb300 as kvq
+    w = _w(D, G, bits, ks, vs, B=2, Hkv=1, Hq=4, L=700)
+    pb = make_problem(w, 5 + D + G, lens=[700, 300])
+    res = run_gpu(pb, flags=kvq.FLAG_TEST_STALL_MMA)
+    assert res["status"] & kvq.DEV_TIMEOUT
+    res = run_gpu(pb)
+    assert res["status"] == 0
+    assert_attention_close(pb, res, 0)
+
+
 def test_decode_geometry_e2m1_unsupported():
     """The E2M1 V placement is built for head dim 128 with groups of 128 only."""
     import bit_quantized_kv_decode_gb300 as kvq

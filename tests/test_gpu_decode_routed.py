@@ -64,3 +64,19 @@ def test_general_kernel_default_geometry_stall_reports_timeout(bits, kcw, vcw):
     again = run_gpu(pb)
     assert again["status"] == 0
     assert_attention_close(pb, again, 0)
+
+
+@pytest.mark.parametrize("bits,kcw,vcw,gq", [(2, 0, 0, 4), (4, 0, 1, 4), (4, 0, 0, 8), (4, 1, 0, 4)])
+def test_general_kernel_default_geometry_mma_stall_reports_timeout(bits, kcw, vcw, gq):
+    """A QK^T completion that never signals (test hook: the first CTA's MMA
+    barrier waits for two signals a phase) makes the waits for it run out --
+    per warp with token-wise K, the failure kept in shared memory and read at
+    the next CTA barrier; CTA-wide with channel-wise K: the call returns with
+    KVQ_DEV_TIMEOUT set, nothing hangs, and the next call is correct."""
+    import bit_quantized_kv_decode_gb300 as kvq
+    pb = make_problem(_workload(bits, kcw, vcw, gq), seed=980 + bits + 2 * vcw + gq, lens=LENS)
+    res = run_gpu(pb, flags=kvq.FLAG_TEST_STALL_MMA)
+    assert res["status"] & kvq.DEV_TIMEOUT
+    again = run_gpu(pb)
+    assert again["status"] == 0
+    assert_attention_close(pb, again, 0)
